@@ -1,0 +1,604 @@
+/*
+ * CPU oracle for hash-blocked TSDF integration.  TEST INFRASTRUCTURE ONLY:
+ * the tests, the smoke check and the benchmark's CPU-baseline leg may call
+ * it; the product path never does.  It shares no code, header, table or
+ * constant with the CUDA path.
+ *
+ * What it restates (from "What Irregularity Costs: CUDA C++, Rust, and
+ * Triton on a Hash-Blocked GPU Workload", arXiv 2608.08287):
+ *
+ *   - design section, data structure: the volume is cut into blocks of
+ *     8^3 = 512 voxels; each block holds five per-voxel quantities (signed
+ *     distance, weight, three colour channels);
+ *   - design section, integration: two passes over the same back-projected
+ *     points.  The first (allocate) walks each point's truncation band and
+ *     makes sure every block it touches exists; the second (update) walks the
+ *     same band and adds each observation into its voxel;
+ *   - design section, accumulation: the arrays hold weighted SUMS, not
+ *     running means, so the mean is only formed at read-out;
+ *   - design section, occlusion: one occlusion test, applied identically in
+ *     both passes;
+ *   - correctness section (analytic tier): the signed distance is evaluated
+ *     at the voxel centre, not at the ray sample that selected the voxel.
+ *
+ * Where the page is silent this file takes the following readings (they are
+ * listed with their reasons in the design notes of the repository):
+ *   - pinhole camera, pixel centres at integer (u, v), x right, y down,
+ *     z forward; pose = camera-to-world [R | t], R row-major;
+ *   - the band is walked along the unit ray through the observed point, in
+ *     steps of one voxel, S = 2k + 1 samples at offsets (i - k) * voxel with
+ *     k = round(trunc / voxel);
+ *   - projective signed distance at the voxel centre: sdf = d - z_c, where z_c
+ *     is the camera-frame depth of the centre and d the pixel's depth;
+ *   - occlusion test: z_c > 0 and sdf >= -trunc;
+ *   - value added: tsdf = min(1, sdf / trunc), weight 1, the pixel's colour;
+ *   - voxel order inside a block: x fastest, j = lx + 8 ly + 64 lz;
+ *   - block coordinates must lie in [-2^20, 2^20 - 1] on every axis (the
+ *     range of the packed 21-bit key); samples outside are counted, skipped.
+ *
+ * Arithmetic: the walk is float32 with one rounding per written operation,
+ * evaluated in the order written (the library is compiled with
+ * -ffp-contract=off and without fast-math), so that the voxel each sample
+ * selects is defined to the bit.  The sums are accumulated in double, i.e.
+ * they are the exact sums of the float32 terms up to double rounding.
+ *
+ * The blocks live in a std::unordered_map keyed by block coordinate; the
+ * oracle never uses the packed key or the hash table.  The key packing, the
+ * multiply-xor slot hash and a sequential linear-probing table are restated
+ * separately at the end of this file, as a reference for the table's
+ * structure (occupied slots, displacement), not as part of integration.
+ */
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <memory>
+#include <unordered_map>
+#include <unordered_set>
+#include <vector>
+
+/* Planted mistakes for the self-test of the pins.  Every normal build has
+ * ORACLE_MUTANT == 0; the test suite compiles throw-away variants with one
+ * mistake each and checks that some pin rejects every one of them. */
+#ifndef ORACLE_MUTANT
+#define ORACLE_MUTANT 0
+#endif
+
+namespace {
+
+const int kEdge = 8;                 // voxels per block edge
+const int kBlockVoxels = 512;        // 8^3
+const int32_t kCoordMin = -(1 << 20);
+const int32_t kCoordMax = (1 << 20) - 1;
+
+struct BlockCoord {
+    int32_t x, y, z;
+};
+
+bool operator==(const BlockCoord& a, const BlockCoord& b)
+{
+    return a.x == b.x && a.y == b.y && a.z == b.z;
+}
+
+bool operator<(const BlockCoord& a, const BlockCoord& b)
+{
+    if (a.x != b.x) return a.x < b.x;
+    if (a.y != b.y) return a.y < b.y;
+    return a.z < b.z;
+}
+
+struct BlockCoordHash {
+    size_t operator()(const BlockCoord& c) const noexcept
+    {
+        size_t h = std::hash<int32_t>()(c.x);
+        h = h * 1000003u + std::hash<int32_t>()(c.y);
+        h = h * 1000003u + std::hash<int32_t>()(c.z);
+        return h;
+    }
+};
+
+/* Exact-as-possible per-voxel sums of one block.  tsdf_abs is the sum of
+ * |tsdf| over the same terms, kept so a test can bound the float32 rounding
+ * error of any summation order. */
+struct BlockSums {
+    double tsdf[kBlockVoxels];
+    double weight[kBlockVoxels];
+    double r[kBlockVoxels];
+    double g[kBlockVoxels];
+    double b[kBlockVoxels];
+    double tsdf_abs[kBlockVoxels];
+};
+
+struct Camera {
+    float fx, fy, cx, cy;
+    float R[3][3];   // camera-to-world rotation, row-major
+    float t[3];      // camera position in the world
+};
+
+enum SampleStatus { SAMPLE_PASS = 0, SAMPLE_OCCLUDED = 1, SAMPLE_OUT_OF_RANGE = 2 };
+
+struct Sample {
+    int32_t ix, iy, iz;   // voxel index
+    float tsdf;
+};
+
+/* floor(a / 8) for any int32 a, written without shifts. */
+int32_t floor_div8(int32_t a)
+{
+#if ORACLE_MUTANT == 9
+    return a / kEdge;                       // planted: truncates toward zero
+#else
+    int32_t q = a / kEdge;
+    if (a % kEdge != 0 && a < 0) q -= 1;
+    return q;
+#endif
+}
+
+/* One sample of the truncation band: the point on the unit ray at signed
+ * offset `off` from the observed point p, its voxel, and the truncated
+ * signed distance at that voxel's centre. */
+SampleStatus band_sample(const Camera& cam, float voxel, float trunc, float d,
+                         float px, float py, float pz, float dx, float dy, float dz,
+                         float off, Sample* s)
+{
+    // sample point, camera frame
+    float sx = px + off * dx;
+    float sy = py + off * dy;
+    float sz = pz + off * dz;
+    // to the world frame: w = R s + t
+    float wx = ((cam.R[0][0] * sx + cam.R[0][1] * sy) + cam.R[0][2] * sz) + cam.t[0];
+    float wy = ((cam.R[1][0] * sx + cam.R[1][1] * sy) + cam.R[1][2] * sz) + cam.t[1];
+    float wz = ((cam.R[2][0] * sx + cam.R[2][1] * sy) + cam.R[2][2] * sz) + cam.t[2];
+    // voxel index = floor(w / voxel), kept inside the packable block range
+#if ORACLE_MUTANT == 8
+    float qx = std::trunc(wx / voxel), qy = std::trunc(wy / voxel), qz = std::trunc(wz / voxel);
+#else
+    float qx = std::floor(wx / voxel), qy = std::floor(wy / voxel), qz = std::floor(wz / voxel);
+#endif
+    const float lo = (float)kCoordMin * kEdge;           // -2^23
+    const float hi = (float)(kCoordMax * kEdge + (kEdge - 1));  // 2^23 - 1
+    if (!(qx >= lo && qx <= hi && qy >= lo && qy <= hi && qz >= lo && qz <= hi))
+        return SAMPLE_OUT_OF_RANGE;
+    s->ix = (int32_t)qx;
+    s->iy = (int32_t)qy;
+    s->iz = (int32_t)qz;
+    // the voxel centre, moved to the camera origin ...
+#if ORACLE_MUTANT == 3
+    float cxw = ((float)s->ix) * voxel - cam.t[0];      // planted: corner, not centre
+    float cyw = ((float)s->iy) * voxel - cam.t[1];
+    float czw = ((float)s->iz) * voxel - cam.t[2];
+#else
+    float cxw = ((float)s->ix + 0.5f) * voxel - cam.t[0];
+    float cyw = ((float)s->iy + 0.5f) * voxel - cam.t[1];
+    float czw = ((float)s->iz + 0.5f) * voxel - cam.t[2];
+#endif
+    // ... and its camera-frame depth z_c = (R^T c)_z = column 2 of R dotted with c
+#if ORACLE_MUTANT == 4
+    float zc = (cam.R[2][0] * cxw + cam.R[2][1] * cyw) + cam.R[2][2] * czw;  // planted: R not transposed
+#else
+    float zc = (cam.R[0][2] * cxw + cam.R[1][2] * cyw) + cam.R[2][2] * czw;
+#endif
+    // projective signed distance at the centre (positive in front of the surface)
+#if ORACLE_MUTANT == 1
+    float sdf = d - sz;                     // planted: distance at the sample, not the centre
+#elif ORACLE_MUTANT == 2
+    float sdf = zc - d;                     // planted: sign flipped
+#else
+    float sdf = d - zc;
+#endif
+    // occlusion test
+#if ORACLE_MUTANT == 6
+    if (!(zc > 0.0f)) return SAMPLE_OCCLUDED;            // planted: no truncation side test
+#else
+    if (!(zc > 0.0f && sdf >= -trunc)) return SAMPLE_OCCLUDED;
+#endif
+#if ORACLE_MUTANT == 7
+    s->tsdf = sdf / trunc;                  // planted: no clamp at +1
+#else
+    s->tsdf = std::fmin(1.0f, sdf / trunc);
+#endif
+    return SAMPLE_PASS;
+}
+
+/* Walk the truncation band of pixel (u, v) with depth d, calling
+ * visit(status, sample) once per band sample.  Returns false (and visits
+ * nothing) for an invalid pixel. */
+template <class Visit>
+bool walk_pixel(const Camera& cam, float voxel, float trunc, int band_half,
+                int u, int v, float d, Visit visit)
+{
+    if (!(std::isfinite(d) && d > 0.0f)) return false;
+    // back-project the pixel: p = d * ((u - cx) / fx, (v - cy) / fy, 1)
+    float xn = ((float)u - cam.cx) / cam.fx;
+    float yn = ((float)v - cam.cy) / cam.fy;
+    float px = xn * d, py = yn * d, pz = d;
+    // unit ray direction through the pixel
+    float len = std::sqrt((xn * xn + yn * yn) + 1.0f);
+#if ORACLE_MUTANT == 14
+    float dx = xn, dy = yn, dz = 1.0f;      // planted: ray not normalised
+    (void)len;
+#else
+    float dx = xn / len, dy = yn / len, dz = 1.0f / len;
+#endif
+#if ORACLE_MUTANT == 13
+    int steps_half = band_half + 1;         // planted: band one voxel too wide
+#else
+    int steps_half = band_half;
+#endif
+    for (int i = -steps_half; i <= steps_half; ++i) {
+        float off = (float)i * voxel;
+        Sample s;
+        SampleStatus st = band_sample(cam, voxel, trunc, d, px, py, pz, dx, dy, dz, off, &s);
+        visit(st, s);
+    }
+    return true;
+}
+
+struct Volume {
+    float voxel;
+    float trunc;
+    int band_half;           // k: samples at offsets -k..k voxels
+    long long block_limit;   // < 0: no pool limit
+
+    bool keep_all = true;    // false: sums are kept only for blocks in `keep`
+    std::unordered_set<BlockCoord, BlockCoordHash> keep;
+
+    // every allocated block; the sums pointer is null when not kept
+    std::unordered_map<BlockCoord, std::unique_ptr<BlockSums>, BlockCoordHash> blocks;
+    // keys that found the pool full (each counted once)
+    std::unordered_set<BlockCoord, BlockCoordHash> dropped;
+
+    unsigned long long valid_points = 0;          // pixels with finite depth > 0
+    unsigned long long passing_samples = 0;       // samples that pass the occlusion test
+    unsigned long long accumulated = 0;           // passing samples added into a block
+    unsigned long long missed_contributions = 0;  // passing samples whose block is absent
+    unsigned long long out_of_range_samples = 0;  // samples outside the key range
+    unsigned long long dropped_blocks = 0;        // distinct keys refused for lack of pool
+    unsigned long long bad_local_index = 0;       // self-check: local index outside [0, 512)
+};
+
+BlockCoord block_of(const Sample& s)
+{
+    return BlockCoord{floor_div8(s.ix), floor_div8(s.iy), floor_div8(s.iz)};
+}
+
+int local_index(const Sample& s, const BlockCoord& b)
+{
+    int lx = s.ix - kEdge * b.x, ly = s.iy - kEdge * b.y, lz = s.iz - kEdge * b.z;
+#if ORACLE_MUTANT == 5
+    return lz + kEdge * ly + kEdge * kEdge * lx;   // planted: x slowest
+#else
+    return lx + kEdge * ly + kEdge * kEdge * lz;
+#endif
+}
+
+Camera make_camera(const float K[4], const float pose[16])
+{
+    Camera c;
+    c.fx = K[0];
+    c.fy = K[1];
+    c.cx = K[2];
+    c.cy = K[3];
+    for (int r = 0; r < 3; ++r) {
+        for (int k = 0; k < 3; ++k) c.R[r][k] = pose[4 * r + k];
+        c.t[r] = pose[4 * r + 3];
+    }
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+/* ------------------------------------------------------------------------
+ * Integration
+ * --------------------------------------------------------------------- */
+
+void* oracle_create(float voxel_size, float trunc, long long block_limit)
+{
+    if (!(voxel_size > 0.0f) || !(trunc > 0.0f) || !std::isfinite(voxel_size) ||
+        !std::isfinite(trunc))
+        return nullptr;
+    Volume* v = new Volume();
+    v->voxel = voxel_size;
+    v->trunc = trunc;
+    v->band_half = (int)std::lround((double)trunc / (double)voxel_size);
+    v->block_limit = block_limit;
+    return v;
+}
+
+void oracle_destroy(void* h) { delete static_cast<Volume*>(h); }
+
+/* Keep sums only for the listed blocks (coords: n x 3).  The block set and
+ * all counters are still tracked for every block. */
+int oracle_keep_only(void* h, const int32_t* coords, long long n)
+{
+    Volume* v = static_cast<Volume*>(h);
+    if (!v->blocks.empty()) return -1;
+    v->keep_all = false;
+    for (long long i = 0; i < n; ++i)
+        v->keep.insert(BlockCoord{coords[3 * i], coords[3 * i + 1], coords[3 * i + 2]});
+    return 0;
+}
+
+/* Integrate one frame: depth float32 [H][W] (metres, 0 = invalid),
+ * rgb float32 [H][W][3], K = {fx, fy, cx, cy}, pose = row-major 4x4
+ * camera-to-world. */
+int oracle_integrate(void* h, const float* depth, const float* rgb, int W, int H,
+                     const float K[4], const float pose[16])
+{
+    Volume* v = static_cast<Volume*>(h);
+    if (W <= 0 || H <= 0) return -1;
+    const Camera cam = make_camera(K, pose);
+
+    // Pass 1, allocate: every block touched by a passing sample exists
+    // afterwards (unless the pool limit refuses it).
+    for (int py = 0; py < H; ++py) {
+        for (int px = 0; px < W; ++px) {
+            float d = depth[(size_t)py * W + px];
+            walk_pixel(cam, v->voxel, v->trunc, v->band_half, px, py, d,
+                       [&](SampleStatus st, const Sample& s) {
+                if (st == SAMPLE_OUT_OF_RANGE) {
+                    v->out_of_range_samples++;
+                    return;
+                }
+                bool allocate = (st == SAMPLE_PASS);
+#if ORACLE_MUTANT == 12
+                allocate = true;                   // planted: allocate ignores occlusion
+#endif
+                if (!allocate) return;
+                BlockCoord b = block_of(s);
+                if (v->blocks.count(b) || v->dropped.count(b)) return;
+                if (v->block_limit >= 0 && (long long)v->blocks.size() >= v->block_limit) {
+                    v->dropped.insert(b);
+                    v->dropped_blocks++;
+                    return;
+                }
+                std::unique_ptr<BlockSums> sums;
+                if (v->keep_all || v->keep.count(b)) {
+                    sums.reset(new BlockSums);
+                    std::memset(sums.get(), 0, sizeof(BlockSums));
+                }
+                v->blocks.emplace(b, std::move(sums));
+            });
+        }
+    }
+
+    // Pass 2, update: add (tsdf, 1, r, g, b) of every passing sample into
+    // its voxel's sums.
+    for (int py = 0; py < H; ++py) {
+        for (int px = 0; px < W; ++px) {
+            size_t pix = (size_t)py * W + px;
+            float d = depth[pix];
+            float cr = rgb[3 * pix + 0], cg = rgb[3 * pix + 1], cb = rgb[3 * pix + 2];
+#if ORACLE_MUTANT == 10
+            std::swap(cr, cb);                     // planted: red and blue swapped
+#endif
+            bool valid = walk_pixel(cam, v->voxel, v->trunc, v->band_half, px, py, d,
+                                    [&](SampleStatus st, const Sample& s) {
+                if (st != SAMPLE_PASS) return;
+                v->passing_samples++;
+                BlockCoord b = block_of(s);
+                auto it = v->blocks.find(b);
+                if (it == v->blocks.end()) {
+                    v->missed_contributions++;
+                    return;
+                }
+                v->accumulated++;
+                BlockSums* sums = it->second.get();
+                if (!sums) return;
+                int j = local_index(s, b);
+                if (j < 0 || j >= kBlockVoxels) {          // cannot happen in a correct build
+                    v->bad_local_index++;
+                    return;
+                }
+                sums->tsdf[j] += (double)s.tsdf;
+                sums->tsdf_abs[j] += std::fabs((double)s.tsdf);
+#if ORACLE_MUTANT == 11
+                sums->weight[j] += 2.0;            // planted: weight 2 per observation
+#else
+                sums->weight[j] += 1.0;
+#endif
+                sums->r[j] += (double)cr;
+                sums->g[j] += (double)cg;
+                sums->b[j] += (double)cb;
+            });
+            if (valid) v->valid_points++;
+        }
+    }
+    return 0;
+}
+
+long long oracle_block_count(void* h) { return (long long)static_cast<Volume*>(h)->blocks.size(); }
+
+/* Counters, in this order: valid_points, passing_samples, accumulated,
+ * missed_contributions, out_of_range_samples, dropped_blocks,
+ * bad_local_index. */
+void oracle_counters(void* h, unsigned long long out[7])
+{
+    Volume* v = static_cast<Volume*>(h);
+    out[0] = v->valid_points;
+    out[1] = v->passing_samples;
+    out[2] = v->accumulated;
+    out[3] = v->missed_contributions;
+    out[4] = v->out_of_range_samples;
+    out[5] = v->dropped_blocks;
+    out[6] = v->bad_local_index;
+}
+
+/* Every allocated block coordinate, sorted by (x, y, z).  Returns the count
+ * written (at most max_n). */
+long long oracle_export_coords(void* h, long long max_n, int32_t* coords)
+{
+    Volume* v = static_cast<Volume*>(h);
+    std::vector<BlockCoord> all;
+    all.reserve(v->blocks.size());
+    for (const auto& kv : v->blocks) all.push_back(kv.first);
+    std::sort(all.begin(), all.end());
+    long long n = std::min<long long>(max_n, (long long)all.size());
+    for (long long i = 0; i < n; ++i) {
+        coords[3 * i] = all[i].x;
+        coords[3 * i + 1] = all[i].y;
+        coords[3 * i + 2] = all[i].z;
+    }
+    return n;
+}
+
+/* Blocks whose sums are kept, sorted by (x, y, z), with their six per-voxel
+ * arrays ([n][512] each; any pointer may be null to skip that array). */
+long long oracle_export_sums(void* h, long long max_n, int32_t* coords, double* tsdf,
+                             double* weight, double* r, double* g, double* b,
+                             double* tsdf_abs)
+{
+    Volume* v = static_cast<Volume*>(h);
+    std::vector<std::pair<BlockCoord, const BlockSums*>> kept;
+    for (const auto& kv : v->blocks)
+        if (kv.second) kept.emplace_back(kv.first, kv.second.get());
+    std::sort(kept.begin(), kept.end(),
+              [](const std::pair<BlockCoord, const BlockSums*>& a,
+                 const std::pair<BlockCoord, const BlockSums*>& c) { return a.first < c.first; });
+    long long n = std::min<long long>(max_n, (long long)kept.size());
+    const size_t bytes = sizeof(double) * kBlockVoxels;
+    for (long long i = 0; i < n; ++i) {
+        const BlockSums* s = kept[i].second;
+        coords[3 * i] = kept[i].first.x;
+        coords[3 * i + 1] = kept[i].first.y;
+        coords[3 * i + 2] = kept[i].first.z;
+        if (tsdf) std::memcpy(tsdf + i * kBlockVoxels, s->tsdf, bytes);
+        if (weight) std::memcpy(weight + i * kBlockVoxels, s->weight, bytes);
+        if (r) std::memcpy(r + i * kBlockVoxels, s->r, bytes);
+        if (g) std::memcpy(g + i * kBlockVoxels, s->g, bytes);
+        if (b) std::memcpy(b + i * kBlockVoxels, s->b, bytes);
+        if (tsdf_abs) std::memcpy(tsdf_abs + i * kBlockVoxels, s->tsdf_abs, bytes);
+    }
+    return n;
+}
+
+long long oracle_kept_count(void* h)
+{
+    Volume* v = static_cast<Volume*>(h);
+    long long n = 0;
+    for (const auto& kv : v->blocks)
+        if (kv.second) ++n;
+    return n;
+}
+
+/* ------------------------------------------------------------------------
+ * Packed key, slot hash and a sequential linear-probing table: a reference
+ * for the hash table's structure ("What Irregularity Costs", design section,
+ * data structure: 64-bit key with each block axis biased by 2^20 into 21
+ * bits; open addressing, linear probing; multiply-xor hash).
+ * --------------------------------------------------------------------- */
+
+/* Key layout (a reading; the page's formula did not survive): x in bits
+ * 0-20, y in bits 21-41, z in bits 42-62, each stored as coordinate + 2^20.
+ * Bit 63 is always zero, so the all-ones word can mark an empty slot.
+ * Returns 0 and writes *key for an in-range coordinate, -1 otherwise. */
+int oracle_pack_key(int32_t x, int32_t y, int32_t z, uint64_t* key)
+{
+    const int64_t bias = (int64_t)1 << 20;
+    int64_t c[3] = {x, y, z};
+    uint64_t out = 0;
+    for (int a = 0; a < 3; ++a) {
+        int64_t biased = c[a] + bias;
+        if (biased < 0 || biased >= ((int64_t)1 << 21)) return -1;
+        out += (uint64_t)biased * ((uint64_t)1 << (21 * a));
+    }
+    *key = out;
+    return 0;
+}
+
+/* Inverse of oracle_pack_key; -1 if bit 63 is set. */
+int oracle_unpack_key(uint64_t key, int32_t out[3])
+{
+    if (key >> 63) return -1;
+    const int64_t bias = (int64_t)1 << 20;
+    for (int a = 0; a < 3; ++a) {
+        uint64_t field = (key / ((uint64_t)1 << (21 * a))) % ((uint64_t)1 << 21);
+        out[a] = (int32_t)((int64_t)field - bias);
+    }
+    return 0;
+}
+
+/* Home slot of a key in a table of T = 2^m slots (a reading; the page names
+ * a multiply-xor hash but not its constants): the 64-bit finalizer of
+ * SplitMix64 (Steele, Lea and Flood, "Fast splittable pseudorandom number
+ * generators", OOPSLA 2014) -- xor-shift, multiply, xor-shift, multiply,
+ * xor-shift -- then the low m bits.  Every step is a bijection on 64-bit
+ * words, and every output bit depends on every key bit, so neighbouring
+ * block coordinates spread over the whole table. */
+uint64_t oracle_hash_slot(uint64_t key, uint64_t table_size)
+{
+    uint64_t z = key;
+    z = z ^ (z >> 30);
+    z = z * 0xBF58476D1CE4E5B9ull;        // modulo 2^64
+    z = z ^ (z >> 27);
+    z = z * 0x94D049BB133111EBull;
+    z = z ^ (z >> 31);
+    return z % table_size;                // table_size is a power of two
+}
+
+/* Insert keys[0..n) one after another into an empty table of T slots with
+ * linear probing.  A key already present is found, not inserted again.
+ * table_out[T]: the key in each slot, or all-ones for an empty slot.
+ * probe_len[i]: slots examined by the i-th insert (1 = its home slot).
+ * *total_displacement: sum over distinct keys of (final slot - home) mod T.
+ * Returns the number of distinct keys, or -1 if the table filled up. */
+long long oracle_probe_build(const uint64_t* keys, long long n, uint64_t table_size,
+                             uint64_t* table_out, long long* probe_len,
+                             long long* total_displacement)
+{
+    const uint64_t empty = ~(uint64_t)0;
+    for (uint64_t s = 0; s < table_size; ++s) table_out[s] = empty;
+    long long distinct = 0;
+    long long disp = 0;
+    for (long long i = 0; i < n; ++i) {
+        uint64_t home = oracle_hash_slot(keys[i], table_size);
+        uint64_t slot = home;
+        long long examined = 1;
+        while (table_out[slot] != empty && table_out[slot] != keys[i]) {
+            slot = (slot + 1) % table_size;
+            ++examined;
+            if ((uint64_t)examined > table_size) return -1;
+        }
+        if (table_out[slot] == empty) {
+            table_out[slot] = keys[i];
+            ++distinct;
+            disp += (long long)((slot + table_size - home) % table_size);
+        }
+        if (probe_len) probe_len[i] = examined;
+    }
+    if (total_displacement) *total_displacement = disp;
+    return distinct;
+}
+
+/* Block coordinates whose home slot lies in [window_start, window_start +
+ * window_len) of a T-slot table: scans the cube origin + [0, side)^3 in
+ * x-fastest raster order and keeps the first `want` hits (coords_out: want
+ * x 3).  Returns the number found. */
+long long oracle_clustered_coords(uint64_t table_size, uint64_t window_start,
+                                  uint64_t window_len, const int32_t origin[3], int32_t side,
+                                  long long want, int32_t* coords_out)
+{
+    long long found = 0;
+    for (int32_t z = 0; z < side && found < want; ++z)
+        for (int32_t y = 0; y < side && found < want; ++y)
+            for (int32_t x = 0; x < side && found < want; ++x) {
+                uint64_t key;
+                int32_t c[3] = {origin[0] + x, origin[1] + y, origin[2] + z};
+                if (oracle_pack_key(c[0], c[1], c[2], &key) != 0) continue;
+                uint64_t slot = oracle_hash_slot(key, table_size);
+                uint64_t rel = (slot + table_size - window_start) % table_size;
+                if (rel < window_len) {
+                    coords_out[3 * found] = c[0];
+                    coords_out[3 * found + 1] = c[1];
+                    coords_out[3 * found + 2] = c[2];
+                    ++found;
+                }
+            }
+    return found;
+}
+
+int oracle_mutant_id(void) { return ORACLE_MUTANT; }
+
+}  // extern "C"
