@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 
-CUDA_SOURCES = ["tsdf_volume.cu", "tsdf_alloc.cu", "tsdf_update.cu", "tsdf_probe.cu"]
+CUDA_SOURCES = ["tsdf_volume.cu", "tsdf_alloc.cu", "tsdf_update.cu", "tsdf_table.cu"]
 CUDA_HEADERS = ["tsdf_device.cuh", "tsdf_internal.h"]
 
 NVCC_FLAGS = [
@@ -95,8 +95,10 @@ def build_tsdf_library(force: bool = False, extra_flags=(), verbose_ptxas: bool 
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(cmds)) as ex:
         logs = list(ex.map(_run, cmds))
     tmp = out + f".tmp{os.getpid()}"
-    _run([nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp] + objs
-         + ["-lcudart"])
+    # cudart is linked statically so the library loads without any search-path
+    # setup; it still shares the process's CUDA context with PyTorch
+    _run([nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-cudart", "static",
+          "-Xcompiler", "-fPIC", "-o", tmp] + objs)
     os.replace(tmp, out)
     if verbose_ptxas:
         print("".join(logs))

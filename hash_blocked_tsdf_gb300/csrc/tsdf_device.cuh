@@ -1,0 +1,200 @@
+// Device building blocks of the integrate path: back-projection, the
+// truncation-band walk with its occlusion test, the packed block key, the
+// slot hash, and the table probe / insert / lookup.
+//
+// Arithmetic of the walk ("What Irregularity Costs", design section,
+// integration; correctness section, analytic tier for the voxel-centre
+// distance): every float operation is spelled with a round-to-nearest
+// intrinsic, so no multiply-add is ever fused and divisions and square
+// roots are IEEE-exact.  The voxel a sample selects is therefore the one any
+// IEEE float32 evaluation of the same operations in the same order selects.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tsdf_internal.h"
+
+namespace tsdf {
+
+enum SampleStatus { kSamplePass = 0, kSampleOccluded = 1, kSampleOutOfRange = 2 };
+
+// A valid pixel's back-projected point p = d * (xn, yn, 1) and the unit ray
+// direction through it.
+struct RayPoint {
+    float d;
+    float px, py, pz;
+    float dx, dy, dz;
+};
+
+struct VoxelSample {
+    int ix, iy, iz;     // voxel index
+    float tsdf;         // min(1, sdf / trunc)
+};
+
+__device__ __forceinline__ bool back_project(const Camera& c, int u, int v, float d,
+                                             RayPoint& p)
+{
+    if (!(isfinite(d) && d > 0.0f)) return false;
+    const float xn = __fdiv_rn(__fsub_rn((float)u, c.cx), c.fx);
+    const float yn = __fdiv_rn(__fsub_rn((float)v, c.cy), c.fy);
+    p.d = d;
+    p.px = __fmul_rn(xn, d);
+    p.py = __fmul_rn(yn, d);
+    p.pz = d;
+    const float len = __fsqrt_rn(__fadd_rn(__fadd_rn(__fmul_rn(xn, xn), __fmul_rn(yn, yn)), 1.0f));
+    p.dx = __fdiv_rn(xn, len);
+    p.dy = __fdiv_rn(yn, len);
+    p.dz = __fdiv_rn(1.0f, len);
+    return true;
+}
+
+// Band sample `i` (offset i * voxel along the unit ray, i in -k..k): its
+// voxel and truncated signed distance at the voxel centre, or the reason it
+// is skipped.  The same function serves the allocate and the update kernels,
+// which is what makes their occlusion decisions identical.
+__device__ __forceinline__ int band_sample(const Camera& c, float voxel, float trunc,
+                                           const RayPoint& p, int i, VoxelSample& s)
+{
+    const float off = __fmul_rn((float)i, voxel);
+    const float sx = __fadd_rn(p.px, __fmul_rn(off, p.dx));
+    const float sy = __fadd_rn(p.py, __fmul_rn(off, p.dy));
+    const float sz = __fadd_rn(p.pz, __fmul_rn(off, p.dz));
+    // world = R s + t, summed left to right
+    const float wx = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r00, sx), __fmul_rn(c.r01, sy)),
+                                         __fmul_rn(c.r02, sz)), c.tx);
+    const float wy = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r10, sx), __fmul_rn(c.r11, sy)),
+                                         __fmul_rn(c.r12, sz)), c.ty);
+    const float wz = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, sx), __fmul_rn(c.r21, sy)),
+                                         __fmul_rn(c.r22, sz)), c.tz);
+    const float qx = floorf(__fdiv_rn(wx, voxel));
+    const float qy = floorf(__fdiv_rn(wy, voxel));
+    const float qz = floorf(__fdiv_rn(wz, voxel));
+    // voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1]
+    const float lo = -8388608.0f, hi = 8388607.0f;
+    if (!(qx >= lo && qx <= hi && qy >= lo && qy <= hi && qz >= lo && qz <= hi))
+        return kSampleOutOfRange;
+    s.ix = (int)qx;
+    s.iy = (int)qy;
+    s.iz = (int)qz;
+    // voxel centre relative to the camera position, then its camera z:
+    // z_c = (R^T (centre - t))_z = r02 * cx + r12 * cy + r22 * cz
+    const float cxr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.ix, 0.5f), voxel), c.tx);
+    const float cyr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iy, 0.5f), voxel), c.ty);
+    const float czr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iz, 0.5f), voxel), c.tz);
+    const float zc = __fadd_rn(__fadd_rn(__fmul_rn(c.r02, cxr), __fmul_rn(c.r12, cyr)),
+                               __fmul_rn(c.r22, czr));
+    const float sdf = __fsub_rn(p.d, zc);
+    // occlusion test: in front of the camera, and not more than one
+    // truncation distance behind the observed surface
+    if (!(zc > 0.0f && sdf >= -trunc)) return kSampleOccluded;
+    s.tsdf = fminf(1.0f, __fdiv_rn(sdf, trunc));
+    return kSamplePass;
+}
+
+// Packed key: block coordinate (voxel index >> 3, an arithmetic shift, i.e.
+// floor division) biased by 2^20 into 21 bits per axis; x in bits 0-20,
+// y in 21-41, z in 42-62.  Bit 63 stays clear, so no key equals kEmptyKey.
+__device__ __forceinline__ unsigned long long block_key(int ix, int iy, int iz)
+{
+    const unsigned long long bx = (unsigned long long)((ix >> 3) + (1 << 20));
+    const unsigned long long by = (unsigned long long)((iy >> 3) + (1 << 20));
+    const unsigned long long bz = (unsigned long long)((iz >> 3) + (1 << 20));
+    return bx | (by << 21) | (bz << 42);
+}
+
+__device__ __forceinline__ unsigned long long pack_block(int bx, int by, int bz)
+{
+    return (unsigned long long)(bx + (1 << 20)) |
+           ((unsigned long long)(by + (1 << 20)) << 21) |
+           ((unsigned long long)(bz + (1 << 20)) << 42);
+}
+
+__device__ __forceinline__ void unpack_block(unsigned long long key, int32_t* out)
+{
+    out[0] = (int32_t)(key & 0x1FFFFFull) - (1 << 20);
+    out[1] = (int32_t)((key >> 21) & 0x1FFFFFull) - (1 << 20);
+    out[2] = (int32_t)((key >> 42) & 0x1FFFFFull) - (1 << 20);
+}
+
+// Voxel offset inside its block, x fastest.
+__device__ __forceinline__ int local_voxel(int ix, int iy, int iz)
+{
+    return (ix & 7) | ((iy & 7) << 3) | ((iz & 7) << 6);
+}
+
+// Slot hash: the SplitMix64 output mix (xor-shift / multiply, twice, then a
+// final xor-shift; Steele, Lea and Flood, OOPSLA 2014), masked to the table.
+__device__ __forceinline__ uint32_t home_slot(unsigned long long key, uint32_t mask)
+{
+    unsigned long long z = key;
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return (uint32_t)z & mask;
+}
+
+enum ProbeResult { kProbeFound = 0, kProbeWon = 1, kProbeOverflow = 2 };
+
+// Find or claim `key` by linear probing from its home slot.  Slots are read
+// with plain (L1-cacheable) loads: a stale EMPTY only costs a failed
+// compare-and-swap that returns the slot's real key, after which the probe
+// carries on; keys are never removed while a kernel runs, so a stale
+// non-empty key is never wrong.  The probe is unbounded up to the table size.
+__device__ __forceinline__ int probe_insert(Entry* table, uint32_t mask, unsigned long long key,
+                                            uint32_t* slot_out, uint32_t* steps_out)
+{
+    uint32_t slot = home_slot(key, mask);
+    uint32_t steps = 1;
+    int res;
+    for (;;) {
+        const unsigned long long k = table[slot].key;
+        if (k == key) {
+            res = kProbeFound;
+            break;
+        }
+        if (k == kEmptyKey) {
+            const unsigned long long old = atomicCAS(&table[slot].key, kEmptyKey, key);
+            if (old == kEmptyKey) {
+                res = kProbeWon;
+                break;
+            }
+            if (old == key) {
+                res = kProbeFound;
+                break;
+            }
+        }
+        if (steps > mask) {           // examined all table_capacity slots
+            res = kProbeOverflow;
+            break;
+        }
+        slot = (slot + 1) & mask;
+        ++steps;
+    }
+    *slot_out = slot;
+    *steps_out = steps;
+    return res;
+}
+
+// Pool index of `key`, or kIndexFailed when the key is absent.  The table is
+// read-only during the update kernel, so whole entries are read through the
+// non-coherent path in one 16-byte load.
+__device__ __forceinline__ uint32_t lookup(const Entry* __restrict__ table, uint32_t mask,
+                                           unsigned long long key)
+{
+    uint32_t slot = home_slot(key, mask);
+    for (uint32_t n = 0; n <= mask; ++n) {
+        const uint4 e = __ldg(reinterpret_cast<const uint4*>(table) + slot);
+        const unsigned long long k = (unsigned long long)e.x | ((unsigned long long)e.y << 32);
+        if (k == key) return e.z;
+        if (k == kEmptyKey) return kIndexFailed;
+        slot = (slot + 1) & mask;
+    }
+    return kIndexFailed;
+}
+
+__device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
+
+}  // namespace tsdf

@@ -1,0 +1,82 @@
+// Internal declarations shared by the libtsdf translation units: the device
+// view of a volume, the per-frame launch parameters, the device counters and
+// the kernel launchers.  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tsdf.h"
+
+namespace tsdf {
+
+constexpr int kBlockEdge = 8;
+constexpr int kBlockVoxels = 512;
+constexpr int kCounterStripes = 32;     // high-rate counters are spread over 32 words
+constexpr unsigned long long kEmptyKey = TSDF_EMPTY_KEY;
+constexpr uint32_t kIndexPending = TSDF_INDEX_PENDING;
+constexpr uint32_t kIndexFailed = TSDF_INDEX_FAILED;
+
+// One hash-table slot: the packed block key, the block's pool index, padding.
+struct __align__(16) Entry {
+    unsigned long long key;
+    uint32_t idx;
+    uint32_t pad;
+};
+static_assert(sizeof(Entry) == 16, "table entries are 16 bytes");
+
+struct DeviceCounters {
+    unsigned long long pool_exhausted;
+    unsigned long long probe_overflow;
+    unsigned long long probe_inserts;
+    unsigned long long probe_steps;
+    unsigned long long probe_max;
+    unsigned long long reserved[3];
+    unsigned long long probe_hist[TSDF_PROBE_HIST_BINS];
+    unsigned long long missed[kCounterStripes];
+    unsigned long long out_of_range[kCounterStripes];
+    unsigned long long valid_points[kCounterStripes];
+    unsigned long long voxel_updates[kCounterStripes];
+};
+
+// Camera intrinsics and camera-to-world pose, by value in every launch.
+struct Camera {
+    float fx, fy, cx, cy;
+    float r00, r01, r02, r10, r11, r12, r20, r21, r22;   // R, row-major
+    float tx, ty, tz;                                   // t
+};
+
+// Everything a kernel needs to reach a volume.
+struct VolumeView {
+    Entry* table;
+    uint32_t table_mask;        // table_capacity - 1
+    uint32_t pool_capacity;
+    float* tsdf;                // the five SoA arrays, [pool_capacity][512] each
+    float* weight;
+    float* red;
+    float* green;
+    float* blue;
+    uint32_t* pool_counter;     // bump allocator for pool indices
+    DeviceCounters* counters;
+    float voxel;
+    float trunc;
+    int band_half;              // samples at offsets -band_half .. band_half voxels
+};
+
+struct FrameView {
+    const float* depth;         // [height][width]
+    const float* rgb;           // [height][width][3] (update only)
+    int width;
+    int height;
+    Camera cam;
+};
+
+cudaError_t launch_allocate(const VolumeView& vol, const FrameView& fr, bool instrument,
+                            cudaStream_t stream);
+cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,
+                                   bool instrument, cudaStream_t stream);
+cudaError_t launch_update(const VolumeView& vol, const FrameView& fr, cudaStream_t stream);
+cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
+cudaError_t launch_export_coords(const VolumeView& vol, int32_t* coords, cudaStream_t stream);
+
+}  // namespace tsdf

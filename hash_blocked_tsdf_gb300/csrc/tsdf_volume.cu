@@ -1,0 +1,504 @@
+// Host side of libtsdf.so: the C ABI declared in include/tsdf.h.  It owns
+// the volume's device memory, validates every argument before enqueueing
+// anything, and launches the kernels on the caller's stream.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "tsdf_internal.h"
+
+using namespace tsdf;
+
+namespace {
+
+// Device-resident mutable state: the pool's bump counter and the counters.
+struct DeviceState {
+    uint32_t pool_counter;
+    uint32_t pad[7];
+    DeviceCounters counters;
+};
+
+}  // namespace
+
+struct tsdf_volume {
+    int device = 0;
+    uint32_t pool_capacity = 0;
+    uint32_t table_capacity = 0;
+    float voxel = 0.0f;
+    float trunc = 0.0f;
+    int band_half = 0;
+    bool instrument = false;
+
+    Entry* table = nullptr;
+    float* pool = nullptr;          // five arrays of pool_capacity * 512 floats, back to back
+    DeviceState* state = nullptr;
+    int32_t* coords = nullptr;      // [pool_capacity][3], allocated on first export
+
+    // host-batch staging: two buffers of (depth, rgb) frames
+    float* stage[2] = {nullptr, nullptr};
+    size_t stage_pixels = 0;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t copied[2] = {nullptr, nullptr};
+    cudaEvent_t consumed[2] = {nullptr, nullptr};
+};
+
+namespace {
+
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg)
+{
+    g_last_error = msg;
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    return e == cudaErrorMemoryAllocation ? TSDF_ERR_OOM : TSDF_ERR_CUDA;
+}
+
+#define TSDF_CUDA(call, what)                         \
+    do {                                              \
+        cudaError_t e_ = (call);                      \
+        if (e_ != cudaSuccess) return cuda_fail(e_, what); \
+    } while (0)
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+size_t array_floats(const tsdf_volume* v) { return (size_t)v->pool_capacity * kBlockVoxels; }
+
+VolumeView view_of(const tsdf_volume* v)
+{
+    VolumeView w;
+    w.table = v->table;
+    w.table_mask = v->table_capacity - 1;
+    w.pool_capacity = v->pool_capacity;
+    const size_t n = array_floats(v);
+    w.tsdf = v->pool;
+    w.weight = v->pool + n;
+    w.red = v->pool + 2 * n;
+    w.green = v->pool + 3 * n;
+    w.blue = v->pool + 4 * n;
+    w.pool_counter = &v->state->pool_counter;
+    w.counters = &v->state->counters;
+    w.voxel = v->voxel;
+    w.trunc = v->trunc;
+    w.band_half = v->band_half;
+    return w;
+}
+
+bool is_pow2(uint64_t x) { return x && !(x & (x - 1)); }
+
+int make_camera(const float* K, const float* pose, Camera* c)
+{
+    if (!K || !pose) return fail(TSDF_ERR_ARG, "K and pose must be non-null host arrays");
+    for (int i = 0; i < 4; ++i)
+        if (!std::isfinite(K[i])) return fail(TSDF_ERR_ARG, "K has a non-finite entry");
+    if (K[0] == 0.0f || K[1] == 0.0f) return fail(TSDF_ERR_ARG, "fx and fy must be non-zero");
+    for (int i = 0; i < 12; ++i)
+        if (!std::isfinite(pose[i])) return fail(TSDF_ERR_ARG, "pose has a non-finite entry");
+    c->fx = K[0];
+    c->fy = K[1];
+    c->cx = K[2];
+    c->cy = K[3];
+    c->r00 = pose[0]; c->r01 = pose[1]; c->r02 = pose[2];  c->tx = pose[3];
+    c->r10 = pose[4]; c->r11 = pose[5]; c->r12 = pose[6];  c->ty = pose[7];
+    c->r20 = pose[8]; c->r21 = pose[9]; c->r22 = pose[10]; c->tz = pose[11];
+    return TSDF_OK;
+}
+
+int check_size(int width, int height)
+{
+    if (width <= 0 || height <= 0) return fail(TSDF_ERR_ARG, "width and height must be positive");
+    if ((int64_t)width * (int64_t)height > (int64_t)1 << 30)
+        return fail(TSDF_ERR_ARG, "width * height exceeds 2^30 pixels");
+    return TSDF_OK;
+}
+
+int check_volume(const tsdf_volume* v)
+{
+    if (!v) return fail(TSDF_ERR_ARG, "volume is null");
+    return TSDF_OK;
+}
+
+int ensure_staging(tsdf_volume* v, size_t pixels)
+{
+    if (!v->copy_stream) {
+        TSDF_CUDA(cudaStreamCreateWithFlags(&v->copy_stream, cudaStreamNonBlocking),
+                  "cudaStreamCreateWithFlags");
+        for (int b = 0; b < 2; ++b) {
+            TSDF_CUDA(cudaEventCreateWithFlags(&v->copied[b], cudaEventDisableTiming),
+                      "cudaEventCreateWithFlags");
+            TSDF_CUDA(cudaEventCreateWithFlags(&v->consumed[b], cudaEventDisableTiming),
+                      "cudaEventCreateWithFlags");
+        }
+    }
+    if (v->stage_pixels >= pixels) return TSDF_OK;
+    for (int b = 0; b < 2; ++b) {
+        if (v->stage[b]) {
+            TSDF_CUDA(cudaEventSynchronize(v->consumed[b]), "cudaEventSynchronize");
+            TSDF_CUDA(cudaFree(v->stage[b]), "cudaFree");
+            v->stage[b] = nullptr;
+        }
+    }
+    v->stage_pixels = 0;
+    for (int b = 0; b < 2; ++b)
+        TSDF_CUDA(cudaMalloc(&v->stage[b], pixels * 4 * sizeof(float)), "cudaMalloc(staging)");
+    v->stage_pixels = pixels;
+    return TSDF_OK;
+}
+
+void release(tsdf_volume* v)
+{
+    if (v->table) cudaFree(v->table);
+    if (v->pool) cudaFree(v->pool);
+    if (v->state) cudaFree(v->state);
+    if (v->coords) cudaFree(v->coords);
+    for (int b = 0; b < 2; ++b) {
+        if (v->stage[b]) cudaFree(v->stage[b]);
+        if (v->copied[b]) cudaEventDestroy(v->copied[b]);
+        if (v->consumed[b]) cudaEventDestroy(v->consumed[b]);
+    }
+    if (v->copy_stream) cudaStreamDestroy(v->copy_stream);
+    delete v;
+}
+
+int frame_kernels(tsdf_volume* v, const float* depth, const float* rgb, int width, int height,
+                  const Camera& cam, bool do_allocate, bool do_update, cudaStream_t stream)
+{
+    const VolumeView vol = view_of(v);
+    FrameView fr;
+    fr.depth = depth;
+    fr.rgb = rgb;
+    fr.width = width;
+    fr.height = height;
+    fr.cam = cam;
+    if (do_allocate) TSDF_CUDA(launch_allocate(vol, fr, v->instrument, stream), "allocate kernel");
+    if (do_update) TSDF_CUDA(launch_update(vol, fr, stream), "update kernel");
+    return TSDF_OK;
+}
+
+int one_frame(tsdf_volume* v, const float* depth, const float* rgb, int width, int height,
+              const float K[4], const float pose[16], void* stream, bool do_allocate,
+              bool do_update)
+{
+    int rc = check_volume(v);
+    if (rc) return rc;
+    if ((rc = check_size(width, height))) return rc;
+    if (!depth) return fail(TSDF_ERR_ARG, "depth is null");
+    if (do_update && !rgb) return fail(TSDF_ERR_ARG, "rgb is null");
+    Camera cam;
+    if ((rc = make_camera(K, pose, &cam))) return rc;
+    return frame_kernels(v, depth, rgb, width, height, cam, do_allocate, do_update,
+                         as_stream(stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* tsdf_last_error(void) { return g_last_error.c_str(); }
+
+int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_size, float trunc,
+                   tsdf_volume** out)
+{
+    if (!out) return fail(TSDF_ERR_ARG, "out is null");
+    *out = nullptr;
+    if (pool_capacity < 1 || pool_capacity > TSDF_MAX_POOL_CAPACITY)
+        return fail(TSDF_ERR_ARG, "pool_capacity must be in [1, 2^23]");
+    if (!std::isfinite(voxel_size) || !(voxel_size > 0.0f) || !std::isfinite(trunc) ||
+        !(trunc > 0.0f))
+        return fail(TSDF_ERR_ARG, "voxel_size and trunc must be finite and positive");
+    const double ratio = std::round((double)trunc / (double)voxel_size);
+    if (2.0 * ratio + 1.0 > TSDF_MAX_BAND_SAMPLES)
+        return fail(TSDF_ERR_ARG, "trunc / voxel_size is too large");
+    uint64_t T = table_capacity;
+    if (T == 0) {
+        T = 1;
+        while (T <= 2ull * pool_capacity) T <<= 1;     // strictly above twice the pool
+    } else if (!is_pow2(T) || T < 2ull * pool_capacity) {
+        return fail(TSDF_ERR_ARG, "table_capacity must be a power of two >= 2 * pool_capacity");
+    }
+    if (T > TSDF_MAX_TABLE_CAPACITY) return fail(TSDF_ERR_ARG, "table_capacity exceeds 2^30");
+
+    tsdf_volume* v = new (std::nothrow) tsdf_volume();
+    if (!v) return fail(TSDF_ERR_OOM, "host allocation failed");
+    v->pool_capacity = pool_capacity;
+    v->table_capacity = (uint32_t)T;
+    v->voxel = voxel_size;
+    v->trunc = trunc;
+    v->band_half = (int)ratio;
+    cudaError_t e = cudaGetDevice(&v->device);
+    const size_t pool_bytes = 5 * array_floats(v) * sizeof(float);
+    if (e == cudaSuccess) e = cudaMalloc(&v->table, T * sizeof(Entry));
+    if (e == cudaSuccess) e = cudaMalloc(&v->pool, pool_bytes);
+    if (e == cudaSuccess) e = cudaMalloc(&v->state, sizeof(DeviceState));
+    if (e == cudaSuccess) e = cudaMemsetAsync(v->pool, 0, pool_bytes, 0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(v->table, 0xFF, T * sizeof(Entry), 0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(v->state, 0, sizeof(DeviceState), 0);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+    if (e != cudaSuccess) {
+        int rc = cuda_fail(e, "tsdf_create");
+        release(v);
+        cudaGetLastError();
+        return rc;
+    }
+    *out = v;
+    return TSDF_OK;
+}
+
+int tsdf_create(uint32_t pool_capacity, float voxel_size, float trunc, tsdf_volume** out)
+{
+    return tsdf_create_ex(pool_capacity, 0, voxel_size, trunc, out);
+}
+
+int tsdf_destroy(tsdf_volume* vol)
+{
+    if (!vol) return fail(TSDF_ERR_ARG, "volume is null");
+    cudaError_t e = cudaDeviceSynchronize();
+    release(vol);
+    if (e != cudaSuccess) return cuda_fail(e, "tsdf_destroy");
+    return TSDF_OK;
+}
+
+int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out)
+{
+    if (!vol || !out) return fail(TSDF_ERR_ARG, "null argument");
+    out->pool_capacity = vol->pool_capacity;
+    out->table_capacity = vol->table_capacity;
+    out->voxel_size = vol->voxel;
+    out->trunc = vol->trunc;
+    out->band_samples = 2 * vol->band_half + 1;
+    out->device = vol->device;
+    return TSDF_OK;
+}
+
+int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out)
+{
+    if (!vol || !out) return fail(TSDF_ERR_ARG, "null argument");
+    const VolumeView w = view_of(vol);
+    out->tsdf = w.tsdf;
+    out->weight = w.weight;
+    out->r = w.red;
+    out->g = w.green;
+    out->b = w.blue;
+    out->pool_capacity = vol->pool_capacity;
+    out->reserved = 0;
+    return TSDF_OK;
+}
+
+int tsdf_reset(tsdf_volume* vol, void* stream)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    cudaStream_t s = as_stream(stream);
+    TSDF_CUDA(launch_zero_used_blocks(view_of(vol), s), "zero kernel");
+    TSDF_CUDA(cudaMemsetAsync(vol->table, 0xFF, (size_t)vol->table_capacity * sizeof(Entry), s),
+              "cudaMemsetAsync(table)");
+    TSDF_CUDA(cudaMemsetAsync(vol->state, 0, sizeof(DeviceState), s), "cudaMemsetAsync(state)");
+    return TSDF_OK;
+}
+
+int tsdf_integrate(tsdf_volume* vol, const float* depth, const float* rgb, int width, int height,
+                   const float K[4], const float pose[16], void* stream)
+{
+    return one_frame(vol, depth, rgb, width, height, K, pose, stream, true, true);
+}
+
+int tsdf_allocate(tsdf_volume* vol, const float* depth, int width, int height, const float K[4],
+                  const float pose[16], void* stream)
+{
+    return one_frame(vol, depth, nullptr, width, height, K, pose, stream, true, false);
+}
+
+int tsdf_update(tsdf_volume* vol, const float* depth, const float* rgb, int width, int height,
+                const float K[4], const float pose[16], void* stream)
+{
+    return one_frame(vol, depth, rgb, width, height, K, pose, stream, false, true);
+}
+
+int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
+                         int width, int height, const float K[4], const float* poses,
+                         void* stream)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (n_frames < 0) return fail(TSDF_ERR_ARG, "n_frames must be >= 0");
+    if (n_frames == 0) return TSDF_OK;
+    if ((rc = check_size(width, height))) return rc;
+    if (!depth || !rgb || !poses) return fail(TSDF_ERR_ARG, "null frame pointer");
+    std::vector<Camera> cams((size_t)n_frames);
+    for (int f = 0; f < n_frames; ++f)
+        if ((rc = make_camera(K, poses + 16 * (size_t)f, &cams[f]))) return rc;
+    const size_t px = (size_t)width * (size_t)height;
+    for (int f = 0; f < n_frames; ++f) {
+        rc = frame_kernels(vol, depth + f * px, rgb + 3 * f * px, width, height, cams[f], true,
+                           true, as_stream(stream));
+        if (rc) return rc;
+    }
+    return TSDF_OK;
+}
+
+int tsdf_integrate_batch_host(tsdf_volume* vol, int n_frames, const float* depth_host,
+                              const float* rgb_host, int width, int height, const float K[4],
+                              const float* poses, void* stream)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (n_frames < 0) return fail(TSDF_ERR_ARG, "n_frames must be >= 0");
+    if (n_frames == 0) return TSDF_OK;
+    if ((rc = check_size(width, height))) return rc;
+    if (!depth_host || !rgb_host || !poses) return fail(TSDF_ERR_ARG, "null frame pointer");
+    std::vector<Camera> cams((size_t)n_frames);
+    for (int f = 0; f < n_frames; ++f)
+        if ((rc = make_camera(K, poses + 16 * (size_t)f, &cams[f]))) return rc;
+    const size_t px = (size_t)width * (size_t)height;
+    if ((rc = ensure_staging(vol, px))) return rc;
+    cudaStream_t s = as_stream(stream);
+    for (int f = 0; f < n_frames; ++f) {
+        const int b = f & 1;
+        float* d_dev = vol->stage[b];
+        float* c_dev = vol->stage[b] + px;
+        // the copy into buffer b waits for the kernels that last read it
+        TSDF_CUDA(cudaStreamWaitEvent(vol->copy_stream, vol->consumed[b], 0), "cudaStreamWaitEvent");
+        TSDF_CUDA(cudaMemcpyAsync(d_dev, depth_host + f * px, px * sizeof(float),
+                                  cudaMemcpyHostToDevice, vol->copy_stream), "cudaMemcpyAsync(depth)");
+        TSDF_CUDA(cudaMemcpyAsync(c_dev, rgb_host + 3 * f * px, 3 * px * sizeof(float),
+                                  cudaMemcpyHostToDevice, vol->copy_stream), "cudaMemcpyAsync(rgb)");
+        TSDF_CUDA(cudaEventRecord(vol->copied[b], vol->copy_stream), "cudaEventRecord");
+        TSDF_CUDA(cudaStreamWaitEvent(s, vol->copied[b], 0), "cudaStreamWaitEvent");
+        rc = frame_kernels(vol, d_dev, c_dev, width, height, cams[f], true, true, s);
+        if (rc) return rc;
+        TSDF_CUDA(cudaEventRecord(vol->consumed[b], s), "cudaEventRecord");
+    }
+    return TSDF_OK;
+}
+
+int tsdf_allocate_blocks(tsdf_volume* vol, const int32_t* coords, uint32_t n, void* stream)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (n == 0) return TSDF_OK;
+    if (!coords) return fail(TSDF_ERR_ARG, "coords is null");
+    if (n > (1u << 30)) return fail(TSDF_ERR_ARG, "n exceeds 2^30");
+    TSDF_CUDA(launch_allocate_blocks(view_of(vol), coords, n, vol->instrument, as_stream(stream)),
+              "allocate_blocks kernel");
+    return TSDF_OK;
+}
+
+int tsdf_block_count(tsdf_volume* vol, void* stream, uint32_t* out)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (!out) return fail(TSDF_ERR_ARG, "out is null");
+    uint32_t counter = 0;
+    cudaStream_t s = as_stream(stream);
+    TSDF_CUDA(cudaMemcpyAsync(&counter, &vol->state->pool_counter, sizeof(uint32_t),
+                              cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(count)");
+    TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    *out = counter < vol->pool_capacity ? counter : vol->pool_capacity;
+    return TSDF_OK;
+}
+
+int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t count,
+                       int32_t* coords, float* tsdf_out, float* weight, float* r, float* g,
+                       float* b)
+{
+    uint32_t n = 0;
+    int rc = tsdf_block_count(vol, stream, &n);
+    if (rc) return rc;
+    if ((uint64_t)first + count > n)
+        return fail(TSDF_ERR_ARG, "first + count exceeds the number of allocated blocks");
+    if (count == 0) return TSDF_OK;
+    cudaStream_t s = as_stream(stream);
+    if (coords) {
+        if (!vol->coords)
+            TSDF_CUDA(cudaMalloc(&vol->coords, (size_t)vol->pool_capacity * 3 * sizeof(int32_t)),
+                      "cudaMalloc(coords)");
+        TSDF_CUDA(launch_export_coords(view_of(vol), vol->coords, s), "export_coords kernel");
+        TSDF_CUDA(cudaMemcpyAsync(coords, vol->coords + 3 * (size_t)first,
+                                  (size_t)count * 3 * sizeof(int32_t), cudaMemcpyDeviceToHost, s),
+                  "cudaMemcpyAsync(coords)");
+    }
+    const VolumeView w = view_of(vol);
+    float* src[5] = {w.tsdf, w.weight, w.red, w.green, w.blue};
+    float* dst[5] = {tsdf_out, weight, r, g, b};
+    for (int a = 0; a < 5; ++a) {
+        if (!dst[a]) continue;
+        TSDF_CUDA(cudaMemcpyAsync(dst[a], src[a] + (size_t)first * kBlockVoxels,
+                                  (size_t)count * kBlockVoxels * sizeof(float),
+                                  cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(sums)");
+    }
+    TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    return TSDF_OK;
+}
+
+int tsdf_export_table(tsdf_volume* vol, void* stream, uint32_t capacity, uint64_t* keys,
+                      uint32_t* indices)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (capacity != vol->table_capacity)
+        return fail(TSDF_ERR_ARG, "capacity must equal the table capacity");
+    std::vector<Entry> host(capacity);
+    cudaStream_t s = as_stream(stream);
+    TSDF_CUDA(cudaMemcpyAsync(host.data(), vol->table, (size_t)capacity * sizeof(Entry),
+                              cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(table)");
+    TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    for (uint32_t i = 0; i < capacity; ++i) {
+        if (keys) keys[i] = host[i].key;
+        if (indices) indices[i] = host[i].idx;
+    }
+    return TSDF_OK;
+}
+
+int tsdf_get_stats(tsdf_volume* vol, void* stream, tsdf_stats* out)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (!out) return fail(TSDF_ERR_ARG, "out is null");
+    DeviceState h;
+    cudaStream_t s = as_stream(stream);
+    TSDF_CUDA(cudaMemcpyAsync(&h, vol->state, sizeof(DeviceState), cudaMemcpyDeviceToHost, s),
+              "cudaMemcpyAsync(stats)");
+    TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    std::memset(out, 0, sizeof(*out));
+    const DeviceCounters& c = h.counters;
+    out->blocks_allocated = h.pool_counter;
+    out->pool_exhausted = c.pool_exhausted;
+    out->probe_overflow = c.probe_overflow;
+    for (int i = 0; i < kCounterStripes; ++i) {
+        out->missed_contributions += c.missed[i];
+        out->out_of_range_samples += c.out_of_range[i];
+        out->valid_points += c.valid_points[i];
+        out->voxel_updates += c.voxel_updates[i];
+    }
+    out->probe_inserts = c.probe_inserts;
+    out->probe_steps = c.probe_steps;
+    out->probe_max = c.probe_max;
+    for (int i = 0; i < TSDF_PROBE_HIST_BINS; ++i) out->probe_hist[i] = c.probe_hist[i];
+    return TSDF_OK;
+}
+
+int tsdf_clear_stats(tsdf_volume* vol, void* stream)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    TSDF_CUDA(cudaMemsetAsync(&vol->state->counters, 0, sizeof(DeviceCounters), as_stream(stream)),
+              "cudaMemsetAsync(counters)");
+    return TSDF_OK;
+}
+
+int tsdf_set_instrumentation(tsdf_volume* vol, int on)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    vol->instrument = on != 0;
+    return TSDF_OK;
+}
+
+}  // extern "C"

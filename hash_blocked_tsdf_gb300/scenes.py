@@ -167,16 +167,29 @@ def _finish_depth(rng, depth64, noise_sigma, invalid_frac):
 
 
 def _render(rng, prims, poses, K, width, height, noise_sigma, invalid_frac=0.0,
-            plane_z=None, room_half=None):
-    """Ray cast every pose, then draw colour and noise frame by frame."""
+            plane_z=None, room_half=None, frame_seeds=None):
+    """Ray cast every pose, then draw colour and noise frame by frame: from
+    ``rng`` in frame order, or, when ``frame_seeds`` is given, from a fresh
+    generator per frame seeded with that frame's entry (so any range of frames
+    can be rendered on its own)."""
     d64 = raycast(prims, poses, K, width, height, plane_z=plane_z, room_half=room_half)
     n = len(poses)
     depth = np.empty((n, height, width), dtype=np.float32)
     rgb = np.empty((n, height, width, 3), dtype=np.float32)
     for f in range(n):
-        rgb[f] = rng.random((height, width, 3), dtype=np.float32)
-        depth[f] = _finish_depth(rng, d64[f], noise_sigma, invalid_frac)
+        g = rng if frame_seeds is None else np.random.Generator(np.random.PCG64(frame_seeds[f]))
+        rgb[f] = g.random((height, width, 3), dtype=np.float32)
+        depth[f] = _finish_depth(g, d64[f], noise_sigma, invalid_frac)
     return depth, rgb
+
+
+def _frame_range(n_frames, frames):
+    if frames is None:
+        return 0, n_frames
+    start, stop = frames
+    if not (0 <= start <= stop <= n_frames):
+        raise ValueError(f"frame range {frames} outside [0, {n_frames}]")
+    return start, stop
 
 
 def sphere_plane(width=160, height=120, fx=131.25, fy=131.25, cx=None, cy=None,
@@ -240,25 +253,30 @@ def random_primitives(rng, n, lo, hi, size_lo=0.1, size_hi=0.8):
 
 def orbit_trajectory(n_frames=100, seed=0, width=640, height=480,
                      voxel_size=0.005, trunc=0.02, pool_capacity=1 << 18,
-                     table_capacity=0) -> Frames:
+                     table_capacity=0, frames=None) -> Frames:
     """40 random boxes/spheres in a 4 m cube, camera orbiting at 2.5 m.
 
     The camera circles the origin in the y = 0 plane, 3.6 degrees per frame,
     always looking at the origin.  Depth noise 2 mm; rays that hit nothing
-    read 0.
+    read 0.  ``frames=(start, stop)`` renders only that range of the
+    trajectory (identical to the same frames of the full render).
     """
     rng = np.random.Generator(np.random.PCG64(seed))
     prims = random_primitives(rng, 40, -2.0, 2.0)
     K = np.array([525.0, 525.0, 319.5, 239.5], dtype=np.float32)
+    start, stop = _frame_range(n_frames, frames)
     poses = []
-    for f in range(n_frames):
+    for f in range(start, stop):
         a = math.radians(3.6 * f)
         pos = (2.5 * math.sin(a), 0.0, 2.5 * math.cos(a))
         poses.append(look_at(pos, (0.0, 0.0, 0.0)))
-    depth, rgb = _render(rng, prims, poses, K, width, height, 0.002)
-    return Frames(f"orbit_{n_frames}x{width}x{height}", depth, rgb,
-                  np.asarray(poses, dtype=np.float32), K, voxel_size, trunc,
-                  pool_capacity, table_capacity, seed)
+    seeds = [[seed, 1, f] for f in range(start, stop)]
+    depth, rgb = _render(rng, prims, poses, K, width, height, 0.002, frame_seeds=seeds)
+    name = f"orbit_{n_frames}x{width}x{height}"
+    if frames is not None:
+        name += f"[{start}:{stop}]"
+    return Frames(name, depth, rgb, np.asarray(poses, dtype=np.float32).reshape(-1, 4, 4), K,
+                  voxel_size, trunc, pool_capacity, table_capacity, seed)
 
 
 def _prim_bounds(kind, centre, size):
@@ -312,14 +330,22 @@ def room_walk_poses(rng, prims, n_frames, room_half=4.0, margin=0.5,
 
 def room_random_walk(n_frames=300, seed=0, width=1280, height=720,
                      voxel_size=0.004, trunc=0.016, pool_capacity=1 << 20,
-                     table_capacity=1 << 21, n_prims=400) -> Frames:
+                     table_capacity=1 << 21, n_prims=400, frames=None) -> Frames:
     """400 random boxes/spheres inside an 8 m room whose six inner walls are
-    part of the scene; 1280x720 random-walk trajectory, depth noise 3 mm."""
+    part of the scene; 1280x720 random-walk trajectory, depth noise 3 mm.
+    ``frames=(start, stop)`` renders only that range of the trajectory
+    (identical to the same frames of the full render)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     prims = random_primitives(rng, n_prims, -3.6, 3.6)
     K = np.array([920.0, 920.0, 639.5, 359.5], dtype=np.float32)
     poses = room_walk_poses(rng, prims, n_frames)
-    depth, rgb = _render(rng, prims, poses, K, width, height, 0.003, room_half=4.0)
-    return Frames(f"room_walk_{n_frames}x{width}x{height}", depth, rgb,
-                  np.asarray(poses, dtype=np.float32), K, voxel_size, trunc,
-                  pool_capacity, table_capacity, seed)
+    start, stop = _frame_range(n_frames, frames)
+    poses = poses[start:stop]
+    seeds = [[seed, 2, f] for f in range(start, stop)]
+    depth, rgb = _render(rng, prims, poses, K, width, height, 0.003, room_half=4.0,
+                         frame_seeds=seeds)
+    name = f"room_walk_{n_frames}x{width}x{height}"
+    if frames is not None:
+        name += f"[{start}:{stop}]"
+    return Frames(name, depth, rgb, np.asarray(poses, dtype=np.float32).reshape(-1, 4, 4), K,
+                  voxel_size, trunc, pool_capacity, table_capacity, seed)

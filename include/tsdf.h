@@ -1,0 +1,235 @@
+/*
+ * tsdf.h -- C ABI of libtsdf.so: hash-blocked TSDF integration on one GPU.
+ *
+ * The operation is the integrate path of "What Irregularity Costs: CUDA C++,
+ * Rust, and Triton on a Hash-Blocked GPU Workload" (arXiv 2608.08287):
+ *
+ *   design section, data structure: the volume is cut into blocks of
+ *     8^3 = 512 voxels.  An open-addressed, linear-probing hash table of
+ *     16-byte entries (a packed 64-bit block key, a 32-bit pool index, 4 bytes
+ *     of padding), sized to a power of two at least twice the pool capacity,
+ *     maps a block coordinate to an index into a flat pool of five float
+ *     arrays: TSDF sum, weight sum, red, green and blue sums.
+ *   design section, integration: two kernels run over the same
+ *     back-projected depth points.  ALLOCATE walks each point's truncation
+ *     band and inserts every missing block with a single 64-bit
+ *     compare-exchange.  UPDATE walks the same band and adds each passing
+ *     sample into its voxel with atomic additions.  Both apply the same
+ *     occlusion test.
+ *   design section, accumulation: the arrays hold sums, so the mean of a
+ *     voxel is sum / weight, formed only at read-out.
+ *
+ * Per sample (band offsets (i - k) * voxel, i = 0..2k, k = round(trunc /
+ * voxel), along the unit ray through the pixel's back-projected point):
+ * voxel = floor(world / voxel); signed distance at the voxel CENTRE
+ * sdf = depth - z_centre (camera frame); the sample passes iff
+ * z_centre > 0 and sdf >= -trunc; it adds (min(1, sdf / trunc), 1, r, g, b).
+ * The walk is computed in IEEE float32 with one rounding per operation
+ * (no fused multiply-add), so the voxel each sample selects is reproducible
+ * bit for bit by any IEEE implementation that evaluates the same operations
+ * in the same order.
+ *
+ * Conventions
+ *   - depth: float32 [height][width], metres, camera-frame z; a pixel is
+ *     valid iff its depth is finite and > 0.
+ *   - rgb: float32 [height][width][3] (any range; [0, 1] by convention).
+ *   - K: host float[4] = {fx, fy, cx, cy}; pixel centres at integer (u, v).
+ *   - pose: host float[16], row-major 4x4 camera-to-world [R | t] (the last
+ *     row is ignored).
+ *   - block coordinates must lie in [-2^20, 2^20 - 1] per axis (the 21-bit
+ *     key fields); samples outside are counted (out_of_range_samples) and
+ *     skipped.
+ *   - pool layout: for each of the five arrays, block b's voxel
+ *     j = lx + 8 * ly + 64 * lz lives at element b * 512 + j.
+ *
+ * Ownership and synchronisation
+ *   - A tsdf_volume owns its device memory (table, pool, counters), allocated
+ *     at create and released at destroy, on the device that was current at
+ *     create.  Call every function with that device current.
+ *   - Device pointers passed in (depth, rgb, coords) are borrowed: they must
+ *     stay valid until the work enqueued on `stream` has finished.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     that enqueue work return without synchronising, except the read-out
+ *     calls (block_count, export_*, get_stats), which synchronise `stream`.
+ *   - A volume is not thread-safe; concurrent calls on one volume race.
+ *
+ * Errors: every call returns TSDF_OK or a negative code.  On TSDF_ERR_ARG
+ * nothing was enqueued.  tsdf_last_error() returns a message describing the
+ * last failure on the calling thread.
+ */
+#ifndef TSDF_H
+#define TSDF_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TSDF_OK 0
+#define TSDF_ERR_ARG (-1)      /* invalid argument; nothing enqueued */
+#define TSDF_ERR_CUDA (-2)     /* a CUDA runtime call failed */
+#define TSDF_ERR_OOM (-3)      /* a device or pinned allocation failed */
+
+#define TSDF_BLOCK_VOXELS 512
+#define TSDF_PROBE_HIST_BINS 32
+#define TSDF_MAX_POOL_CAPACITY (1u << 23)
+#define TSDF_MAX_TABLE_CAPACITY (1u << 30)
+#define TSDF_MAX_BAND_SAMPLES 255
+#define TSDF_EMPTY_KEY 0xFFFFFFFFFFFFFFFFull   /* key of an empty table slot */
+#define TSDF_INDEX_PENDING 0xFFFFFFFFu         /* slot claimed, index not yet published */
+#define TSDF_INDEX_FAILED 0xFFFFFFFEu          /* key inserted but the pool was full */
+
+typedef struct tsdf_volume tsdf_volume;
+
+typedef struct tsdf_info {
+    uint32_t pool_capacity;     /* blocks in the pool */
+    uint32_t table_capacity;    /* table slots (a power of two) */
+    float voxel_size;           /* metres */
+    float trunc;                /* metres */
+    int32_t band_samples;       /* samples per point, 2k + 1 */
+    int32_t device;             /* CUDA device ordinal that owns the memory */
+} tsdf_info;
+
+/* Device pointers to the pool's five arrays, each float32
+ * [pool_capacity][512] (block b, voxel j at b * 512 + j).  They stay valid
+ * until tsdf_destroy; reading them races with kernels still running. */
+typedef struct tsdf_pool_view {
+    float* tsdf;
+    float* weight;
+    float* r;
+    float* g;
+    float* b;
+    uint32_t pool_capacity;
+    uint32_t reserved;
+} tsdf_pool_view;
+
+/* Counters accumulated since create / reset / tsdf_clear_stats. */
+typedef struct tsdf_stats {
+    uint64_t blocks_allocated;      /* pool counter; may exceed capacity when exhausted */
+    uint64_t pool_exhausted;        /* distinct keys inserted with no pool slot left */
+    uint64_t probe_overflow;        /* inserts that examined every slot without success */
+    uint64_t missed_contributions;  /* passing samples whose block was absent or FAILED */
+    uint64_t out_of_range_samples;  /* samples outside the key range (allocate pass) */
+    uint64_t valid_points;          /* valid pixels seen by the update pass */
+    uint64_t voxel_updates;         /* samples accumulated by the update pass */
+    /* probe statistics, collected only while instrumentation is on: */
+    uint64_t probe_inserts;         /* insert probes issued (after de-duplication) */
+    uint64_t probe_steps;           /* slots examined by those probes */
+    uint64_t probe_max;             /* longest probe */
+    uint64_t probe_hist[TSDF_PROBE_HIST_BINS];  /* bin b: probes of length b + 1; last bin: longer */
+} tsdf_stats;
+
+/* Create a volume of `pool_capacity` blocks, voxel edge `voxel_size` metres,
+ * truncation `trunc` metres, with the default table size: the smallest power
+ * of two strictly greater than 2 * pool_capacity.  Requires
+ * 1 <= pool_capacity <= TSDF_MAX_POOL_CAPACITY, finite voxel_size > 0 and
+ * trunc > 0, and 2 * round(trunc / voxel_size) + 1 <= TSDF_MAX_BAND_SAMPLES.
+ * Zeroes the pool and empties the table (synchronously).  *out receives the
+ * handle, or NULL on failure. */
+int tsdf_create(uint32_t pool_capacity, float voxel_size, float trunc, tsdf_volume** out);
+
+/* As tsdf_create with an explicit table size: table_capacity must be a power
+ * of two with 2 * pool_capacity <= table_capacity <= TSDF_MAX_TABLE_CAPACITY,
+ * or 0 for the default. */
+int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_size,
+                   float trunc, tsdf_volume** out);
+
+/* Release the volume's device memory (synchronises the device first). */
+int tsdf_destroy(tsdf_volume* vol);
+
+int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out);
+
+/* Zero-copy access to the pool arrays (for read-out kernels of the caller). */
+int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out);
+
+/* Empty the volume on `stream`: zero the used prefix of the pool (the first
+ * min(blocks_allocated, pool_capacity) blocks of all five arrays), empty the
+ * table and zero every counter. */
+int tsdf_reset(tsdf_volume* vol, void* stream);
+
+/* Integrate one frame: tsdf_allocate followed by tsdf_update on `stream`. */
+int tsdf_integrate(tsdf_volume* vol, const float* depth, const float* rgb, int width,
+                   int height, const float K[4], const float pose[16], void* stream);
+
+/* The allocate kernel alone: make sure every block touched by a passing
+ * sample of this frame exists in the table (keys are de-duplicated within a
+ * warp before probing; a new key is claimed with one 64-bit compare-and-swap
+ * and receives the next pool index).  Probing is unbounded up to the table
+ * size; an insert that finds no slot counts probe_overflow, a key that finds
+ * the pool full is published as TSDF_INDEX_FAILED and counts
+ * pool_exhausted. */
+int tsdf_allocate(tsdf_volume* vol, const float* depth, int width, int height,
+                  const float K[4], const float pose[16], void* stream);
+
+/* The update kernel alone: add (tsdf, 1, r, g, b) of every passing sample
+ * into its voxel.  A sample whose block is absent or FAILED counts
+ * missed_contributions.  Call it after tsdf_allocate of the same frame (on
+ * the same stream) for the full integrate semantics. */
+int tsdf_update(tsdf_volume* vol, const float* depth, const float* rgb, int width,
+                int height, const float K[4], const float pose[16], void* stream);
+
+/* Integrate n_frames frames in order.  depth: device float32
+ * [n_frames][height][width]; rgb: device float32 [n_frames][height][width][3];
+ * K: host float[4] shared by all frames; poses: host float[n_frames][16]. */
+int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
+                         int width, int height, const float K[4], const float* poses,
+                         void* stream);
+
+/* As tsdf_integrate_batch, but depth and rgb are HOST arrays.  Each frame is
+ * copied into a double-buffered device staging area owned by the volume on a
+ * separate copy stream, overlapping the copy of frame f + 1 with the kernels
+ * of frame f.  For the copies to be asynchronous the host arrays must be
+ * page-locked (cudaHostAlloc / cudaHostRegister); pageable memory works but
+ * serialises.  The host arrays must stay valid and unchanged until the work on
+ * `stream` has finished.  The staging area is allocated on first use (and
+ * grown for larger frames); that first call must not be made during stream
+ * capture. */
+int tsdf_integrate_batch_host(tsdf_volume* vol, int n_frames, const float* depth_host,
+                              const float* rgb_host, int width, int height, const float K[4],
+                              const float* poses, void* stream);
+
+/* Insert explicit block coordinates (device int32 [n][3]) through the same
+ * de-duplicate / probe / compare-and-swap / pool-index path as the allocate
+ * kernel.  Coordinates outside the key range count out_of_range_samples. */
+int tsdf_allocate_blocks(tsdf_volume* vol, const int32_t* coords, uint32_t n, void* stream);
+
+/* Synchronise `stream` and return min(blocks_allocated, pool_capacity). */
+int tsdf_block_count(tsdf_volume* vol, void* stream, uint32_t* out);
+
+/* Copy pool blocks [first, first + count) to the host, after synchronising
+ * `stream`: coords int32 [count][3] (block coordinates, recovered from the
+ * table) and the five sum arrays float32 [count][512].  Any output pointer may
+ * be NULL to skip it.  first + count must not exceed tsdf_block_count.  Pool
+ * order is the order in which blocks won their pool index, which is not
+ * deterministic: compare by coordinate. */
+int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t count,
+                       int32_t* coords, float* tsdf, float* weight, float* r, float* g,
+                       float* b);
+
+/* Copy the raw hash table to the host after synchronising `stream`: keys
+ * uint64 [table_capacity] (TSDF_EMPTY_KEY for an empty slot) and indices
+ * uint32 [table_capacity].  `capacity` must equal the table capacity. Either
+ * output may be NULL. */
+int tsdf_export_table(tsdf_volume* vol, void* stream, uint32_t capacity, uint64_t* keys,
+                      uint32_t* indices);
+
+/* Synchronise `stream` and read the counters. */
+int tsdf_get_stats(tsdf_volume* vol, void* stream, tsdf_stats* out);
+
+/* Zero the counters (not the pool counter, the table or the pool). */
+int tsdf_clear_stats(tsdf_volume* vol, void* stream);
+
+/* Turn probe instrumentation (probe_* statistics) on or off for later
+ * launches.  It costs a shared-memory histogram per block of threads; keep it
+ * off when timing. */
+int tsdf_set_instrumentation(tsdf_volume* vol, int on);
+
+/* Message of the last failure on the calling thread ("" if none). */
+const char* tsdf_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSDF_H */

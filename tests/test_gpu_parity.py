@@ -1,0 +1,340 @@
+"""Parity of the CUDA integrate path (through the C ABI) with the CPU oracle.
+
+Exact: block coordinate set, block count, every weight sum, the counters.
+Float: TSDF and colour sums within max(1e-5 |x|, 1e-6) for single frames;
+for trajectories the float32 summation bound is admitted as well (see
+tests/parity.py).
+"""
+import numpy as np
+import pytest
+
+import parity
+from hash_blocked_tsdf_gb300 import scenes
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+    __graft_entry__.build()
+    return torch
+
+
+def _gpu_volume(torch, frames, **kw):
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    cap = kw.get("pool_capacity", frames.pool_capacity)
+    table = kw.get("table_capacity", frames.table_capacity)
+    return TsdfVolume(cap, frames.voxel_size, frames.trunc, table)
+
+
+def _integrate_gpu(torch, frames, vol, batch=True):
+    d = torch.from_numpy(frames.depth).cuda()
+    c = torch.from_numpy(frames.rgb).cuda()
+    if batch:
+        vol.integrate_batch(d, c, frames.K, frames.poses)
+    else:
+        for f in range(frames.n_frames):
+            vol.integrate(d[f], c[f], frames.K, frames.poses[f])
+    torch.cuda.synchronize()
+
+
+def _oracle(oracle_mod, frames, block_limit=-1):
+    o = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc, block_limit=block_limit)
+    o.integrate_frames(frames)
+    return o
+
+
+def _full_parity(torch, oracle_mod, frames, strict, batch=True):
+    vol = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, vol, batch)
+    g = vol.export_blocks()
+    st = vol.stats()
+    o = _oracle(oracle_mod, frames)
+    rep = parity.compare_volume(g, o.export(), strict)
+    parity.check_counters(st, o.counters())
+    assert st["pool_exhausted"] == 0
+    assert vol.block_count() == o.block_count()
+    # every allocated block received a contribution (same occlusion test in both passes)
+    assert np.all(g["weight"].sum(axis=1) > 0)
+    vol.close()
+    return rep
+
+
+def test_smoke_entry(torch_cuda):
+    import __graft_entry__
+    __graft_entry__.smoke()
+
+
+def test_parity_tiny_sphere_plane(torch_cuda, oracle_mod):
+    rep = _full_parity(torch_cuda, oracle_mod, scenes.tiny_sphere_plane(), strict=True)
+    assert rep["blocks"] > 500
+
+
+def test_parity_vga_sphere_plane(torch_cuda, oracle_mod):
+    _full_parity(torch_cuda, oracle_mod, scenes.vga_sphere_plane(), strict=True)
+
+
+def test_parity_oblique_pose(torch_cuda, oracle_mod):
+    from test_oracle_pins import oblique_sphere_frames
+    _full_parity(torch_cuda, oracle_mod, oblique_sphere_frames(), strict=True)
+
+
+@pytest.mark.parametrize("wh", [(1, 1), (7, 3), (33, 17), (161, 121), (257, 1), (1, 300)])
+def test_parity_ragged_sizes(torch_cuda, oracle_mod, wh):
+    W, H = wh
+    depth, rgb, pose, K = scenes.sphere_plane(W, H, fx=0.8 * max(W, H), fy=0.8 * max(W, H),
+                                              noise_sigma=0.002, invalid_frac=0.1, seed=W * H)
+    frames = scenes.Frames(f"ragged_{W}x{H}", depth[None], rgb[None], pose[None], K,
+                           0.01, 0.04, 4096, 0, 0)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True)
+
+
+def test_parity_orbit_prefix_per_frame_vs_batch(torch_cuda, oracle_mod):
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 8))
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, batch=False)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, batch=True)
+
+
+@pytest.mark.slow
+def test_parity_orbit_trajectory_full(torch_cuda, oracle_mod):
+    rep = _full_parity(torch_cuda, oracle_mod, scenes.orbit_trajectory(), strict=False)
+    print("orbit trajectory parity:", rep)
+
+
+def test_host_batch_matches_device_batch(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(10, 15))
+    a = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, a)
+    b = _gpu_volume(torch, frames)
+    d = torch.from_numpy(frames.depth).pin_memory()
+    c = torch.from_numpy(frames.rgb).pin_memory()
+    b.integrate_batch_host(d, c, frames.K, frames.poses)
+    torch.cuda.synchronize()
+    ga, gb = a.export_blocks(), b.export_blocks()
+    oa, ob = parity.sort_by_coords(ga["coords"]), parity.sort_by_coords(gb["coords"])
+    assert np.array_equal(ga["coords"][oa], gb["coords"][ob])
+    assert np.array_equal(ga["weight"][oa], gb["weight"][ob])
+    o = _oracle(oracle_mod, frames)
+    parity.compare_volume(gb, o.export(), strict=False)
+    a.close()
+    b.close()
+
+
+def test_reset_gives_a_fresh_volume(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.vga_sphere_plane()
+    vol = _gpu_volume(torch, frames)
+    other = scenes.orbit_trajectory(n_frames=100, frames=(0, 2))
+    _integrate_gpu(torch, other.subset(0, 2), vol)  # different scene first
+    vol.reset()
+    _integrate_gpu(torch, frames, vol)
+    o = _oracle(oracle_mod, frames)
+    parity.compare_volume(vol.export_blocks(), o.export(), strict=True)
+    parity.check_counters(vol.stats(), o.counters())
+    vol.close()
+
+
+def test_empty_and_invalid_frames(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.tiny_sphere_plane()
+    d = frames.depth[0].copy()
+    d[:, :] = 0.0
+    vol = _gpu_volume(torch, frames)
+    vol.integrate(torch.from_numpy(d).cuda(), torch.from_numpy(frames.rgb[0]).cuda(), frames.K,
+                  frames.poses[0])
+    assert vol.block_count() == 0
+    st = vol.stats()
+    assert st["valid_points"] == 0 and st["voxel_updates"] == 0
+    d = frames.depth[0].copy()
+    d[0, :] = np.nan
+    d[1, :] = np.inf
+    d[2, :] = -np.inf
+    d[3, :] = -0.5
+    vol.reset()
+    vol.integrate(torch.from_numpy(d).cuda(), torch.from_numpy(frames.rgb[0]).cuda(), frames.K,
+                  frames.poses[0])
+    o = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
+    o.integrate(d, frames.rgb[0], frames.K, frames.poses[0])
+    parity.compare_volume(vol.export_blocks(), o.export(), strict=True)
+    parity.check_counters(vol.stats(), o.counters())
+    vol.close()
+
+
+def test_out_of_range_pose_counts_and_skips(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.tiny_sphere_plane()
+    far = np.eye(4, dtype=np.float32)
+    far[0, 3] = 1.0e6
+    vol = _gpu_volume(torch, frames)
+    vol.integrate(torch.from_numpy(frames.depth[0]).cuda(),
+                  torch.from_numpy(frames.rgb[0]).cuda(), frames.K, far)
+    st = vol.stats()
+    assert vol.block_count() == 0
+    assert st["out_of_range_samples"] == 9 * st["valid_points"] > 0
+    vol.close()
+
+
+def test_pool_exhaustion_is_counted_not_hidden(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.vga_sphere_plane()
+    full = _oracle(oracle_mod, frames)
+    B = full.block_count()
+    cap = B // 2
+    vol = _gpu_volume(torch, frames, pool_capacity=cap, table_capacity=0)
+    _integrate_gpu(torch, frames, vol)
+    st = vol.stats()
+    assert vol.block_count() == cap
+    assert st["pool_exhausted"] == B - cap
+    assert st["probe_overflow"] == 0
+    assert st["missed_contributions"] > 0
+    assert st["voxel_updates"] + st["missed_contributions"] == full.counters()["passing_samples"]
+    g = vol.export_blocks()
+    assert g["weight"].sum() == st["voxel_updates"]
+    # a block that won a pool slot received every one of its contributions
+    ref = full.export()
+    rows = np.searchsorted(
+        np.ravel_multi_index((ref["coords"] + 4096).T, (8192, 8192, 8192)),
+        np.ravel_multi_index((g["coords"] + 4096).T, (8192, 8192, 8192)))
+    assert np.array_equal(ref["coords"][rows], g["coords"])
+    parity.compare_sums({k: g[k] for k in ("tsdf", "weight", "r", "g", "b")}, ref, strict=True,
+                        rows=rows)
+    vol.close()
+
+
+def _check_table_structure(oracle_mod, vol, expected_coords):
+    keys, idx = vol.export_table()
+    empty = np.uint64(0xFFFFFFFFFFFFFFFF)
+    occ = keys != empty
+    T = keys.size
+    want = oracle_mod.pack_keys(expected_coords)
+    assert np.array_equal(np.sort(keys[occ]), np.sort(want)), "table keys differ"
+    n = int(occ.sum())
+    assert np.array_equal(np.sort(idx[occ]), np.arange(n, dtype=np.uint32)), \
+        "pool indices are not a permutation of [0, B)"
+    # linear probing with insertions only: the occupied slots and the total
+    # displacement do not depend on the insertion order, so the concurrent
+    # table must equal the sequential reference exactly in both
+    ref_table, _, ref_disp, _ = oracle_mod.probe_build(want, T)
+    assert np.array_equal(occ, ref_table != empty), "occupied slot sets differ"
+    slots = np.nonzero(occ)[0]
+    home = np.array([oracle_mod.hash_slot(int(k), T) for k in keys[occ]], dtype=np.int64)
+    disp = int(((slots - home) % T).sum())
+    assert disp == ref_disp
+    return disp / max(n, 1)
+
+
+def test_table_structure_matches_sequential_linear_probing(torch_cuda, oracle_mod):
+    torch = torch_cuda
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 4))
+    vol = _gpu_volume(torch, frames, pool_capacity=1 << 15, table_capacity=1 << 16)
+    _integrate_gpu(torch, frames, vol)
+    o = _oracle(oracle_mod, frames)
+    _check_table_structure(oracle_mod, vol, o.coords())
+    vol.close()
+
+
+def test_adversarial_clustered_keys(torch_cuda, oracle_mod):
+    """Keys whose home slots all fall in a window of T/64 slots, filling the
+    table to load 0.5: one long cluster; nothing may be dropped."""
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    torch = torch_cuda
+    T = 1 << 16
+    want = T // 2
+    coords = oracle_mod.clustered_coords(T, 12345, T // 64, (-100, 50, -20), 160, want)
+    assert coords.shape[0] == want
+    vol = TsdfVolume(T // 2, 0.01, 0.04, T)
+    vol.set_instrumentation(True)
+    dup = np.concatenate([coords, coords[::3]])            # repeated keys are found, not re-added
+    perm = np.random.Generator(np.random.PCG64(1)).permutation(dup.shape[0])
+    vol.allocate_blocks(torch.from_numpy(np.ascontiguousarray(dup[perm])).cuda())
+    torch.cuda.synchronize()
+    st = vol.stats()
+    assert vol.block_count() == want
+    assert st["pool_exhausted"] == 0 and st["probe_overflow"] == 0
+    mean_disp = _check_table_structure(oracle_mod, vol, coords)
+    assert mean_disp > want / 2 - T // 64
+    assert st["probe_inserts"] > 0 and st["probe_max"] > 1000
+    print("adversarial: mean displacement", mean_disp, "probe max", st["probe_max"],
+          "mean probe", st["probe_steps"] / st["probe_inserts"])
+    vol.close()
+
+
+def test_load_factor_sweep(torch_cuda, oracle_mod):
+    """Trajectory prefixes of the orbit scene into a fixed 2^15-slot table, up
+    to a final occupancy of 0.5; parity at every checkpoint."""
+    torch = torch_cuda
+    T = 1 << 15
+    full = scenes.orbit_trajectory(n_frames=100, frames=(0, 40))
+    vol = _gpu_volume(torch, full, pool_capacity=T // 2, table_capacity=T)
+    o = oracle_mod.OracleVolume(full.voxel_size, full.trunc)
+    targets = [0.1, 0.2, 0.3, 0.4, 0.5]
+    reached = []
+    d = torch.from_numpy(full.depth).cuda()
+    c = torch.from_numpy(full.rgb).cuda()
+    for f in range(full.n_frames):
+        o.integrate(full.depth[f], full.rgb[f], full.K, full.poses[f])
+        if o.block_count() > T // 2:
+            break
+        vol.integrate(d[f], c[f], full.K, full.poses[f])
+        load = o.block_count() / T
+        if targets and load >= targets[0]:
+            while targets and load >= targets[0]:
+                targets.pop(0)
+            rep = parity.compare_volume(vol.export_blocks(), o.export(), strict=False)
+            parity.check_counters(vol.stats(), o.counters())
+            _check_table_structure(oracle_mod, vol, o.coords())
+            reached.append((f + 1, round(load, 3), rep["blocks"]))
+    print("load sweep (frames, load, blocks):", reached)
+    assert len(reached) >= 4, reached
+    vol.close()
+
+
+@pytest.mark.slow
+def test_room_walk_full_size_sampled(torch_cuda, oracle_mod):
+    """The 300-frame 1280x720 room walk (pool 2^20, table 2^21) in the batch
+    call the benchmark times.  Exact: block set (against a frame-parallel
+    oracle), counters.  Sampled: 96 blocks' sums, chosen from the oracle's own
+    first and last frames."""
+    torch = torch_cuda
+    n = 300
+    frames = scenes.room_random_walk(n_frames=n)
+    vol = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, vol)
+    st = vol.stats()
+    B = vol.block_count()
+    g = vol.export_blocks(fields=("coords",))
+    # sample blocks from the oracle's view of frames 0 and n-1
+    rng = np.random.Generator(np.random.PCG64(2024))
+    keep = []
+    for f in (0, n - 1):
+        o1 = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
+        o1.integrate(frames.depth[f], frames.rgb[f], frames.K, frames.poses[f])
+        c1 = o1.coords()
+        keep.append(c1[rng.choice(c1.shape[0], size=48, replace=False)])
+    keep = np.unique(np.concatenate(keep), axis=0)
+    del frames
+    import os
+    workers = max(2, min(16, (os.cpu_count() or 2)))
+    coords, counters, merged = parity.parallel_oracle("room_random_walk", {"n_frames": n}, n,
+                                                      keep, workers)
+    assert B == coords.shape[0], (B, coords.shape[0])
+    gc = g["coords"][parity.sort_by_coords(g["coords"])]
+    assert np.array_equal(gc, coords)
+    assert st["pool_exhausted"] == 0 and st["probe_overflow"] == 0
+    assert st["valid_points"] == counters["valid_points"]
+    assert st["voxel_updates"] == counters["accumulated"] == counters["passing_samples"]
+    assert st["out_of_range_samples"] == counters["out_of_range_samples"]
+    # sampled sums
+    lut = {tuple(int(v) for v in c): i for i, c in enumerate(g["coords"])}
+    for key, ref in merged.items():
+        i = lut[key]
+        one = vol.export_blocks(first=i, count=1)
+        parity.compare_sums({k: one[k] for k in ("tsdf", "weight", "r", "g", "b")},
+                            {k: ref[k][None, :] for k in ref}, strict=False)
+    print(f"room walk: {B} blocks, {st['voxel_updates']} voxel updates, "
+          f"{len(merged)} sampled blocks match")
+    vol.close()
