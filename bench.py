@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="room_walk")
     ap.add_argument("--frames", type=int, default=0, help="override the trajectory length")
+    ap.add_argument("--group", type=int, default=0,
+                    help="frames per batch call (default: the library's frames per launch)")
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -82,7 +84,7 @@ def workload_config(frames, args) -> dict:
         "table_capacity": frames.table_capacity or "default",
         "seed": frames.seed,
         "l2": "inputs larger than L2 (frames and pool exceed 129 MB)",
-        "step": "reset + (allocate, update) per frame",
+        "step": "reset + (allocate, update) per group of frames",
     }
 
 
@@ -294,22 +296,25 @@ def run_ours(args):
     sptr = stream.cuda_stream
     dptr, cptr = d_dev.data_ptr(), c_dev.data_ptr()
 
+    group = args.group or vol.info["max_frames_per_launch"]
+    groups = [(a, min(n, a + group)) for a in range(0, n, group)]
+
     def one_step(events=None):
         rc = lib.tsdf_reset(h, sptr)
         assert rc == 0
-        for f in range(n):
+        for g, (a, b) in enumerate(groups):
             if events is not None:
-                events[2 * f].record(stream)
-            rc = lib.tsdf_allocate(h, dptr + 4 * f * px, frames.width, frames.height, kp,
-                                   pps[f], sptr)
-            assert rc == 0, binding.load_library().tsdf_last_error()
+                events[2 * g].record(stream)
+            rc = lib.tsdf_allocate_batch(h, b - a, dptr + 4 * a * px, frames.width,
+                                         frames.height, kp, pps[a], sptr)
+            assert rc == 0, lib.tsdf_last_error()
             if events is not None:
-                events[2 * f + 1].record(stream)
-            rc = lib.tsdf_update(h, dptr + 4 * f * px, cptr + 12 * f * px, frames.width,
-                                 frames.height, kp, pps[f], sptr)
-            assert rc == 0, binding.load_library().tsdf_last_error()
+                events[2 * g + 1].record(stream)
+            rc = lib.tsdf_update_batch(h, b - a, dptr + 4 * a * px, cptr + 12 * a * px,
+                                       frames.width, frames.height, kp, pps[a], sptr)
+            assert rc == 0, lib.tsdf_last_error()
         if events is not None:
-            events[2 * n].record(stream)
+            events[2 * len(groups)].record(stream)
 
     # warm-up, and the per-step counts from the first warm-up step
     for i in range(max(args.warmup, 1)):
@@ -321,14 +326,12 @@ def run_ours(args):
     points_per_step = st["valid_points"]
     updates_per_step = st["voxel_updates"]
 
-    # census of distinct voxels per frame (untimed): the algorithmic bytes
-    # of the update kernel are counted per distinct voxel it must modify
-    distinct = census_distinct_voxels(torch, vol, frames, d_dev, c_dev)
+    # census of distinct voxels each update launch modifies (untimed): the
+    # algorithmic bytes of a launch count each such voxel once
+    distinct = census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups)
 
     # timed region
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n + 1)]
-    stage_alloc = 0.0
-    stage_update = 0.0
+    ng = len(groups)
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
@@ -338,7 +341,7 @@ def run_ours(args):
     t_start.record(stream)
     per_step_events = []
     for k in range(args.steps):
-        evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * n + 1)]
+        evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ng + 1)]
         one_step(evk)
         per_step_events.append(evk)
     t_end.record(stream)
@@ -346,34 +349,47 @@ def run_ours(args):
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
+    stage_alloc = 0.0
+    stage_update = 0.0
     for evk in per_step_events:
-        for f in range(n):
-            stage_alloc += evk[2 * f].elapsed_time(evk[2 * f + 1])
-            stage_update += evk[2 * f + 1].elapsed_time(evk[2 * f + 2] if f + 1 < n
-                                                        else evk[2 * n])
+        for g in range(ng):
+            stage_alloc += evk[2 * g].elapsed_time(evk[2 * g + 1])
+            stage_update += evk[2 * g + 1].elapsed_time(evk[2 * g + 2])
     max_ms = max_over_ranks(elapsed_ms, world)
     total_points = sum_over_ranks(points_per_step * args.steps, world)
     value = total_points / (max_ms / 1000.0)
     upd_rate = sum_over_ranks(updates_per_step * args.steps, world) / (max_ms / 1000.0)
 
     # roofline of the update kernel
+    red_peaks = measure_red_peaks(torch)
+    red_peak = max(v["adds_per_s"] for v in red_peaks["hbm_4GB"].values())
     hbm_peak, peak_kind = _peaks()
-    n_update_launches = n * args.steps
+    n_update_launches = ng * args.steps
     upd_ms_avg = stage_update / n_update_launches
     alloc_ms_avg = stage_alloc / n_update_launches
-    bytes_per_launch = (16.0 * points_per_step + 40.0 * distinct["total"]) / n
+    bytes_per_launch = (16.0 * points_per_step + 40.0 * distinct["total"]) / ng
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
     roofline = {
         "bound": "hbm", "kernel": "update_kernel", "achieved": achieved, "peak": hbm_peak,
         "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
         "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch_alg": bytes_per_launch,
         "avg_launch_ms": upd_ms_avg,
-        "atomics": {
-            "issued_per_launch": 5.0 * updates_per_step / n,
-            "algorithmic_per_launch": 5.0 * distinct["total"] / n,
-            "achieved_issued_per_s": 5.0 * updates_per_step / n / (upd_ms_avg / 1000.0),
-        },
     }
+    adds_alg = 5.0 * distinct["total"] / ng
+    red_roof = {
+        "bound": "l2_red", "kernel": "update_kernel", "unit": "float adds/s",
+        "achieved": adds_alg / (upd_ms_avg / 1000.0), "peak": red_peak,
+        "frac": adds_alg / (upd_ms_avg / 1000.0) / red_peak,
+        "algorithmic_adds_per_launch": adds_alg,
+        "issued_adds_per_launch": 5.0 * updates_per_step / ng,
+        "peak_source": "measured live: best red.global.add pattern, 4 GB footprint",
+        "probe": red_peaks,
+    }
+    t_hbm = bytes_per_launch / (hbm_peak * 1e9)
+    t_red = adds_alg / red_peak
+    combined = {"roofline_ms_per_launch": 1000.0 * max(t_hbm, t_red),
+                "binding_term": "hbm" if t_hbm >= t_red else "l2_red",
+                "frac": 1000.0 * max(t_hbm, t_red) / upd_ms_avg}
     result = {
         "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
@@ -381,13 +397,20 @@ def run_ours(args):
         "data": "synthetic",
         "config": dict(workload_config(frames, args), parallelism=f"replicas{world}"),
         "voxel_updates_per_s": upd_rate,
-        "stages_ms_per_frame": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
+        "frames_per_launch": group,
+        "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
+        "stages_ms_per_frame": {"allocate": stage_alloc / (n * args.steps),
+                                "update": stage_update / (n * args.steps)},
         "blocks": blocks, "points_per_step": points_per_step,
         "voxel_updates_per_step": updates_per_step,
         "distinct_voxels_per_step": distinct["total"],
+        "distinct_voxels_per_step_frame_by_frame": distinct["frame_by_frame"],
+        "fixed_divisor_fast_path": vol.info["fixed_divisor_fast_path"],
         "clocks": clk,
-        "gpu_launches": args.steps * (1 + 2 * n),
+        "gpu_launches": args.steps * (1 + 2 * ng),
         "roofline": roofline,
+        "roofline_l2_red": red_roof,
+        "roofline_update_combined": combined,
     }
 
     if not args.no_e2e:
@@ -402,25 +425,75 @@ def run_ours(args):
         print(json.dumps(result), flush=True)
 
 
-def census_distinct_voxels(torch, vol, frames, d_dev, c_dev) -> dict:
-    """Distinct voxels the update kernel modifies in each frame, counted by
-    comparing the weight array before and after each frame."""
+RED_MODES = ((0, "scalar_coalesced", 1), (1, "scalar_scattered", 1), (2, "v4_coalesced", 4),
+             (3, "v4_scattered", 4), (4, "scalar_sector_grouped", 1))
+
+
+def measure_red_peaks(torch) -> dict:
+    """L2 float-reduction throughput (red.global.add), float additions per
+    second, for scalar / 4-wide operands and coalesced / scattered addresses,
+    over an L2-resident (32 MB) and an HBM-resident (4 GB) footprint; best of
+    5 launches each."""
+    import ctypes
+    from hash_blocked_tsdf_gb300 import _build
+    lib = ctypes.CDLL(_build.peaks_library_path())
+    lib.peak_red.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_int, ctypes.c_int,
+                             ctypes.c_int, ctypes.c_void_p]
+    lib.peak_red.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    stream = torch.cuda.current_stream()
+    out = {}
+    for foot, nbytes in (("l2_32MB", 32 << 20), ("hbm_4GB", 4 << 30)):
+        buf = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
+        res = {}
+        for mode, name, width in RED_MODES:
+            blocks, reps = sms * 8, 64
+            best = None
+            for _ in range(6):
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                rc = lib.peak_red(buf.data_ptr(), buf.numel(), mode, reps, blocks,
+                                  stream.cuda_stream)
+                b.record(stream)
+                assert rc == 0, rc
+                torch.cuda.synchronize()
+                ms = a.elapsed_time(b)
+                best = ms if best is None else min(best, ms)
+            ops = blocks * 256 * reps
+            res[name] = {"ops_per_s": ops / (best / 1e3), "adds_per_s": width * ops / (best / 1e3)}
+        out[foot] = res
+        del buf
+    torch.cuda.empty_cache()
+    return out
+
+
+def census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups) -> dict:
+    """Distinct voxels each update launch modifies (a launch covers a group of
+    frames), and for reference the sum over single frames, counted by
+    comparing the weight array before and after."""
     from hash_blocked_tsdf_gb300 import binding
-    vol.reset()
-    ptrs = binding.tsdf_pool_arrays(vol.handle)
+    ptrs = binding.tsdf_get_pool(vol.handle)
     cap = vol.info["pool_capacity"]
     weight = _as_tensor(torch, ptrs["weight"], cap * 512)
     prev = torch.empty_like(weight)
-    per_frame = []
-    for f in range(frames.n_frames):
-        used = vol.block_count() * 512
-        prev[:used].copy_(weight[:used])
-        vol.integrate(d_dev[f], c_dev[f], frames.K, frames.poses[f])
-        used = vol.block_count() * 512
-        per_frame.append(int((weight[:used] != prev[:used]).sum().item()))
+    out = {}
+    for name, grp in (("total", groups), ("frame_by_frame",
+                                          [(f, f + 1) for f in range(frames.n_frames)])):
+        vol.reset()
+        counts = []
+        for a, b in grp:
+            used = vol.block_count() * 512
+            prev[:used].copy_(weight[:used])
+            vol.allocate_batch(d_dev[a:b], frames.K, frames.poses[a:b])
+            vol.update_batch(d_dev[a:b], c_dev[a:b], frames.K, frames.poses[a:b])
+            used = vol.block_count() * 512
+            counts.append(int((weight[:used] != prev[:used]).sum().item()))
+        out[name] = int(sum(counts))
     vol.reset()
     torch.cuda.synchronize()
-    return {"total": int(sum(per_frame)), "per_frame_mean": float(np.mean(per_frame))}
+    del prev
+    return out
 
 
 def _as_tensor(torch, ptr: int, n: int):

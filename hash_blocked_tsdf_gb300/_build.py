@@ -48,6 +48,10 @@ def tsdf_library_path() -> str:
     return os.path.join(PKG_DIR, "libtsdf.so")
 
 
+def peaks_library_path() -> str:
+    return os.path.join(PKG_DIR, "libtsdf_peaks.so")
+
+
 def scene_library_path() -> str:
     return os.path.join(PKG_DIR, "libscene_raycast.so")
 
@@ -105,6 +109,20 @@ def build_tsdf_library(force: bool = False, extra_flags=(), verbose_ptxas: bool 
     return out
 
 
+def build_peaks_library(force: bool = False) -> str:
+    """The L2 reduction-throughput probe used by the benchmark."""
+    src = os.path.join(CSRC, "peaks.cu")
+    out = peaks_library_path()
+    if force or not _newer(out, [src]):
+        tmp = out + f".tmp{os.getpid()}"
+        _run([nvcc()] + NVCC_FLAGS + ["-shared", "-cudart", "static", "-o", tmp, src])
+        os.replace(tmp, out)
+    return out
+
+
 def build_all(force: bool = False) -> None:
-    build_scene_library(force)
-    build_tsdf_library(force)
+    with concurrent.futures.ThreadPoolExecutor(max_workers=3) as ex:
+        futs = [ex.submit(build_scene_library, force), ex.submit(build_tsdf_library, force),
+                ex.submit(build_peaks_library, force)]
+        for f in futs:
+            f.result()

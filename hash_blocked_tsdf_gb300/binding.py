@@ -36,7 +36,9 @@ class TsdfError(RuntimeError):
 class tsdf_info(ctypes.Structure):
     _fields_ = [("pool_capacity", ctypes.c_uint32), ("table_capacity", ctypes.c_uint32),
                 ("voxel_size", ctypes.c_float), ("trunc", ctypes.c_float),
-                ("band_samples", ctypes.c_int32), ("device", ctypes.c_int32)]
+                ("band_samples", ctypes.c_int32), ("device", ctypes.c_int32),
+                ("fixed_divisor_fast_path", ctypes.c_int32),
+                ("max_frames_per_launch", ctypes.c_int32)]
 
 
 class tsdf_pool_view(ctypes.Structure):
@@ -70,6 +72,8 @@ SIGNATURES = {
     "tsdf_update": ([_VP, _VP, _VP, _I, _I, _FP, _FP, _VP], _I),
     "tsdf_integrate_batch": ([_VP, _I, _VP, _VP, _I, _I, _FP, _FP, _VP], _I),
     "tsdf_integrate_batch_host": ([_VP, _I, _VP, _VP, _I, _I, _FP, _FP, _VP], _I),
+    "tsdf_allocate_batch": ([_VP, _I, _VP, _I, _I, _FP, _FP, _VP], _I),
+    "tsdf_update_batch": ([_VP, _I, _VP, _VP, _I, _I, _FP, _FP, _VP], _I),
     "tsdf_allocate_blocks": ([_VP, _VP, _U32, _VP], _I),
     "tsdf_block_count": ([_VP, _VP, ctypes.POINTER(_U32)], _I),
     "tsdf_export_blocks": ([_VP, _VP, _U32, _U32, _VP, _VP, _VP, _VP, _VP, _VP], _I),
@@ -223,6 +227,27 @@ def tsdf_integrate_batch(h, depth, rgb, K, poses, stream=None) -> None:
            "tsdf_integrate_batch")
 
 
+def tsdf_allocate_batch(h, depth, K, poses, stream=None) -> None:
+    import torch
+    n, H, W = depth.shape
+    d = _dev(depth, torch.float32, "depth")
+    k, kp = _floats(K, 4)
+    p, pp = _floats(poses, 16 * n)
+    _check(load_library().tsdf_allocate_batch(h, n, d, W, H, kp, pp, _stream_ptr(stream)),
+           "tsdf_allocate_batch")
+
+
+def tsdf_update_batch(h, depth, rgb, K, poses, stream=None) -> None:
+    import torch
+    n, H, W = depth.shape
+    d = _dev(depth, torch.float32, "depth")
+    c = _dev(rgb, torch.float32, "rgb", (n, H, W, 3))
+    k, kp = _floats(K, 4)
+    p, pp = _floats(poses, 16 * n)
+    _check(load_library().tsdf_update_batch(h, n, d, c, W, H, kp, pp, _stream_ptr(stream)),
+           "tsdf_update_batch")
+
+
 def tsdf_integrate_batch_host(h, depth, rgb, K, poses, stream=None) -> None:
     """depth / rgb: host arrays (numpy, or CPU torch tensors, ideally pinned)."""
     n, H, W = depth.shape
@@ -349,6 +374,12 @@ class TsdfVolume:
 
     def integrate_batch(self, depth, rgb, K, poses, stream=None):
         tsdf_integrate_batch(self.handle, depth, rgb, K, poses, stream)
+
+    def allocate_batch(self, depth, K, poses, stream=None):
+        tsdf_allocate_batch(self.handle, depth, K, poses, stream)
+
+    def update_batch(self, depth, rgb, K, poses, stream=None):
+        tsdf_update_batch(self.handle, depth, rgb, K, poses, stream)
 
     def integrate_batch_host(self, depth, rgb, K, poses, stream=None):
         tsdf_integrate_batch_host(self.handle, depth, rgb, K, poses, stream)

@@ -89,36 +89,84 @@ __device__ __forceinline__ void warp_insert_step(const VolumeView& vol, bool fre
     }
 }
 
-template <bool kInstrument>
-__global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol, FrameView fr)
+// Longest band for which a thread keeps its distinct keys in registers.
+constexpr int kShortBand = 9;
+
+// Block b of the grid covers 256 consecutive pixels (chunk b / n) of frame
+// b % n: the batch's frames are interleaved chunk by chunk.
+//
+// With kShort (bands of at most kShortBand samples) a thread first walks its
+// whole band and keeps the distinct block keys of its passing samples in a
+// small register list; the warp then runs one insert round per list entry
+// (usually two or three) instead of one per band sample.  Longer bands insert
+// step by step.
+template <bool kInstrument, bool kFast, bool kShort>
+__global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
+                                                           const __grid_constant__ FrameBatch fb)
 {
     __shared__ ProbeStats st;
     if (kInstrument) init_probe_stats(&st);
 
-    const int n_pix = fr.width * fr.height;
-    const int pix = blockIdx.x * kThreads + threadIdx.x;
+    const int f = blockIdx.x % fb.n;
+    const int chunk = blockIdx.x / fb.n;
+    const Camera cam = fb.frame[f].cam;
+    const float* depth = fb.frame[f].depth;
+    const int n_pix = fb.width * fb.height;
+    const int pix = chunk * kThreads + threadIdx.x;
     RayPoint p;
     bool valid = false;
     if (pix < n_pix) {
-        const int v = pix / fr.width;
-        const int u = pix - v * fr.width;
-        valid = back_project(fr.cam, u, v, __ldg(fr.depth + pix), p);
+        const int v = pix / fb.width;
+        const int u = pix - v * fb.width;
+        valid = back_project(cam, u, v, __ldg(depth + pix), p);
     }
+    const int steps = 2 * vol.band_half + 1;
     unsigned long long last = kEmptyKey;
     uint32_t out_of_range = 0;
-    for (int i = -vol.band_half; i <= vol.band_half; ++i) {
-        unsigned long long key = kEmptyKey;
-        if (valid) {
-            VoxelSample s;
-            const int status = band_sample(fr.cam, vol.voxel, vol.trunc, p, i, s);
-            if (status == kSamplePass)
-                key = block_key(s.ix, s.iy, s.iz);
-            else if (status == kSampleOutOfRange)
-                ++out_of_range;
+    if (kShort) {
+        unsigned long long keys[kShortBand];
+        int n_keys = 0;
+#pragma unroll
+        for (int j = 0; j < kShortBand; ++j) {
+            keys[j] = kEmptyKey;
+            if (valid && j < steps) {
+                VoxelSample s;
+                const int status = band_sample<kFast, false>(cam, vol.div, p, j - vol.band_half, s);
+                if (status == kSamplePass) {
+                    const unsigned long long key = block_key(s.ix, s.iy, s.iz);
+                    if (key != last) {          // newest key first; static indices only
+#pragma unroll
+                        for (int m = kShortBand - 1; m > 0; --m) keys[m] = keys[m - 1];
+                        keys[0] = key;
+                        ++n_keys;
+                        last = key;
+                    }
+                } else if (status == kSampleOutOfRange) {
+                    ++out_of_range;
+                }
+            }
         }
-        const bool fresh = key != kEmptyKey && key != last;
-        if (key != kEmptyKey) last = key;
-        warp_insert_step<kInstrument>(vol, fresh, key, &st);
+        const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)n_keys);
+        for (int r = 0; r < rounds; ++r) {
+            warp_insert_step<kInstrument>(vol, r < n_keys, keys[0], &st);
+#pragma unroll
+            for (int m = 0; m < kShortBand - 1; ++m) keys[m] = keys[m + 1];
+        }
+    } else {
+        for (int i = -vol.band_half; i <= vol.band_half; ++i) {
+            unsigned long long key = kEmptyKey;
+            if (valid) {
+                VoxelSample s;
+                const int status = band_sample<kFast, false>(cam, vol.div, p, i, s);
+                if (status == kSamplePass)
+                    key = block_key(s.ix, s.iy, s.iz);
+                else if (status == kSampleOutOfRange)
+                    ++out_of_range;
+            }
+            const bool fresh = key != kEmptyKey && key != last;
+            if (key != kEmptyKey) last = key;
+            warp_insert_step<kInstrument>(vol, fresh, key, &st);
+        }
     }
     // one atomic per warp for the out-of-range count
     const uint32_t oor = __reduce_add_sync(0xFFFFFFFFu, out_of_range);
@@ -156,15 +204,32 @@ __global__ void __launch_bounds__(kThreads) allocate_blocks_kernel(VolumeView vo
 
 }  // namespace
 
-cudaError_t launch_allocate(const VolumeView& vol, const FrameView& fr, bool instrument,
+template <bool kInstrument, bool kFast>
+void launch_allocate_t(const VolumeView& vol, const FrameBatch& fb, unsigned grid,
+                       cudaStream_t stream)
+{
+    if (2 * vol.band_half + 1 <= kShortBand)
+        allocate_kernel<kInstrument, kFast, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+    else
+        allocate_kernel<kInstrument, kFast, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+}
+
+cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                             cudaStream_t stream)
 {
-    const int n_pix = fr.width * fr.height;
-    const unsigned grid = (unsigned)((n_pix + kThreads - 1) / kThreads);
-    if (instrument)
-        allocate_kernel<true><<<grid, kThreads, 0, stream>>>(vol, fr);
-    else
-        allocate_kernel<false><<<grid, kThreads, 0, stream>>>(vol, fr);
+    const int n_pix = fb.width * fb.height;
+    const unsigned grid = (unsigned)((n_pix + kThreads - 1) / kThreads) * (unsigned)fb.n;
+    if (instrument) {
+        if (vol.fast_div)
+            launch_allocate_t<true, true>(vol, fb, grid, stream);
+        else
+            launch_allocate_t<true, false>(vol, fb, grid, stream);
+    } else {
+        if (vol.fast_div)
+            launch_allocate_t<false, true>(vol, fb, grid, stream);
+        else
+            launch_allocate_t<false, false>(vol, fb, grid, stream);
+    }
     return cudaGetLastError();
 }
 

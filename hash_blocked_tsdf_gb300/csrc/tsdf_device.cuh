@@ -49,13 +49,61 @@ __device__ __forceinline__ bool back_project(const Camera& c, int u, int v, floa
     return true;
 }
 
+// Division by a divisor y that is fixed for the whole volume (the voxel size
+// or the truncation distance), given r = RN(1 / y): Markstein's
+// reciprocal-and-correction scheme (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(x r) is within an ulp of x / y, the residual x - q0 y is
+// exact in one fused multiply-add, and one more fused multiply-add rounds
+// q0 + r (x - q0 y) to the correctly rounded quotient.  At volume creation the
+// host has the GPU check, for every one of the 2^32 float32 bit patterns x,
+// that what the walk makes of the quotient is the same as with IEEE
+// division: floor(x / voxel) and whether it is a packable voxel index, and
+// min(1, x / trunc) for every x >= -trunc.  Only then is the scheme used.
+__device__ __forceinline__ float div_fixed(float x, float y, float r)
+{
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, y, x);
+    return __fmaf_rn(e, r, q0);
+}
+
+// floor(x / voxel) as the walk uses it (checked exhaustively: same floored
+// value and same range decision as IEEE division for every float32 x).
+template <bool kFast>
+__device__ __forceinline__ float div_voxel(float x, float y, float r)
+{
+    if (kFast) return div_fixed(x, y, r);
+    return __fdiv_rn(x, y);
+}
+
+// x / trunc as the walk uses it (checked exhaustively for x >= -trunc).  The
+// residual of the correction step is only exact while it stays a normal
+// number, i.e. for |x| well above the subnormal range; smaller dividends
+// (which real depths never produce) take the IEEE division.
+template <bool kFast>
+__device__ __forceinline__ float div_trunc(float x, float y, float r)
+{
+    if (kFast && fabsf(x) >= 0x1p-96f) return div_fixed(x, y, r);
+    return __fdiv_rn(x, y);
+}
+
+// Voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1].
+constexpr float kVoxelIndexMin = -8388608.0f;
+constexpr float kVoxelIndexMax = 8388607.0f;
+
 // Band sample `i` (offset i * voxel along the unit ray, i in -k..k): its
 // voxel and truncated signed distance at the voxel centre, or the reason it
 // is skipped.  The same function serves the allocate and the update kernels,
-// which is what makes their occlusion decisions identical.
-__device__ __forceinline__ int band_sample(const Camera& c, float voxel, float trunc,
+// which is what makes their occlusion decisions identical; the allocate
+// kernel, which only needs the voxel, skips the final division.  Written
+// without early exits: every quantity is computed and the status is selected
+// at the end (out-of-range indices are clamped before the integer conversion
+// and never used).
+template <bool kFast, bool kWantTsdf = true>
+__device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
                                            const RayPoint& p, int i, VoxelSample& s)
 {
+    const float voxel = dv.voxel;
     const float off = __fmul_rn((float)i, voxel);
     const float sx = __fadd_rn(p.px, __fmul_rn(off, p.dx));
     const float sy = __fadd_rn(p.py, __fmul_rn(off, p.dy));
@@ -67,16 +115,15 @@ __device__ __forceinline__ int band_sample(const Camera& c, float voxel, float t
                                          __fmul_rn(c.r12, sz)), c.ty);
     const float wz = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, sx), __fmul_rn(c.r21, sy)),
                                          __fmul_rn(c.r22, sz)), c.tz);
-    const float qx = floorf(__fdiv_rn(wx, voxel));
-    const float qy = floorf(__fdiv_rn(wy, voxel));
-    const float qz = floorf(__fdiv_rn(wz, voxel));
-    // voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1]
-    const float lo = -8388608.0f, hi = 8388607.0f;
-    if (!(qx >= lo && qx <= hi && qy >= lo && qy <= hi && qz >= lo && qz <= hi))
-        return kSampleOutOfRange;
-    s.ix = (int)qx;
-    s.iy = (int)qy;
-    s.iz = (int)qz;
+    const float qx = floorf(div_voxel<kFast>(wx, voxel, dv.inv_voxel));
+    const float qy = floorf(div_voxel<kFast>(wy, voxel, dv.inv_voxel));
+    const float qz = floorf(div_voxel<kFast>(wz, voxel, dv.inv_voxel));
+    const bool in_range = qx >= kVoxelIndexMin && qx <= kVoxelIndexMax &&
+                          qy >= kVoxelIndexMin && qy <= kVoxelIndexMax &&
+                          qz >= kVoxelIndexMin && qz <= kVoxelIndexMax;
+    s.ix = (int)fminf(fmaxf(qx, kVoxelIndexMin), kVoxelIndexMax);
+    s.iy = (int)fminf(fmaxf(qy, kVoxelIndexMin), kVoxelIndexMax);
+    s.iz = (int)fminf(fmaxf(qz, kVoxelIndexMin), kVoxelIndexMax);
     // voxel centre relative to the camera position, then its camera z:
     // z_c = (R^T (centre - t))_z = r02 * cx + r12 * cy + r22 * cz
     const float cxr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.ix, 0.5f), voxel), c.tx);
@@ -87,9 +134,9 @@ __device__ __forceinline__ int band_sample(const Camera& c, float voxel, float t
     const float sdf = __fsub_rn(p.d, zc);
     // occlusion test: in front of the camera, and not more than one
     // truncation distance behind the observed surface
-    if (!(zc > 0.0f && sdf >= -trunc)) return kSampleOccluded;
-    s.tsdf = fminf(1.0f, __fdiv_rn(sdf, trunc));
-    return kSamplePass;
+    const bool visible = zc > 0.0f && sdf >= -dv.trunc;
+    if (kWantTsdf) s.tsdf = fminf(1.0f, div_trunc<kFast>(sdf, dv.trunc, dv.inv_trunc));
+    return !in_range ? kSampleOutOfRange : (visible ? kSamplePass : kSampleOccluded);
 }
 
 // Packed key: block coordinate (voxel index >> 3, an arithmetic shift, i.e.

@@ -46,6 +46,12 @@ struct Camera {
     float tx, ty, tz;                                   // t
 };
 
+// The two divisors of the walk with their float reciprocals.
+struct DivisorPair {
+    float voxel, inv_voxel;
+    float trunc, inv_trunc;
+};
+
 // Everything a kernel needs to reach a volume.
 struct VolumeView {
     Entry* table;
@@ -58,24 +64,39 @@ struct VolumeView {
     float* blue;
     uint32_t* pool_counter;     // bump allocator for pool indices
     DeviceCounters* counters;
-    float voxel;
-    float trunc;
+    DivisorPair div;            // voxel size and truncation, with reciprocals
+    bool fast_div;              // the fixed-divisor division was verified exact
     int band_half;              // samples at offsets -band_half .. band_half voxels
 };
 
 struct FrameView {
     const float* depth;         // [height][width]
     const float* rgb;           // [height][width][3] (update only)
-    int width;
-    int height;
     Camera cam;
 };
 
-cudaError_t launch_allocate(const VolumeView& vol, const FrameView& fr, bool instrument,
+// Up to kMaxBatch frames of one size, processed by one launch of each kernel;
+// blocks of threads are ordered region-major, frame-minor, so the frames'
+// work on the same part of the scene runs close together in time.
+constexpr int kMaxBatch = 8;
+struct FrameBatch {
+    int n;
+    int width;
+    int height;
+    FrameView frame[kMaxBatch];
+};
+
+cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                             cudaStream_t stream);
 cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,
                                    bool instrument, cudaStream_t stream);
-cudaError_t launch_update(const VolumeView& vol, const FrameView& fr, cudaStream_t stream);
+cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, cudaStream_t stream);
+// Count the float32 x (all 2^32 bit patterns) for which the walk's use of the
+// fixed-divisor quotient differs from its use of the IEEE quotient x / y
+// (role 0: floored voxel index and range decision; role 1: min(1, x / y) for
+// x >= -y); result added to *mismatches.
+cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int role,
+                                        unsigned long long* mismatches, cudaStream_t stream);
 cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 cudaError_t launch_export_coords(const VolumeView& vol, int32_t* coords, cudaStream_t stream);
 

@@ -31,6 +31,8 @@ struct tsdf_volume {
     float trunc = 0.0f;
     int band_half = 0;
     bool instrument = false;
+    DivisorPair div = {};
+    bool fast_div = false;          // the fixed-divisor division was verified for both divisors
 
     Entry* table = nullptr;
     float* pool = nullptr;          // five arrays of pool_capacity * 512 floats, back to back
@@ -85,8 +87,8 @@ VolumeView view_of(const tsdf_volume* v)
     w.blue = v->pool + 4 * n;
     w.pool_counter = &v->state->pool_counter;
     w.counters = &v->state->counters;
-    w.voxel = v->voxel;
-    w.trunc = v->trunc;
+    w.div = v->div;
+    w.fast_div = v->fast_div;
     w.band_half = v->band_half;
     return w;
 }
@@ -167,18 +169,46 @@ void release(tsdf_volume* v)
     delete v;
 }
 
-int frame_kernels(tsdf_volume* v, const float* depth, const float* rgb, int width, int height,
-                  const Camera& cam, bool do_allocate, bool do_update, cudaStream_t stream)
+// Launch the allocate and/or update kernels over n_frames frames laid out
+// back to back (depth [n][H][W], rgb [n][H][W][3]), at most kMaxBatch frames
+// per launch.  With `interleave`, each group's update follows its allocate;
+// otherwise every allocate launch precedes every update launch.
+int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float* rgb,
+                  int width, int height, const Camera* cams, bool do_allocate, bool do_update,
+                  cudaStream_t stream)
 {
     const VolumeView vol = view_of(v);
-    FrameView fr;
-    fr.depth = depth;
-    fr.rgb = rgb;
-    fr.width = width;
-    fr.height = height;
-    fr.cam = cam;
-    if (do_allocate) TSDF_CUDA(launch_allocate(vol, fr, v->instrument, stream), "allocate kernel");
-    if (do_update) TSDF_CUDA(launch_update(vol, fr, stream), "update kernel");
+    const size_t px = (size_t)width * (size_t)height;
+    for (int first = 0; first < n_frames; first += kMaxBatch) {
+        FrameBatch fb;
+        fb.n = n_frames - first < kMaxBatch ? n_frames - first : kMaxBatch;
+        fb.width = width;
+        fb.height = height;
+        for (int f = 0; f < fb.n; ++f) {
+            fb.frame[f].depth = depth + (first + f) * px;
+            fb.frame[f].rgb = rgb ? rgb + 3 * (first + f) * px : nullptr;
+            fb.frame[f].cam = cams[first + f];
+        }
+        if (do_allocate)
+            TSDF_CUDA(launch_allocate(vol, fb, v->instrument, stream), "allocate kernel");
+        if (do_update) TSDF_CUDA(launch_update(vol, fb, stream), "update kernel");
+    }
+    return TSDF_OK;
+}
+
+int check_batch(tsdf_volume* v, int n_frames, const float* depth, const float* rgb, int width,
+                int height, const float* K, const float* poses, bool need_rgb,
+                std::vector<Camera>* cams)
+{
+    int rc = check_volume(v);
+    if (rc) return rc;
+    if (n_frames < 0) return fail(TSDF_ERR_ARG, "n_frames must be >= 0");
+    if ((rc = check_size(width, height))) return rc;
+    if (n_frames > 0 && (!depth || !poses || (need_rgb && !rgb)))
+        return fail(TSDF_ERR_ARG, "null frame pointer");
+    cams->resize((size_t)n_frames);
+    for (int f = 0; f < n_frames; ++f)
+        if ((rc = make_camera(K, poses + 16 * (size_t)f, &(*cams)[f]))) return rc;
     return TSDF_OK;
 }
 
@@ -186,15 +216,30 @@ int one_frame(tsdf_volume* v, const float* depth, const float* rgb, int width, i
               const float K[4], const float pose[16], void* stream, bool do_allocate,
               bool do_update)
 {
-    int rc = check_volume(v);
+    std::vector<Camera> cams;
+    int rc = check_batch(v, 1, depth, rgb, width, height, K, pose, do_update, &cams);
     if (rc) return rc;
-    if ((rc = check_size(width, height))) return rc;
-    if (!depth) return fail(TSDF_ERR_ARG, "depth is null");
-    if (do_update && !rgb) return fail(TSDF_ERR_ARG, "rgb is null");
-    Camera cam;
-    if ((rc = make_camera(K, pose, &cam))) return rc;
-    return frame_kernels(v, depth, rgb, width, height, cam, do_allocate, do_update,
+    return batch_kernels(v, 1, depth, rgb, width, height, cams.data(), do_allocate, do_update,
                          as_stream(stream));
+}
+
+// Check, for every float32 dividend, that the walk makes the same decisions
+// and values with the fixed-divisor division as with IEEE division, for both
+// of the volume's divisors.
+int verify_divisors(tsdf_volume* v)
+{
+    unsigned long long* bad = &v->state->counters.reserved[0];
+    TSDF_CUDA(cudaMemsetAsync(bad, 0, 2 * sizeof(unsigned long long), 0), "cudaMemsetAsync");
+    TSDF_CUDA(launch_verify_fixed_divisor(v->div.voxel, v->div.inv_voxel, 0, bad, 0),
+              "verify kernel");
+    TSDF_CUDA(launch_verify_fixed_divisor(v->div.trunc, v->div.inv_trunc, 1, bad + 1, 0),
+              "verify kernel");
+    unsigned long long h[2] = {1, 1};
+    TSDF_CUDA(cudaMemcpyAsync(h, bad, sizeof(h), cudaMemcpyDeviceToHost, 0), "cudaMemcpyAsync");
+    TSDF_CUDA(cudaMemsetAsync(bad, 0, 2 * sizeof(unsigned long long), 0), "cudaMemsetAsync");
+    TSDF_CUDA(cudaStreamSynchronize(0), "cudaStreamSynchronize");
+    v->fast_div = h[0] == 0 && h[1] == 0;
+    return TSDF_OK;
 }
 
 }  // namespace
@@ -232,6 +277,10 @@ int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_
     v->voxel = voxel_size;
     v->trunc = trunc;
     v->band_half = (int)ratio;
+    v->div.voxel = voxel_size;
+    v->div.inv_voxel = 1.0f / voxel_size;     // IEEE reciprocal, correctly rounded
+    v->div.trunc = trunc;
+    v->div.inv_trunc = 1.0f / trunc;
     cudaError_t e = cudaGetDevice(&v->device);
     const size_t pool_bytes = 5 * array_floats(v) * sizeof(float);
     if (e == cudaSuccess) e = cudaMalloc(&v->table, T * sizeof(Entry));
@@ -245,6 +294,11 @@ int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_
         int rc = cuda_fail(e, "tsdf_create");
         release(v);
         cudaGetLastError();
+        return rc;
+    }
+    int rc = verify_divisors(v);
+    if (rc) {
+        release(v);
         return rc;
     }
     *out = v;
@@ -274,6 +328,8 @@ int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out)
     out->trunc = vol->trunc;
     out->band_samples = 2 * vol->band_half + 1;
     out->device = vol->device;
+    out->fixed_divisor_fast_path = vol->fast_div ? 1 : 0;
+    out->max_frames_per_launch = kMaxBatch;
     return TSDF_OK;
 }
 
@@ -325,53 +381,59 @@ int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, con
                          int width, int height, const float K[4], const float* poses,
                          void* stream)
 {
-    int rc = check_volume(vol);
-    if (rc) return rc;
-    if (n_frames < 0) return fail(TSDF_ERR_ARG, "n_frames must be >= 0");
-    if (n_frames == 0) return TSDF_OK;
-    if ((rc = check_size(width, height))) return rc;
-    if (!depth || !rgb || !poses) return fail(TSDF_ERR_ARG, "null frame pointer");
-    std::vector<Camera> cams((size_t)n_frames);
-    for (int f = 0; f < n_frames; ++f)
-        if ((rc = make_camera(K, poses + 16 * (size_t)f, &cams[f]))) return rc;
-    const size_t px = (size_t)width * (size_t)height;
-    for (int f = 0; f < n_frames; ++f) {
-        rc = frame_kernels(vol, depth + f * px, rgb + 3 * f * px, width, height, cams[f], true,
-                           true, as_stream(stream));
-        if (rc) return rc;
-    }
-    return TSDF_OK;
+    std::vector<Camera> cams;
+    int rc = check_batch(vol, n_frames, depth, rgb, width, height, K, poses, true, &cams);
+    if (rc || n_frames == 0) return rc;
+    return batch_kernels(vol, n_frames, depth, rgb, width, height, cams.data(), true, true,
+                         as_stream(stream));
+}
+
+int tsdf_allocate_batch(tsdf_volume* vol, int n_frames, const float* depth, int width,
+                        int height, const float K[4], const float* poses, void* stream)
+{
+    std::vector<Camera> cams;
+    int rc = check_batch(vol, n_frames, depth, nullptr, width, height, K, poses, false, &cams);
+    if (rc || n_frames == 0) return rc;
+    return batch_kernels(vol, n_frames, depth, nullptr, width, height, cams.data(), true, false,
+                         as_stream(stream));
+}
+
+int tsdf_update_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
+                      int width, int height, const float K[4], const float* poses, void* stream)
+{
+    std::vector<Camera> cams;
+    int rc = check_batch(vol, n_frames, depth, rgb, width, height, K, poses, true, &cams);
+    if (rc || n_frames == 0) return rc;
+    return batch_kernels(vol, n_frames, depth, rgb, width, height, cams.data(), false, true,
+                         as_stream(stream));
 }
 
 int tsdf_integrate_batch_host(tsdf_volume* vol, int n_frames, const float* depth_host,
                               const float* rgb_host, int width, int height, const float K[4],
                               const float* poses, void* stream)
 {
-    int rc = check_volume(vol);
-    if (rc) return rc;
-    if (n_frames < 0) return fail(TSDF_ERR_ARG, "n_frames must be >= 0");
-    if (n_frames == 0) return TSDF_OK;
-    if ((rc = check_size(width, height))) return rc;
-    if (!depth_host || !rgb_host || !poses) return fail(TSDF_ERR_ARG, "null frame pointer");
-    std::vector<Camera> cams((size_t)n_frames);
-    for (int f = 0; f < n_frames; ++f)
-        if ((rc = make_camera(K, poses + 16 * (size_t)f, &cams[f]))) return rc;
+    std::vector<Camera> cams;
+    int rc = check_batch(vol, n_frames, depth_host, rgb_host, width, height, K, poses, true,
+                         &cams);
+    if (rc || n_frames == 0) return rc;
     const size_t px = (size_t)width * (size_t)height;
-    if ((rc = ensure_staging(vol, px))) return rc;
+    if ((rc = ensure_staging(vol, px * kMaxBatch))) return rc;
     cudaStream_t s = as_stream(stream);
-    for (int f = 0; f < n_frames; ++f) {
-        const int b = f & 1;
+    int group = 0;
+    for (int first = 0; first < n_frames; first += kMaxBatch, ++group) {
+        const int n = n_frames - first < kMaxBatch ? n_frames - first : kMaxBatch;
+        const int b = group & 1;
         float* d_dev = vol->stage[b];
-        float* c_dev = vol->stage[b] + px;
+        float* c_dev = vol->stage[b] + px * kMaxBatch;
         // the copy into buffer b waits for the kernels that last read it
         TSDF_CUDA(cudaStreamWaitEvent(vol->copy_stream, vol->consumed[b], 0), "cudaStreamWaitEvent");
-        TSDF_CUDA(cudaMemcpyAsync(d_dev, depth_host + f * px, px * sizeof(float),
+        TSDF_CUDA(cudaMemcpyAsync(d_dev, depth_host + first * px, n * px * sizeof(float),
                                   cudaMemcpyHostToDevice, vol->copy_stream), "cudaMemcpyAsync(depth)");
-        TSDF_CUDA(cudaMemcpyAsync(c_dev, rgb_host + 3 * f * px, 3 * px * sizeof(float),
+        TSDF_CUDA(cudaMemcpyAsync(c_dev, rgb_host + 3 * first * px, 3 * n * px * sizeof(float),
                                   cudaMemcpyHostToDevice, vol->copy_stream), "cudaMemcpyAsync(rgb)");
         TSDF_CUDA(cudaEventRecord(vol->copied[b], vol->copy_stream), "cudaEventRecord");
         TSDF_CUDA(cudaStreamWaitEvent(s, vol->copied[b], 0), "cudaStreamWaitEvent");
-        rc = frame_kernels(vol, d_dev, c_dev, width, height, cams[f], true, true, s);
+        rc = batch_kernels(vol, n, d_dev, c_dev, width, height, cams.data() + first, true, true, s);
         if (rc) return rc;
         TSDF_CUDA(cudaEventRecord(vol->consumed[b], s), "cudaEventRecord");
     }

@@ -89,6 +89,11 @@ typedef struct tsdf_info {
     float trunc;                /* metres */
     int32_t band_samples;       /* samples per point, 2k + 1 */
     int32_t device;             /* CUDA device ordinal that owns the memory */
+    int32_t fixed_divisor_fast_path;  /* 1: divisions by voxel_size and trunc use a
+                                          reciprocal-and-correction sequence that was
+                                          checked at create to equal IEEE division for
+                                          every float32 dividend; 0: IEEE division */
+    int32_t max_frames_per_launch;    /* frames a batch call packs into one launch */
 } tsdf_info;
 
 /* Device pointers to the pool's five arrays, each float32
@@ -169,17 +174,33 @@ int tsdf_allocate(tsdf_volume* vol, const float* depth, int width, int height,
 int tsdf_update(tsdf_volume* vol, const float* depth, const float* rgb, int width,
                 int height, const float K[4], const float pose[16], void* stream);
 
-/* Integrate n_frames frames in order.  depth: device float32
- * [n_frames][height][width]; rgb: device float32 [n_frames][height][width][3];
- * K: host float[4] shared by all frames; poses: host float[n_frames][16]. */
+/* Integrate n_frames frames.  depth: device float32 [n_frames][height][width];
+ * rgb: device float32 [n_frames][height][width][3]; K: host float[4] shared by
+ * all frames; poses: host float[n_frames][16].  Frames are taken in groups of
+ * up to max_frames_per_launch (tsdf_info): one allocate launch over the group,
+ * then one update launch over the group, whose blocks of threads run image
+ * region by image region, frame-minor, so updates of the same voxels from
+ * neighbouring frames meet in L2.  The result equals integrating the frames
+ * one by one (same blocks, same weights; sums up to float summation order),
+ * except under pool exhaustion, where which blocks are refused depends on the
+ * order in which inserts win pool indices, which is unspecified. */
 int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
                          int width, int height, const float K[4], const float* poses,
                          void* stream);
 
-/* As tsdf_integrate_batch, but depth and rgb are HOST arrays.  Each frame is
- * copied into a double-buffered device staging area owned by the volume on a
- * separate copy stream, overlapping the copy of frame f + 1 with the kernels
- * of frame f.  For the copies to be asynchronous the host arrays must be
+/* The two stages of tsdf_integrate_batch separately, each over all n_frames
+ * frames in launches of up to max_frames_per_launch frames: every allocate
+ * launch of tsdf_allocate_batch, then (when called next on the same stream)
+ * every update launch of tsdf_update_batch.  For timing the stages. */
+int tsdf_allocate_batch(tsdf_volume* vol, int n_frames, const float* depth, int width,
+                        int height, const float K[4], const float* poses, void* stream);
+int tsdf_update_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
+                      int width, int height, const float K[4], const float* poses, void* stream);
+
+/* As tsdf_integrate_batch, but depth and rgb are HOST arrays.  Each group of
+ * frames is copied into a double-buffered device staging area owned by the
+ * volume on a separate copy stream, overlapping the copy of group g + 1 with
+ * the kernels of group g.  For the copies to be asynchronous the host arrays must be
  * page-locked (cudaHostAlloc / cudaHostRegister); pageable memory works but
  * serialises.  The host arrays must stay valid and unchanged until the work on
  * `stream` has finished.  The staging area is allocated on first use (and

@@ -263,34 +263,49 @@ def test_adversarial_clustered_keys(torch_cuda, oracle_mod):
     vol.close()
 
 
+@pytest.mark.slow
 def test_load_factor_sweep(torch_cuda, oracle_mod):
-    """Trajectory prefixes of the orbit scene into a fixed 2^15-slot table, up
-    to a final occupancy of 0.5; parity at every checkpoint."""
+    """Table occupancy 0.1 ... 0.5 on the orbit scene.  Two fixed tables
+    follow the trajectory (2^17 slots for the low loads, 2^16 for the high
+    ones); at the first frame that crosses each target the GPU state is
+    compared with the oracle's (blocks, sums, counters, and the table against
+    sequential linear probing).  The last target, exactly 0.5, is reached by
+    topping the 2^16 table up with extra blocks far from the scene."""
     torch = torch_cuda
-    T = 1 << 15
-    full = scenes.orbit_trajectory(n_frames=100, frames=(0, 40))
-    vol = _gpu_volume(torch, full, pool_capacity=T // 2, table_capacity=T)
+    full = scenes.orbit_trajectory(n_frames=100)
+    small = _gpu_volume(torch, full, pool_capacity=1 << 15, table_capacity=1 << 16)
+    large = _gpu_volume(torch, full, pool_capacity=1 << 16, table_capacity=1 << 17)
+    plan = [(0.1, large, 1 << 17), (0.2, large, 1 << 17), (0.3, small, 1 << 16),
+            (0.4, small, 1 << 16)]
     o = oracle_mod.OracleVolume(full.voxel_size, full.trunc)
-    targets = [0.1, 0.2, 0.3, 0.4, 0.5]
-    reached = []
     d = torch.from_numpy(full.depth).cuda()
     c = torch.from_numpy(full.rgb).cuda()
+    reached = []
     for f in range(full.n_frames):
         o.integrate(full.depth[f], full.rgb[f], full.K, full.poses[f])
-        if o.block_count() > T // 2:
-            break
-        vol.integrate(d[f], c[f], full.K, full.poses[f])
-        load = o.block_count() / T
-        if targets and load >= targets[0]:
-            while targets and load >= targets[0]:
-                targets.pop(0)
+        for vol in (small, large):
+            vol.integrate(d[f], c[f], full.K, full.poses[f])
+        while plan and o.block_count() / plan[0][2] >= plan[0][0]:
+            target, vol, T = plan.pop(0)
             rep = parity.compare_volume(vol.export_blocks(), o.export(), strict=False)
             parity.check_counters(vol.stats(), o.counters())
             _check_table_structure(oracle_mod, vol, o.coords())
-            reached.append((f + 1, round(load, 3), rep["blocks"]))
-    print("load sweep (frames, load, blocks):", reached)
-    assert len(reached) >= 4, reached
-    vol.close()
+            reached.append((target, f + 1, round(o.block_count() / T, 3), rep["blocks"]))
+    assert not plan, f"targets not reached: {plan}"
+    # top up to exactly half full with blocks far outside the scene
+    B = o.block_count()
+    extra = np.stack(np.meshgrid(np.arange(1000, 1064), np.arange(0, 64), np.arange(0, 16),
+                                 indexing="ij"), axis=-1).reshape(-1, 3)[: (1 << 15) - B]
+    small.allocate_blocks(torch.from_numpy(np.ascontiguousarray(extra, dtype=np.int32)).cuda())
+    torch.cuda.synchronize()
+    st = small.stats()
+    assert small.block_count() == 1 << 15
+    assert st["pool_exhausted"] == 0 and st["probe_overflow"] == 0
+    _check_table_structure(oracle_mod, small, np.concatenate([o.coords(), extra]))
+    reached.append((0.5, full.n_frames, 0.5, 1 << 15))
+    print("load sweep (target, frames, load, blocks):", reached)
+    small.close()
+    large.close()
 
 
 @pytest.mark.slow
@@ -337,4 +352,17 @@ def test_room_walk_full_size_sampled(torch_cuda, oracle_mod):
                             {k: ref[k][None, :] for k in ref}, strict=False)
     print(f"room walk: {B} blocks, {st['voxel_updates']} voxel updates, "
           f"{len(merged)} sampled blocks match")
+    vol.close()
+
+
+@pytest.mark.parametrize("voxel,trunc", [(0.02, 0.08), (0.01, 0.04), (0.005, 0.02),
+                                         (0.004, 0.016)])
+def test_fixed_divisor_fast_path_verified(torch_cuda, voxel, trunc):
+    """At create the library checks, over all 2^32 float32 dividends, that the
+    reciprocal-and-correction division gives the walk the same floored voxel
+    indices and the same tsdf values as IEEE division; for the workloads'
+    divisors that check must pass (the parity tests then run on that path)."""
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    vol = TsdfVolume(64, voxel, trunc)
+    assert vol.info["fixed_divisor_fast_path"] == 1
     vol.close()
