@@ -83,9 +83,18 @@ def workload_config(frames, args) -> dict:
         "pool_capacity": frames.pool_capacity,
         "table_capacity": frames.table_capacity or "default",
         "seed": frames.seed,
-        "l2": "inputs larger than L2 (frames and pool exceed 129 MB)",
+        "l2": _l2_note(frames),
         "step": "reset + (allocate, update) per group of frames",
     }
+
+
+def _l2_note(frames) -> str:
+    step_bytes = frames.depth.nbytes + frames.rgb.nbytes + 20 * 512 * frames.pool_capacity
+    if frames.depth.nbytes + frames.rgb.nbytes > (129 << 20):
+        return (f"inputs larger than L2: {frames.depth.nbytes + frames.rgb.nbytes >> 20} MB of "
+                f"frames per step, {20 * 512 * frames.pool_capacity >> 20} MB pool; no flush")
+    return (f"not flushed: step inputs {step_bytes >> 20} MB (frames + pool) may stay in the "
+            f"129 MB L2 between steps")
 
 
 # ----------------------------------------------------------------------------
@@ -360,22 +369,33 @@ def run_ours(args):
     value = total_points / (max_ms / 1000.0)
     upd_rate = sum_over_ranks(updates_per_step * args.steps, world) / (max_ms / 1000.0)
 
-    # roofline of the update kernel
+    # rooflines.  Units as defined for the integrate path: per frame, the
+    # update kernel must read 16 B per valid point and read-modify-write the
+    # five 4-byte sums of every distinct voxel the frame touches (40 B), and
+    # issue 5 float additions per such voxel; a launch covers `group` frames.
     red_peaks = measure_red_peaks(torch)
     red_peak = max(v["adds_per_s"] for v in red_peaks["hbm_4GB"].values())
     hbm_peak, peak_kind = _peaks()
     n_update_launches = ng * args.steps
     upd_ms_avg = stage_update / n_update_launches
     alloc_ms_avg = stage_alloc / n_update_launches
-    bytes_per_launch = (16.0 * points_per_step + 40.0 * distinct["total"]) / ng
+    u_frames = distinct["frame_by_frame"]
+    bytes_per_launch = (16.0 * points_per_step + 40.0 * u_frames) / ng
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
+    prof_upd = _profile_record("update_kernel_room_walk_1280x720.md",
+                               ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
+    prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md",
+                                 ["tsdf_alloc.cu", "tsdf_device.cuh", "tsdf_internal.h"])
+    same_shape = frames.width == 1280 and frames.height == 720 and group == 8
     roofline = {
         "bound": "hbm", "kernel": "update_kernel", "achieved": achieved, "peak": hbm_peak,
-        "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": None,
-        "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_launch_alg": bytes_per_launch,
-        "avg_launch_ms": upd_ms_avg,
+        "unit": "GB/s", "frac": achieved / hbm_peak,
+        "traffic": (prof_upd.get("traffic_bytes_per_launch") if same_shape else None),
+        "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS)",
+        "bytes_per_launch_alg": bytes_per_launch, "avg_launch_ms": upd_ms_avg,
+        "units": "per frame: 16 B per valid point + 40 B per distinct voxel of the frame",
     }
-    adds_alg = 5.0 * distinct["total"] / ng
+    adds_alg = 5.0 * u_frames / ng
     red_roof = {
         "bound": "l2_red", "kernel": "update_kernel", "unit": "float adds/s",
         "achieved": adds_alg / (upd_ms_avg / 1000.0), "peak": red_peak,
@@ -390,6 +410,28 @@ def run_ours(args):
     combined = {"roofline_ms_per_launch": 1000.0 * max(t_hbm, t_red),
                 "binding_term": "hbm" if t_hbm >= t_red else "l2_red",
                 "frac": 1000.0 * max(t_hbm, t_red) / upd_ms_avg}
+    # stricter: a launch's voxels counted once for all of its frames
+    u_union = distinct["total"] / ng
+    b_union = (16.0 * points_per_step / ng + 40.0 * u_union)
+    union = {"bytes_per_launch_alg": b_union,
+             "frac_hbm": b_union / (upd_ms_avg / 1000.0) / 1e9 / hbm_peak,
+             "frac_l2_red": 5.0 * u_union / (upd_ms_avg / 1000.0) / red_peak}
+    # the allocate kernel is bound by instruction issue: warp instructions per
+    # launch (ncu count for this kernel source) against 4 issue slots per SM
+    # per cycle at the SM clock sampled over the timed region
+    alloc_roof = None
+    sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if same_shape and prof_alloc.get("warp_instructions_per_launch"):
+        ipl = prof_alloc["warp_instructions_per_launch"]
+        peak_issue = sms * 4 * sm_mhz * 1e6
+        ach = ipl / (alloc_ms_avg / 1000.0)
+        alloc_roof = {"bound": "alu", "kernel": "allocate_kernel", "unit": "warp instructions/s",
+                      "achieved": ach, "peak": peak_issue, "frac": ach / peak_issue,
+                      "warp_instructions_per_launch": ipl,
+                      "peak_source": f"{sms} SMs x 4 issue slots x sampled {sm_mhz:.0f} MHz",
+                      "traffic": prof_alloc.get("traffic_bytes_per_launch")}
+
     result = {
         "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_ms / args.steps,
@@ -411,6 +453,8 @@ def run_ours(args):
         "roofline": roofline,
         "roofline_l2_red": red_roof,
         "roofline_update_combined": combined,
+        "roofline_update_launch_union": union,
+        "roofline_allocate": alloc_roof,
     }
 
     if not args.no_e2e:
@@ -465,6 +509,33 @@ def measure_red_peaks(torch) -> dict:
         out[foot] = res
         del buf
     torch.cuda.empty_cache()
+    return out
+
+
+def _profile_record(name: str, sources) -> dict:
+    """Figures recorded in a committed ncu summary under profiles/, used only
+    while the kernel's source is unchanged since the capture (matching hash)."""
+    import hashlib
+    path = os.path.join(REPO, "profiles", name)
+    try:
+        text = open(path).read()
+    except OSError:
+        return {}
+    h = hashlib.sha256()
+    for src in sources:
+        with open(os.path.join(REPO, "hash_blocked_tsdf_gb300", "csrc", src), "rb") as fh:
+            h.update(fh.read())
+    rec = {}
+    for line in text.splitlines():
+        if ":" in line and not line.startswith(("|", " ", "#")):
+            k, v = line.split(":", 1)
+            rec[k.strip()] = v.strip()
+    if rec.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
+        return {}
+    out = {}
+    for k in ("traffic_bytes_per_launch", "warp_instructions_per_launch"):
+        if k in rec:
+            out[k] = float(rec[k])
     return out
 
 
