@@ -78,6 +78,7 @@ SIGNATURES = {
     "tsdf_block_count": ([_VP, _VP, ctypes.POINTER(_U32)], _I),
     "tsdf_export_blocks": ([_VP, _VP, _U32, _U32, _VP, _VP, _VP, _VP, _VP, _VP], _I),
     "tsdf_export_table": ([_VP, _VP, _U32, _VP, _VP], _I),
+    "tsdf_export_block_coords_noalloc": ([_VP, _VP, _U32, _U32, _VP], _I),
     "tsdf_get_stats": ([_VP, _VP, ctypes.POINTER(tsdf_stats)], _I),
     "tsdf_clear_stats": ([_VP, _VP], _I),
     "tsdf_set_instrumentation": ([_VP, _I], _I),
@@ -308,6 +309,21 @@ def tsdf_export_blocks(h, first: int = 0, count: Optional[int] = None, stream=No
             ptrs.append(None)
     _check(load_library().tsdf_export_blocks(h, _stream_ptr(stream), first, count, *ptrs),
            "tsdf_export_blocks")
+    return out
+
+
+NOALLOC_MAX_BLOCKS = 65536
+
+
+def tsdf_export_block_coords_noalloc(h, first: int, count: int, stream=None) -> np.ndarray:
+    """Block coordinates of pool blocks [first, first + count), int32 [count, 3],
+    through the library's built-in scratch array: no device memory is
+    allocated (for callers whose device memory is spoken for).  count must not
+    exceed NOALLOC_MAX_BLOCKS."""
+    out = np.zeros((count, 3), np.int32)
+    _check(load_library().tsdf_export_block_coords_noalloc(h, _stream_ptr(stream), first, count,
+                                                           out.ctypes.data),
+           "tsdf_export_block_coords_noalloc")
     return out
 
 

@@ -101,3 +101,10 @@ cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 cudaError_t launch_export_coords(const VolumeView& vol, int32_t* coords, cudaStream_t stream);
 
 }  // namespace tsdf
+
+// Internal accessors for translation units other than the volume's own.
+struct tsdf_volume;
+namespace tsdf {
+VolumeView volume_view(const tsdf_volume* vol);
+int record_error(int code, const char* message);   // sets tsdf_last_error, returns code
+}  // namespace tsdf

@@ -244,6 +244,11 @@ int verify_divisors(tsdf_volume* v)
 
 }  // namespace
 
+namespace tsdf {
+VolumeView volume_view(const tsdf_volume* vol) { return view_of(vol); }
+int record_error(int code, const char* message) { return fail(code, message); }
+}  // namespace tsdf
+
 extern "C" {
 
 const char* tsdf_last_error(void) { return g_last_error.c_str(); }

@@ -228,6 +228,25 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
                        int32_t* coords, float* tsdf, float* weight, float* r, float* g,
                        float* b);
 
+/* Block coordinates of pool blocks [first, first + count) into coords
+ * (host int32 [count][3]), like the coords output of tsdf_export_blocks, but
+ * without allocating any memory: for callers that cannot let the library
+ * call cudaMalloc (device memory owned by a caching allocator that has
+ * reserved nearly all of it, a fixed device-memory budget, threads that must
+ * not stall in the allocator).  The paper has no counterpart; it is a
+ * service of this library.  The coordinates pass through a scratch array
+ * compiled into the library (TSDF_NOALLOC_MAX_BLOCKS blocks, 768 KB, held by
+ * every GPU that loads the library until exit), so count must not exceed
+ * TSDF_NOALLOC_MAX_BLOCKS (else TSDF_ERR_ARG, nothing done); first + count
+ * must not exceed tsdf_block_count.  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) and should come before any
+ * stream capture begins.  Every call shares the array: calls whose work
+ * overlaps on the GPU (other streams, other threads) race.  Synchronises
+ * `stream`. */
+#define TSDF_NOALLOC_MAX_BLOCKS 65536u
+int tsdf_export_block_coords_noalloc(tsdf_volume* vol, void* stream, uint32_t first,
+                                     uint32_t count, int32_t* coords);
+
 /* Copy the raw hash table to the host after synchronising `stream`: keys
  * uint64 [table_capacity] (TSDF_EMPTY_KEY for an empty slot) and indices
  * uint32 [table_capacity].  `capacity` must equal the table capacity. Either
