@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced"],
+                    default="adaptive", help="how the library's update reaches the pool")
     return ap.parse_args()
 
 
@@ -294,6 +296,7 @@ def run_ours(args):
     c_dev = torch.from_numpy(frames.rgb).cuda()
     vol = TsdfVolume(frames.pool_capacity, frames.voxel_size, frames.trunc,
                      frames.table_capacity)
+    vol.set_update_kernel(args.update_kernel)
     h = vol.handle
     lib = binding.load_library()
     K = np.ascontiguousarray(frames.K, dtype=np.float32)
@@ -382,13 +385,15 @@ def run_ours(args):
     u_frames = distinct["frame_by_frame"]
     bytes_per_launch = (16.0 * points_per_step + 40.0 * u_frames) / ng
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
-    prof_upd = _profile_record("update_kernel_room_walk_1280x720.md",
+    upd_kernel = ("update_kernel" if args.update_kernel == "per_sample"
+                  else "update_rows_kernel")
+    prof_upd = _profile_record(f"{upd_kernel}_room_walk_1280x720.md",
                                ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md",
                                  ["tsdf_alloc.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     same_shape = frames.width == 1280 and frames.height == 720 and group == 8
     roofline = {
-        "bound": "hbm", "kernel": "update_kernel", "achieved": achieved, "peak": hbm_peak,
+        "bound": "hbm", "kernel": upd_kernel, "achieved": achieved, "peak": hbm_peak,
         "unit": "GB/s", "frac": achieved / hbm_peak,
         "traffic": (prof_upd.get("traffic_bytes_per_launch") if same_shape else None),
         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS)",
@@ -397,7 +402,7 @@ def run_ours(args):
     }
     adds_alg = 5.0 * u_frames / ng
     red_roof = {
-        "bound": "l2_red", "kernel": "update_kernel", "unit": "float adds/s",
+        "bound": "l2_red", "kernel": upd_kernel, "unit": "float adds/s",
         "achieved": adds_alg / (upd_ms_avg / 1000.0), "peak": red_peak,
         "frac": adds_alg / (upd_ms_avg / 1000.0) / red_peak,
         "algorithmic_adds_per_launch": adds_alg,
@@ -440,6 +445,7 @@ def run_ours(args):
         "config": dict(workload_config(frames, args), parallelism=f"replicas{world}"),
         "voxel_updates_per_s": upd_rate,
         "frames_per_launch": group,
+        "update_kernel": args.update_kernel,
         "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
         "stages_ms_per_frame": {"allocate": stage_alloc / (n * args.steps),
                                 "update": stage_update / (n * args.steps)},

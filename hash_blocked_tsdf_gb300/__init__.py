@@ -9,7 +9,8 @@ from .binding import (TsdfError, TsdfVolume, load_library, tsdf_allocate, tsdf_a
                       tsdf_block_count, tsdf_clear_stats, tsdf_create, tsdf_destroy,
                       tsdf_export_blocks, tsdf_export_table, tsdf_get_info, tsdf_get_pool, tsdf_get_stats,
                       tsdf_integrate, tsdf_integrate_batch, tsdf_integrate_batch_host,
-                      tsdf_reset, tsdf_set_instrumentation, tsdf_update)
+                      tsdf_reset, tsdf_set_instrumentation, tsdf_set_update_kernel,
+                      tsdf_update)
 
 __all__ = [
     "TsdfError", "TsdfVolume", "load_library", "tsdf_allocate", "tsdf_allocate_batch",
@@ -17,5 +18,5 @@ __all__ = [
     "tsdf_block_count", "tsdf_clear_stats", "tsdf_create", "tsdf_destroy", "tsdf_export_blocks",
     "tsdf_export_table", "tsdf_get_info", "tsdf_get_pool", "tsdf_get_stats", "tsdf_integrate",
     "tsdf_integrate_batch", "tsdf_integrate_batch_host", "tsdf_reset",
-    "tsdf_set_instrumentation", "tsdf_update",
+    "tsdf_set_instrumentation", "tsdf_set_update_kernel", "tsdf_update",
 ]

@@ -82,6 +82,7 @@ SIGNATURES = {
     "tsdf_get_stats": ([_VP, _VP, ctypes.POINTER(tsdf_stats)], _I),
     "tsdf_clear_stats": ([_VP, _VP], _I),
     "tsdf_set_instrumentation": ([_VP, _I], _I),
+    "tsdf_set_update_kernel": ([_VP, _I], _I),
     "tsdf_last_error": ([], ctypes.c_char_p),
 }
 
@@ -353,6 +354,21 @@ def tsdf_set_instrumentation(h, on: bool) -> None:
     _check(load_library().tsdf_set_instrumentation(h, 1 if on else 0), "tsdf_set_instrumentation")
 
 
+UPDATE_ADAPTIVE = 0
+UPDATE_PER_SAMPLE = 1
+UPDATE_PRE_REDUCED = 2
+UPDATE_KERNELS = {"adaptive": UPDATE_ADAPTIVE, "per_sample": UPDATE_PER_SAMPLE,
+                  "pre_reduced": UPDATE_PRE_REDUCED}
+
+
+def tsdf_set_update_kernel(h, kind) -> None:
+    """Select how updates reach the pool: "adaptive" (default: each tile
+    pre-reduces where samples crowd into voxels), "per_sample" or
+    "pre_reduced"; or the header's integer constants."""
+    k = UPDATE_KERNELS[kind] if isinstance(kind, str) else int(kind)
+    _check(load_library().tsdf_set_update_kernel(h, k), "tsdf_set_update_kernel")
+
+
 # ----------------------------------------------------------------------------
 # Convenience wrapper
 # ----------------------------------------------------------------------------
@@ -420,3 +436,6 @@ class TsdfVolume:
 
     def set_instrumentation(self, on: bool):
         tsdf_set_instrumentation(self.handle, on)
+
+    def set_update_kernel(self, kind):
+        tsdf_set_update_kernel(self.handle, kind)

@@ -91,6 +91,26 @@ __device__ __forceinline__ float div_trunc(float x, float y, float r)
 constexpr float kVoxelIndexMin = -8388608.0f;
 constexpr float kVoxelIndexMax = 8388607.0f;
 
+// Camera-frame depth of the centre of voxel (ix, iy, iz):
+// z_c = (R^T (centre - t))_z = r02 * cx + r12 * cy + r22 * cz, with the
+// centre taken relative to the camera position.
+__device__ __forceinline__ float centre_depth(const Camera& c, float voxel, int ix, int iy, int iz)
+{
+    const float cxr = __fsub_rn(__fmul_rn(__fadd_rn((float)ix, 0.5f), voxel), c.tx);
+    const float cyr = __fsub_rn(__fmul_rn(__fadd_rn((float)iy, 0.5f), voxel), c.ty);
+    const float czr = __fsub_rn(__fmul_rn(__fadd_rn((float)iz, 0.5f), voxel), c.tz);
+    return __fadd_rn(__fadd_rn(__fmul_rn(c.r02, cxr), __fmul_rn(c.r12, cyr)),
+                     __fmul_rn(c.r22, czr));
+}
+
+// The truncated signed distance min(1, sdf / trunc) of a sample whose pixel
+// depth is d and whose voxel centre lies at camera depth zc.
+template <bool kFast>
+__device__ __forceinline__ float truncated_sdf(const DivisorPair& dv, float d, float zc)
+{
+    return fminf(1.0f, div_trunc<kFast>(__fsub_rn(d, zc), dv.trunc, dv.inv_trunc));
+}
+
 // Band sample `i` (offset i * voxel along the unit ray, i in -k..k): its
 // voxel and truncated signed distance at the voxel centre, or the reason it
 // is skipped.  The same function serves the allocate and the update kernels,
@@ -124,18 +144,12 @@ __device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& d
     s.ix = (int)fminf(fmaxf(qx, kVoxelIndexMin), kVoxelIndexMax);
     s.iy = (int)fminf(fmaxf(qy, kVoxelIndexMin), kVoxelIndexMax);
     s.iz = (int)fminf(fmaxf(qz, kVoxelIndexMin), kVoxelIndexMax);
-    // voxel centre relative to the camera position, then its camera z:
-    // z_c = (R^T (centre - t))_z = r02 * cx + r12 * cy + r22 * cz
-    const float cxr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.ix, 0.5f), voxel), c.tx);
-    const float cyr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iy, 0.5f), voxel), c.ty);
-    const float czr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iz, 0.5f), voxel), c.tz);
-    const float zc = __fadd_rn(__fadd_rn(__fmul_rn(c.r02, cxr), __fmul_rn(c.r12, cyr)),
-                               __fmul_rn(c.r22, czr));
+    const float zc = centre_depth(c, voxel, s.ix, s.iy, s.iz);
     const float sdf = __fsub_rn(p.d, zc);
     // occlusion test: in front of the camera, and not more than one
     // truncation distance behind the observed surface
     const bool visible = zc > 0.0f && sdf >= -dv.trunc;
-    if (kWantTsdf) s.tsdf = fminf(1.0f, div_trunc<kFast>(sdf, dv.trunc, dv.inv_trunc));
+    if (kWantTsdf) s.tsdf = truncated_sdf<kFast>(dv, p.d, zc);
     return !in_range ? kSampleOutOfRange : (visible ? kSamplePass : kSampleOccluded);
 }
 

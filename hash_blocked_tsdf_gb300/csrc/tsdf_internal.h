@@ -67,6 +67,15 @@ struct VolumeView {
     DivisorPair div;            // voxel size and truncation, with reciprocals
     bool fast_div;              // the fixed-divisor division was verified exact
     int band_half;              // samples at offsets -band_half .. band_half voxels
+    // Adaptive update: the dense 16 x 16 pixel tiles of the current update
+    // launch, (frame << 24 | tile), listed by the per-sample kernel for the
+    // pre-reducing one; dense_next is the latter's work counter.
+    uint32_t* dense_list;       // [dense_capacity]
+    uint32_t dense_capacity;
+    uint32_t* dense_count;
+    uint32_t* dense_next;
+    uint32_t* dense_done;       // blocks of the pre-reducing kernel that have finished;
+                                // the last one sets all three back to zero
 };
 
 struct FrameView {
@@ -79,6 +88,7 @@ struct FrameView {
 // blocks of threads are ordered region-major, frame-minor, so the frames'
 // work on the same part of the scene runs close together in time.
 constexpr int kMaxBatch = 8;
+constexpr uint32_t kDenseListCapacity = 1u << 20;
 struct FrameBatch {
     int n;
     int width;
@@ -90,7 +100,9 @@ cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool in
                             cudaStream_t stream);
 cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,
                                    bool instrument, cudaStream_t stream);
-cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, cudaStream_t stream);
+// kind: TSDF_UPDATE_ADAPTIVE, TSDF_UPDATE_PER_SAMPLE or TSDF_UPDATE_PRE_REDUCED.
+cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
+                          cudaStream_t stream);
 // Count the float32 x (all 2^32 bit patterns) for which the walk's use of the
 // fixed-divisor quotient differs from its use of the IEEE quotient x / y
 // (role 0: floored voxel index and range decision; role 1: min(1, x / y) for

@@ -1,21 +1,40 @@
-// Update kernel ("What Irregularity Costs", design section, integration:
+// Update kernels ("What Irregularity Costs", design section, integration:
 // the regular stage; accumulation: sums, not running means).
 //
-// A block of 256 threads owns a 16 x 16 pixel tile of one frame of the batch,
-// each warp an 8 x 4 patch of it.  The grid runs tile-major, frame-minor: the
-// batch's frames update the same region of the scene (mostly the same
-// voxels, since consecutive views overlap) within a short window, so those
-// voxels' lines take all of the batch's reductions in L2 and go back to HBM
-// once, not once per frame.  Every thread walks its pixel's truncation band
-// with the same band_sample() as the allocate kernel, finds each passing
-// sample's block with one lookup per new key (almost always a first-probe
-// hit), and adds (tsdf, 1, r, g, b) into the five SoA arrays with
-// red.global.add.f32.
+// By default (adaptive) both kernels run on every batch and split the frame
+// by 16 x 16 pixel tiles: a tile whose pixels are small against the voxels
+// (at least half of them see a voxel edge 5 or more pixels wide) has its
+// samples crowd into few voxels and is pre-reduced by update_rows_kernel;
+// every other tile is left to update_kernel.
 //
-// Reductions are issued per sample.  Pre-summing rows of voxels in shared
-// memory before the reductions cuts the L2 requests about three-fold, but on
-// this workload it costs more issue slots than it saves L2 time (measured on
-// GB300: 0.21-0.25 ms against 0.15 ms per 1280x720 frame).
+// update_kernel (per sample): every thread walks one pixel's band, looks
+// up each passing sample's block (one lookup per new key, almost always a
+// first-probe hit) and adds (tsdf, 1, r, g, b) with five red.global.add.f32.
+// Blocks of 256 threads own 16 x 16 pixel tiles of one frame, each warp an
+// 8 x 4 patch.  Where samples rarely share a voxel this is bound by the L2's
+// rate of reduction sectors, and nothing on chip would save much.
+//
+// update_rows_kernel (pre-reducing): a block of 192 threads owns an 8 x 8
+// pixel tile of one frame, three threads per pixel, each walking one third
+// of the pixel's truncation band (a warp covers an 8 x 4 pixel patch).  The
+// block keeps a shared table of the voxel rows its samples fall in (a row is
+// the 8 voxels of a block that share ly and lz: exactly one 32-byte sector of
+// each pool array), and for every voxel of a row two 64-bit masks: which of
+// the tile's pixels put a sample in it, and which put a second one (a ray
+// puts at most two samples in a voxel: samples are one voxel edge apart and a
+// voxel is sqrt(3) edges across).  That takes one shared atomicOr per sample.
+// Afterwards every touched voxel recomputes its samples' truncated distances
+// from the pixel depths and its own centre -- the walk's arithmetic, so the
+// same values -- sums them with the pixels' colours in pixel order, and adds
+// its five sums to the pool; the voxels of a row are flushed by adjacent
+// lanes, so each row reaches L2 as one reduction per array instead of one
+// per sample and array.  Rows that find no slot in the shared table add
+// their samples directly.
+//
+// Both grids run tile-major, frame-minor, so the frames' updates of the same
+// voxels meet in L2.
+#include <atomic>
+
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -30,7 +49,34 @@ __device__ __forceinline__ void red_add(float* addr, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-template <bool kFast>
+// Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
+// at least half of its valid pixels (finite depth > 0) see a voxel edge at
+// least w pixels wide (voxel * fx >= w * depth): there samples crowd into few
+// voxels and summing them on chip pays; below, they rarely share a voxel and
+// direct additions are cheaper.  Measured on GB300 the crossing lies near 5
+// pixels for launches of several frames (the frames' samples of a voxel
+// meet in L2 as well) and near 10 for a single frame.  The rule and its
+// inputs are the same in both update kernels, so every tile is integrated by
+// exactly one of them.  Launches below kAdaptiveMinPixels pixels use the
+// per-sample kernel alone (there launch latency dominates).
+constexpr uint32_t kAdaptiveMinPixels = 1u << 18;
+
+__device__ __forceinline__ float dense_width(int n_frames) { return n_frames >= 4 ? 5.0f : 10.0f; }
+
+__device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
+
+__device__ __forceinline__ bool dense_pixel(float d, float voxel, float fx, int n_frames)
+{
+    return valid_depth(d) && __fmul_rn(voxel, fx) >= __fmul_rn(dense_width(n_frames), d);
+}
+
+__device__ __forceinline__ bool dense_tile(uint32_t n_valid, uint32_t n_dense)
+{
+    return n_valid != 0 && 2 * n_dense >= n_valid;
+}
+
+// kSparseOnly: leave dense tiles to update_rows_kernel (adaptive mode).
+template <bool kFast, bool kSparseOnly>
 __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                                                          const __grid_constant__ FrameBatch fb)
 {
@@ -45,12 +91,31 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     const int u = (tile % tiles_x) * kTileW + (w & 1) * 8 + (l & 7);
     const int v = (tile / tiles_x) * kTileH + (w >> 1) * 4 + (l >> 3);
 
+    const bool inside = u < fb.width && v < fb.height;
+    const float depth = inside ? __ldg(fb.frame[f].depth + (size_t)v * fb.width + u) : 0.0f;
+    if (kSparseOnly) {
+        const uint32_t n_valid = (uint32_t)__syncthreads_count(valid_depth(depth));
+        const uint32_t n_dense =
+            (uint32_t)__syncthreads_count(dense_pixel(depth, vol.div.voxel, cam.fx, fb.n));
+        if (dense_tile(n_valid, n_dense)) {             // uniform over the block
+            // list the tile for update_rows_kernel; if the list is full,
+            // integrate it here after all
+            __shared__ uint32_t s_listed;
+            if (threadIdx.x == 0) {
+                const uint32_t pos = atomicAdd(vol.dense_count, 1u);
+                s_listed = pos < vol.dense_capacity ? 1u : 0u;
+                if (s_listed) vol.dense_list[pos] = (uint32_t)f << 24 | (uint32_t)tile;
+            }
+            __syncthreads();
+            if (s_listed) return;
+        }
+    }
     RayPoint p;
     bool valid = false;
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
-    if (u < fb.width && v < fb.height) {
+    if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
-        valid = back_project(cam, u, v, __ldg(fb.frame[f].depth + pix), p);
+        valid = back_project(cam, u, v, depth, p);
         if (valid) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);
@@ -95,18 +160,377 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// Pre-reduced update.
+// ---------------------------------------------------------------------------
+constexpr int kRowTile = 8;                           // 8 x 8 pixel tiles
+constexpr int kRowPix = kRowTile * kRowTile;          // 64
+constexpr int kRowParts = 3;                          // threads per pixel
+constexpr int kRowThreads = kRowPix * kRowParts;      // 192
+constexpr int kRowBlocksPerSM = 5;
+constexpr int kRows = 224;                            // shared row slots
+constexpr int kCellWords = 4;                         // once-mask (2 words), twice-mask (2)
+constexpr int kRowWords = 8 * kCellWords + 4;         // + 4 words to spread the banks
+constexpr int kRowMaxProbe = 32;
+constexpr uint32_t kNoRow = 0xFFFFFFFFu;
+// Per-pixel fields in shared memory, [field][64].
+enum PixField { kPxValid = 0, kPxD, kPxPx, kPxPy, kPxPz, kPxDx, kPxDy, kPxDz, kPxR, kPxG, kPxB,
+                kPxFields };
+// Shared layout in 32-bit words (offsets keep the 64-bit block keys 8-byte
+// aligned and the sums 16-byte aligned).
+constexpr int kOffKey = 0;                                   // [kRows] row key or kNoRow
+constexpr int kOffList = kOffKey + kRows;                    // [kRows] claimed slots
+constexpr int kOffCount = kOffList + kRows;                  // [8] rows, cells, vote per warp
+constexpr int kOffBlock = kOffCount + 8;                     // [kRows] u64 block key of the row
+constexpr int kOffCells = kOffBlock + 2 * kRows;             // [kRows][kRowWords]
+constexpr int kOffPix = kOffCells + kRows * kRowWords;       // [kPxFields][64]
+constexpr int kOffCellList = kOffPix + kPxFields * kRowPix;  // [8 * kRows] u16 (slot << 3 | lx)
+constexpr int kRowSmemWords = kOffCellList + 8 * kRows / 2;
+constexpr size_t kRowSmemBytes = (size_t)kRowSmemWords * sizeof(uint32_t);
+static_assert(kOffBlock % 2 == 0 && kOffCells % 4 == 0, "shared layout alignment");
+
+// Find or claim the shared slot of each lane's row (row_key = pool index << 6
+// | row), or -1 for lanes that do not want one or find no slot within
+// kRowMaxProbe probes.  The loop runs the same number of times on every lane
+// (it ends when no lane is still probing), so the warp leaves it converged.
+// The lane that claims a slot records the row's block key and lists the slot.
+__device__ __forceinline__ int claim_row(uint32_t* sm, bool want, uint32_t row_key,
+                                         unsigned long long block)
+{
+    uint32_t* s_key = sm + kOffKey;
+    uint32_t slot = __umulhi(row_key * 0x9E3779B1u, (uint32_t)kRows);
+    int found = -1;
+    bool probing = want;
+    for (int n = 0; n < kRowMaxProbe; ++n) {
+        if (!__any_sync(0xFFFFFFFFu, probing)) break;
+        if (probing) {
+            uint32_t k = s_key[slot];
+            if (k == kNoRow) {
+                k = atomicCAS(&s_key[slot], kNoRow, row_key);
+                if (k == kNoRow) {
+                    reinterpret_cast<unsigned long long*>(sm + kOffBlock)[slot] = block;
+                    sm[kOffList + atomicAdd(sm + kOffCount, 1u)] = slot;
+                    k = row_key;
+                }
+            }
+            if (k == row_key) {
+                found = (int)slot;
+                probing = false;
+            } else {
+                slot = slot + 1 == (uint32_t)kRows ? 0u : slot + 1;
+            }
+        }
+    }
+    return found;
+}
+
+template <bool kFast>
+__device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& cam, uint32_t* sm);
+
+// One 8 x 8 pixel tile (origin u0, v0) of frame f, pre-reduced; called by
+// the whole block.  Adds the tile's counts to the caller's.
+template <bool kFast>
+__device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatch& fb, int f,
+                                          int u0, int v0, uint32_t* sm, uint32_t& n_valid,
+                                          uint32_t& updates, uint32_t& missed)
+{
+    uint32_t* s_key = sm + kOffKey;
+    uint32_t* s_cells = sm + kOffCells;
+    uint32_t* s_pix = sm + kOffPix;
+    float* s_pixf = reinterpret_cast<float*>(s_pix);
+    const int t = threadIdx.x;
+    const Camera cam = fb.frame[f].cam;
+
+    if (t < kRowPix) {
+        const int u = u0 + (t & (kRowTile - 1)), v = v0 + t / kRowTile;
+        RayPoint p = {};
+        bool valid = false;
+        float c[3] = {0.0f, 0.0f, 0.0f};
+        if (u < fb.width && v < fb.height) {
+            const size_t pix = (size_t)v * fb.width + u;
+            valid = back_project(cam, u, v, __ldg(fb.frame[f].depth + pix), p);
+            if (valid) {
+                const float* rgb = fb.frame[f].rgb;
+                c[0] = __ldg(rgb + 3 * pix);
+                c[1] = __ldg(rgb + 3 * pix + 1);
+                c[2] = __ldg(rgb + 3 * pix + 2);
+            }
+        }
+        s_pix[kPxValid * kRowPix + t] = valid ? 1u : 0u;
+        s_pixf[kPxD * kRowPix + t] = p.d;
+        s_pixf[kPxPx * kRowPix + t] = p.px;
+        s_pixf[kPxPy * kRowPix + t] = p.py;
+        s_pixf[kPxPz * kRowPix + t] = p.pz;
+        s_pixf[kPxDx * kRowPix + t] = p.dx;
+        s_pixf[kPxDy * kRowPix + t] = p.dy;
+        s_pixf[kPxDz * kRowPix + t] = p.dz;
+        s_pixf[kPxR * kRowPix + t] = c[0];
+        s_pixf[kPxG * kRowPix + t] = c[1];
+        s_pixf[kPxB * kRowPix + t] = c[2];
+    }
+    for (int i = t; i < kRows; i += kRowThreads) s_key[i] = kNoRow;
+    if (t < 2) sm[kOffCount + t] = 0;
+    uint4* cells4 = reinterpret_cast<uint4*>(s_cells);
+    for (int i = t; i < kRows * kRowWords / 4; i += kRowThreads) cells4[i] = make_uint4(0, 0, 0, 0);
+    __syncthreads();
+
+    // walk: thread (pixel q, part) takes band steps [part * per, (part + 1) * per);
+    // a warp holds 32 pixels of one part, so the trip count is warp-uniform
+    const int q = t % kRowPix;
+    const int part = t / kRowPix;
+    const int steps = 2 * vol.band_half + 1;
+    const int per = (steps + kRowParts - 1) / kRowParts;
+    const int i0 = part * per;
+    const int i1 = min(steps, i0 + per);
+    const bool valid = s_pix[kPxValid * kRowPix + q] != 0;
+    RayPoint p;
+    p.d = s_pixf[kPxD * kRowPix + q];
+    p.px = s_pixf[kPxPx * kRowPix + q];
+    p.py = s_pixf[kPxPy * kRowPix + q];
+    p.pz = s_pixf[kPxPz * kRowPix + q];
+    p.dx = s_pixf[kPxDx * kRowPix + q];
+    p.dy = s_pixf[kPxDy * kRowPix + q];
+    p.dz = s_pixf[kPxDz * kRowPix + q];
+    const uint32_t bit = 1u << (q & 31);
+    const int half_word = q >> 5;
+    unsigned long long last = kEmptyKey;
+    uint32_t idx = kIndexFailed;
+    for (int i = i0; i < i1; ++i) {
+        VoxelSample s;      // (invalid pixels walk a zero ray: finite values, never used)
+        const int status = band_sample<kFast>(cam, vol.div, p, i - vol.band_half, s);
+        const bool pass = valid && status == kSamplePass;
+        const unsigned long long key = pass ? block_key(s.ix, s.iy, s.iz) : kEmptyKey;
+        if (pass && key != last) {
+            idx = lookup(vol.table, vol.table_mask, key);
+            last = key;
+        }
+        const bool add = pass && idx < vol.pool_capacity;   // else absent, FAILED or unpublished
+        missed += (pass && !add) ? 1u : 0u;
+        updates += add ? 1u : 0u;
+        const uint32_t row = (uint32_t)((s.iy & 7) | ((s.iz & 7) << 3));
+        const int lx = s.ix & 7;
+        const int slot = claim_row(sm, add, (idx << 6) | row, key);
+        bool direct = add && slot < 0;
+        if (slot >= 0) {
+            uint32_t* cell = s_cells + slot * kRowWords + lx * kCellWords;
+            const uint32_t once = atomicOr(cell + half_word, bit);
+            if (once & bit) {
+                // a ray puts at most two samples in a voxel (samples are one
+                // voxel edge apart, a voxel is sqrt(3) edges across); a third
+                // would still be added, directly
+                const uint32_t twice = atomicOr(cell + 2 + half_word, bit);
+                direct = (twice & bit) != 0;
+            }
+        }
+        if (direct) {
+            const size_t e = (size_t)idx * kBlockVoxels + row * 8 + lx;
+            red_add(vol.tsdf + e, s.tsdf);
+            red_add(vol.weight + e, 1.0f);
+            red_add(vol.red + e, s_pixf[kPxR * kRowPix + q]);
+            red_add(vol.green + e, s_pixf[kPxG * kRowPix + q]);
+            red_add(vol.blue + e, s_pixf[kPxB * kRowPix + q]);
+        }
+    }
+    flush_rows<kFast>(vol, cam, sm);
+    n_valid += (valid && part == 0) ? 1u : 0u;
+}
+
+// kAlways: block b pre-reduces 8 x 8 tile b / n of frame b % n.  Otherwise
+// the blocks are persistent and take the dense 16 x 16 tiles that
+// update_kernel listed, each as four 8 x 8 tiles.
+template <bool kFast, bool kAlways>
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) update_rows_kernel(
+    VolumeView vol, const __grid_constant__ FrameBatch fb)
+{
+    extern __shared__ __align__(16) uint32_t sm[];
+    const int t = threadIdx.x;
+    uint32_t n_valid = 0, updates = 0, missed = 0;
+    if (kAlways) {
+        const int f = blockIdx.x % fb.n;
+        const int tile = blockIdx.x / fb.n;
+        const int tiles_x = (fb.width + kRowTile - 1) / kRowTile;
+        rows_tile<kFast>(vol, fb, f, (tile % tiles_x) * kRowTile, (tile / tiles_x) * kRowTile, sm,
+                         n_valid, updates, missed);
+    } else {
+        const uint32_t n_items = 4u * min(*vol.dense_count, vol.dense_capacity);
+        const int tiles16_x = (fb.width + 15) / 16;
+        uint32_t* s_item = sm + kOffCount + 2;
+        for (;;) {
+            if (t == 0) *s_item = atomicAdd(vol.dense_next, 1u);
+            __syncthreads();
+            const uint32_t j = *s_item;
+            __syncthreads();                // all have read the item before it is replaced
+            if (j >= n_items) break;        // uniform over the block
+            const uint32_t entry = vol.dense_list[j >> 2];
+            const int f = (int)(entry >> 24);
+            const int tile16 = (int)(entry & 0xFFFFFFu);
+            const int u0 = (tile16 % tiles16_x) * 16 + (int)(j & 1u) * kRowTile;
+            const int v0 = (tile16 / tiles16_x) * 16 + (int)((j >> 1) & 1u) * kRowTile;
+            if (u0 < fb.width && v0 < fb.height)
+                rows_tile<kFast>(vol, fb, f, u0, v0, sm, n_valid, updates, missed);
+        }
+        // the last block to finish leaves the list empty for the next launch
+        // (stream order makes the reset visible to it)
+        if (t == 0 && atomicAdd(vol.dense_done, 1u) == gridDim.x - 1) {
+            *vol.dense_count = 0;
+            *vol.dense_next = 0;
+            *vol.dense_done = 0;
+        }
+    }
+    const unsigned lane = lane_id();
+    const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, n_valid);
+    const uint32_t w_updates = __reduce_add_sync(0xFFFFFFFFu, updates);
+    const uint32_t w_missed = __reduce_add_sync(0xFFFFFFFFu, missed);
+    if (lane == 0) {
+        const int stripe = blockIdx.x % kCounterStripes;
+        if (w_valid) atomicAdd(&vol.counters->valid_points[stripe], (unsigned long long)w_valid);
+        if (w_updates)
+            atomicAdd(&vol.counters->voxel_updates[stripe], (unsigned long long)w_updates);
+        if (w_missed) atomicAdd(&vol.counters->missed[stripe], (unsigned long long)w_missed);
+    }
+}
+
+// The pre-reducing tile's second half (called by the whole block): list the
+// non-empty voxels of the claimed rows, then flush them.
+template <bool kFast>
+__device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& cam, uint32_t* sm)
+{
+    __syncthreads();
+    const uint32_t* s_key = sm + kOffKey;
+    const uint32_t* s_cells = sm + kOffCells;
+    const float* s_pixf = reinterpret_cast<const float*>(sm + kOffPix);
+    uint16_t* s_cell_list = reinterpret_cast<uint16_t*>(sm + kOffCellList);
+    const int t = threadIdx.x;
+    const unsigned lane = lane_id();
+
+    // list the non-empty cells of the claimed rows, row by row, lx ascending
+    const int n_rows = (int)sm[kOffCount];
+    for (int base = t & ~31; base < 8 * n_rows; base += kRowThreads) {   // warp-uniform
+        const int j = base + (int)lane;
+        bool used = false;
+        uint32_t code = 0;
+        if (j < 8 * n_rows) {
+            const uint32_t slot = sm[kOffList + (j >> 3)];
+            const uint32_t* cell = s_cells + slot * kRowWords + (j & 7) * kCellWords;
+            used = (cell[0] | cell[1]) != 0;
+            code = slot << 3 | (uint32_t)(j & 7);
+        }
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, used);
+        uint32_t pos = 0;
+        if (lane == 0 && m) pos = atomicAdd(sm + kOffCount + 1, (uint32_t)__popc(m));
+        pos = __shfl_sync(0xFFFFFFFFu, pos, 0);
+        if (used) s_cell_list[pos + __popc(m & ((1u << lane) - 1u))] = (uint16_t)code;
+    }
+    __syncthreads();
+
+    // flush: each listed cell recomputes its samples' tsdf from the pixel
+    // depths and its voxel centre (the walk's own arithmetic), sums them with
+    // the colours in pixel order, and adds the five sums to the pool; cells of
+    // one row sit next to each other, so a row reaches L2 as one sector per array
+    const int n_cells = (int)sm[kOffCount + 1];
+    float* arrays[5] = {vol.tsdf, vol.weight, vol.red, vol.green, vol.blue};
+    for (int k = t; k < n_cells; k += kRowThreads) {
+        const uint32_t code = s_cell_list[k];
+        const uint32_t slot = code >> 3;
+        const int lx = (int)(code & 7u);
+        const uint32_t row_key = s_key[slot];
+        const unsigned long long block = reinterpret_cast<const unsigned long long*>(sm + kOffBlock)[slot];
+        const uint4 cw = *reinterpret_cast<const uint4*>(s_cells + slot * kRowWords + lx * kCellWords);
+        const int row = (int)(row_key & 63u);
+        int bc[3];
+        unpack_block(block, bc);
+        const float zc = centre_depth(cam, vol.div.voxel, bc[0] * kBlockEdge + lx,
+                                      bc[1] * kBlockEdge + (row & 7), bc[2] * kBlockEdge + (row >> 3));
+        float sum[5] = {0.0f, 0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t once = h == 0 ? cw.x : cw.y;
+            const uint32_t twice = h == 0 ? cw.z : cw.w;
+            while (once) {
+                const int b = __ffs(once) - 1;
+                once &= once - 1;
+                const int px = h * 32 + b;
+                const float tv = truncated_sdf<kFast>(vol.div, s_pixf[kPxD * kRowPix + px], zc);
+                const int reps = (twice >> b & 1u) ? 2 : 1;
+                for (int r = 0; r < reps; ++r) {
+                    sum[0] = __fadd_rn(sum[0], tv);
+                    sum[1] = __fadd_rn(sum[1], 1.0f);
+                    sum[2] = __fadd_rn(sum[2], s_pixf[kPxR * kRowPix + px]);
+                    sum[3] = __fadd_rn(sum[3], s_pixf[kPxG * kRowPix + px]);
+                    sum[4] = __fadd_rn(sum[4], s_pixf[kPxB * kRowPix + px]);
+                }
+            }
+        }
+        const size_t e = (size_t)(row_key >> 6) * kBlockVoxels + (size_t)row * 8 + lx;
+#pragma unroll
+        for (int a = 0; a < 5; ++a) red_add(arrays[a] + e, sum[a]);
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, cudaStream_t stream)
+// Opt in to the pre-reducing kernel's shared memory, once per device and
+// instance.
+template <bool kFast, bool kAlways>
+cudaError_t launch_rows(const VolumeView& vol, const FrameBatch& fb, unsigned grid,
+                        cudaStream_t stream)
 {
-    const unsigned tiles = (unsigned)(((fb.width + kTileW - 1) / kTileW) *
-                                      ((fb.height + kTileH - 1) / kTileH));
-    const unsigned grid = tiles * (unsigned)fb.n;
-    if (vol.fast_div)
-        update_kernel<true><<<grid, kThreads, 0, stream>>>(vol, fb);
-    else
-        update_kernel<false><<<grid, kThreads, 0, stream>>>(vol, fb);
+    static std::atomic<unsigned long long> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        e = cudaFuncSetAttribute(update_rows_kernel<kFast, kAlways>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRowSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    update_rows_kernel<kFast, kAlways><<<grid, kRowThreads, kRowSmemBytes, stream>>>(vol, fb);
     return cudaGetLastError();
+}
+
+cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
+                          cudaStream_t stream)
+{
+    // adaptive: the per-sample kernel takes the sparse 16 x 16 tiles and
+    // lists the dense ones, which the persistent pre-reducing kernel takes
+    if (kind == TSDF_UPDATE_ADAPTIVE &&
+        (uint64_t)fb.width * (uint64_t)fb.height * (uint64_t)fb.n < kAdaptiveMinPixels)
+        kind = TSDF_UPDATE_PER_SAMPLE;
+    if (kind != TSDF_UPDATE_PRE_REDUCED) {
+        const unsigned tiles = (unsigned)(((fb.width + kTileW - 1) / kTileW) *
+                                          ((fb.height + kTileH - 1) / kTileH));
+        const unsigned grid = tiles * (unsigned)fb.n;
+        const bool sparse_only = kind == TSDF_UPDATE_ADAPTIVE;
+        if (vol.fast_div) {
+            if (sparse_only) update_kernel<true, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+            else update_kernel<true, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+        } else {
+            if (sparse_only) update_kernel<false, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+            else update_kernel<false, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+        }
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || kind == TSDF_UPDATE_PER_SAMPLE) return e;
+    }
+    const bool always = kind == TSDF_UPDATE_PRE_REDUCED;
+    unsigned grid;
+    if (always) {
+        grid = (unsigned)(((fb.width + kRowTile - 1) / kRowTile) *
+                          ((fb.height + kRowTile - 1) / kRowTile)) * (unsigned)fb.n;
+    } else {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        grid = (unsigned)(sms > 0 ? sms : 1) * kRowBlocksPerSM;
+    }
+    if (vol.fast_div)
+        return always ? launch_rows<true, true>(vol, fb, grid, stream)
+                      : launch_rows<true, false>(vol, fb, grid, stream);
+    return always ? launch_rows<false, true>(vol, fb, grid, stream)
+                  : launch_rows<false, false>(vol, fb, grid, stream);
 }
 
 }  // namespace tsdf

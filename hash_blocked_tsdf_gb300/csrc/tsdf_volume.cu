@@ -17,7 +17,10 @@ namespace {
 // Device-resident mutable state: the pool's bump counter and the counters.
 struct DeviceState {
     uint32_t pool_counter;
-    uint32_t pad[7];
+    uint32_t dense_count;       // adaptive update: dense tiles listed in this launch,
+    uint32_t dense_next;        // ... taken by the pre-reducing kernel,
+    uint32_t dense_done;        // ... whose blocks count out here (all three are zero
+    uint32_t pad[4];            //     between launches)
     DeviceCounters counters;
 };
 
@@ -31,10 +34,12 @@ struct tsdf_volume {
     float trunc = 0.0f;
     int band_half = 0;
     bool instrument = false;
+    int update_kind = TSDF_UPDATE_ADAPTIVE;
     DivisorPair div = {};
     bool fast_div = false;          // the fixed-divisor division was verified for both divisors
 
     Entry* table = nullptr;
+    uint32_t* dense_list = nullptr;  // [kDenseListCapacity] adaptive update's dense tiles
     float* pool = nullptr;          // five arrays of pool_capacity * 512 floats, back to back
     DeviceState* state = nullptr;
     int32_t* coords = nullptr;      // [pool_capacity][3], allocated on first export
@@ -90,6 +95,11 @@ VolumeView view_of(const tsdf_volume* v)
     w.div = v->div;
     w.fast_div = v->fast_div;
     w.band_half = v->band_half;
+    w.dense_list = v->dense_list;
+    w.dense_capacity = kDenseListCapacity;
+    w.dense_count = &v->state->dense_count;
+    w.dense_next = &v->state->dense_next;
+    w.dense_done = &v->state->dense_done;
     return w;
 }
 
@@ -157,6 +167,7 @@ int ensure_staging(tsdf_volume* v, size_t pixels)
 void release(tsdf_volume* v)
 {
     if (v->table) cudaFree(v->table);
+    if (v->dense_list) cudaFree(v->dense_list);
     if (v->pool) cudaFree(v->pool);
     if (v->state) cudaFree(v->state);
     if (v->coords) cudaFree(v->coords);
@@ -191,7 +202,7 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
         }
         if (do_allocate)
             TSDF_CUDA(launch_allocate(vol, fb, v->instrument, stream), "allocate kernel");
-        if (do_update) TSDF_CUDA(launch_update(vol, fb, stream), "update kernel");
+        if (do_update) TSDF_CUDA(launch_update(vol, fb, v->update_kind, stream), "update kernel");
     }
     return TSDF_OK;
 }
@@ -289,6 +300,7 @@ int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_
     cudaError_t e = cudaGetDevice(&v->device);
     const size_t pool_bytes = 5 * array_floats(v) * sizeof(float);
     if (e == cudaSuccess) e = cudaMalloc(&v->table, T * sizeof(Entry));
+    if (e == cudaSuccess) e = cudaMalloc(&v->dense_list, kDenseListCapacity * sizeof(uint32_t));
     if (e == cudaSuccess) e = cudaMalloc(&v->pool, pool_bytes);
     if (e == cudaSuccess) e = cudaMalloc(&v->state, sizeof(DeviceState));
     if (e == cudaSuccess) e = cudaMemsetAsync(v->pool, 0, pool_bytes, 0);
@@ -565,6 +577,18 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on)
     int rc = check_volume(vol);
     if (rc) return rc;
     vol->instrument = on != 0;
+    return TSDF_OK;
+}
+
+int tsdf_set_update_kernel(tsdf_volume* vol, int kind)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (kind != TSDF_UPDATE_ADAPTIVE && kind != TSDF_UPDATE_PER_SAMPLE &&
+        kind != TSDF_UPDATE_PRE_REDUCED)
+        return fail(TSDF_ERR_ARG, "update mode must be TSDF_UPDATE_ADAPTIVE, "
+                                  "TSDF_UPDATE_PER_SAMPLE or TSDF_UPDATE_PRE_REDUCED");
+    vol->update_kind = kind;
     return TSDF_OK;
 }
 

@@ -52,6 +52,9 @@
  *     that enqueue work return without synchronising, except the read-out
  *     calls (block_count, export_*, get_stats), which synchronise `stream`.
  *   - A volume is not thread-safe; concurrent calls on one volume race.
+ *     Work enqueued on one volume must also run in order on the device: use
+ *     one stream per volume, or order different streams with events (the
+ *     update keeps a per-launch work list in the volume's device state).
  *
  * Errors: every call returns TSDF_OK or a negative code.  On TSDF_ERR_ARG
  * nothing was enqueued.  tsdf_last_error() returns a message describing the
@@ -264,6 +267,30 @@ int tsdf_clear_stats(tsdf_volume* vol, void* stream);
  * launches.  It costs a shared-memory histogram per block of threads; keep it
  * off when timing. */
 int tsdf_set_instrumentation(tsdf_volume* vol, int on);
+
+/* How later update launches (integrate, update and their batch forms) add
+ * the samples to the pool.  Every mode computes the same sums ("What
+ * Irregularity Costs", design section, integration: the update adds tsdf, 1
+ * and the pixel colour into the five arrays for every passing sample); they
+ * differ in how the additions reach memory:
+ *   TSDF_UPDATE_ADAPTIVE (the default): each 16 x 16 pixel tile of a frame
+ *     chooses for itself.  Where at least half of its valid pixels see a voxel
+ *     edge w or more pixels wide (voxel_size * fx >= w * depth; w = 5 when a
+ *     launch holds 4 or more frames, else 10), many samples share a voxel
+ *     and the tile pre-reduces (below); elsewhere its samples are added one by
+ *     one, as with TSDF_UPDATE_PER_SAMPLE.  Launches of fewer than 2^18
+ *     pixels in all are always added one by one.
+ *   TSDF_UPDATE_PER_SAMPLE: every passing sample is added to the pool with
+ *     five float reductions of its own (16 x 16 pixel tiles).
+ *   TSDF_UPDATE_PRE_REDUCED: every tile pre-reduces: it records in shared
+ *     memory which of its pixels reached each voxel (once or twice), then sums
+ *     every touched voxel's contributions in pixel order and adds the five
+ *     sums to the pool once, a row of 8 voxels at a time.
+ * Returns TSDF_ERR_ARG for any other value. */
+#define TSDF_UPDATE_ADAPTIVE 0
+#define TSDF_UPDATE_PER_SAMPLE 1
+#define TSDF_UPDATE_PRE_REDUCED 2
+int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 
 /* Message of the last failure on the calling thread ("" if none). */
 const char* tsdf_last_error(void);

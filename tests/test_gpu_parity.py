@@ -47,8 +47,10 @@ def _oracle(oracle_mod, frames, block_limit=-1):
     return o
 
 
-def _full_parity(torch, oracle_mod, frames, strict, batch=True):
+def _full_parity(torch, oracle_mod, frames, strict, batch=True, kernel=None):
     vol = _gpu_volume(torch, frames)
+    if kernel is not None:
+        vol.set_update_kernel(kernel)
     _integrate_gpu(torch, frames, vol, batch)
     g = vol.export_blocks()
     st = vol.stats()
@@ -68,28 +70,111 @@ def test_smoke_entry(torch_cuda):
     __graft_entry__.smoke()
 
 
-def test_parity_tiny_sphere_plane(torch_cuda, oracle_mod):
-    rep = _full_parity(torch_cuda, oracle_mod, scenes.tiny_sphere_plane(), strict=True)
+KERNELS = ["adaptive", "pre_reduced", "per_sample"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_parity_tiny_sphere_plane(torch_cuda, oracle_mod, kernel):
+    rep = _full_parity(torch_cuda, oracle_mod, scenes.tiny_sphere_plane(), strict=True,
+                       kernel=kernel)
     assert rep["blocks"] > 500
 
 
-def test_parity_vga_sphere_plane(torch_cuda, oracle_mod):
-    _full_parity(torch_cuda, oracle_mod, scenes.vga_sphere_plane(), strict=True)
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_parity_vga_sphere_plane(torch_cuda, oracle_mod, kernel):
+    _full_parity(torch_cuda, oracle_mod, scenes.vga_sphere_plane(), strict=True, kernel=kernel)
 
 
-def test_parity_oblique_pose(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_parity_oblique_pose(torch_cuda, oracle_mod, kernel):
     from test_oracle_pins import oblique_sphere_frames
-    _full_parity(torch_cuda, oracle_mod, oblique_sphere_frames(), strict=True)
+    _full_parity(torch_cuda, oracle_mod, oblique_sphere_frames(), strict=True, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("wh", [(1, 1), (7, 3), (33, 17), (161, 121), (257, 1), (1, 300)])
-def test_parity_ragged_sizes(torch_cuda, oracle_mod, wh):
+def test_parity_ragged_sizes(torch_cuda, oracle_mod, wh, kernel):
     W, H = wh
     depth, rgb, pose, K = scenes.sphere_plane(W, H, fx=0.8 * max(W, H), fy=0.8 * max(W, H),
                                               noise_sigma=0.002, invalid_frac=0.1, seed=W * H)
     frames = scenes.Frames(f"ragged_{W}x{H}", depth[None], rgb[None], pose[None], K,
                            0.01, 0.04, 4096, 0, 0)
-    _full_parity(torch_cuda, oracle_mod, frames, strict=True)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
+
+
+def _flat_frame(name, W, H, f, depth_m, pose, voxel, trunc, pool, rgb_scale=1.0, rgb_shift=0.0,
+                seed=0):
+    """One frame of a surface at constant camera depth, colours uniform."""
+    rng = np.random.default_rng(seed)
+    depth = np.full((1, H, W), depth_m, np.float32)
+    rgb = (rng.random((1, H, W, 3)) * rgb_scale + rgb_shift).astype(np.float32)
+    K = np.array([f, f, (W - 1) / 2, (H - 1) / 2], np.float32)
+    return scenes.Frames(name, depth, rgb, pose[None].astype(np.float32), K, voxel, trunc, pool,
+                         0, seed)
+
+
+def test_pre_reduced_colours_outside_unit_range(torch_cuda, oracle_mod):
+    # colours in [-50, 205): those pixels take the per-sample path; the sums
+    # must still match the oracle exactly as before
+    frames = _flat_frame("colours_wide", 96, 64, 80.0, 1.2031, np.eye(4), 0.01, 0.04, 4096,
+                         rgb_scale=255.0, rgb_shift=-50.0, seed=3)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="pre_reduced")
+
+
+def test_pre_reduced_dense_close_range(torch_cuda, oracle_mod):
+    # 0.25 mm pixels against 1 cm voxels, seen at 40 degrees: every 8 x 8 tile
+    # sends all 64 rays through the same few voxels, up to two samples per ray
+    # and voxel, the most a cell can receive from one tile
+    pose = np.eye(4)
+    pose[:3, :3] = scenes.axis_angle([0.0, 1.0, 0.0], np.deg2rad(40.0))
+    frames = _flat_frame("dense_close", 64, 64, 2000.0, 0.5037, pose, 0.01, 0.04, 4096, seed=4)
+    rep = _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="pre_reduced")
+    o = _oracle(oracle_mod, frames)
+    assert o.export()["weight"].max() >= 64, "the case must put many samples in one voxel"
+    print("dense close range:", rep)
+
+
+def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod):
+    # one 640 x 480 frame, 3 cm voxels at fx = 525: the sphere's front
+    # (depth < 1.575 m) sees a voxel edge 10+ pixels wide (the one-frame
+    # rule) and is pre-reduced, the plane at 2.5 m is not; each tile is
+    # integrated exactly once
+    f = scenes.vga_sphere_plane()
+    frames = scenes.Frames("vga_mixed", f.depth, f.rgb, f.poses, f.K, 0.03, 0.12, 8192, 0, 0)
+    d = frames.depth[0]
+    near = (d > 0) & (0.03 * frames.K[0] >= 10 * d)
+    assert 0.05 < near.mean() < 0.6, "the frame must hold both kinds of pixel"
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="adaptive")
+
+
+def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod):
+    # eight orbit frames in one launch with 2 cm voxels: objects nearer than
+    # 2.1 m see a voxel edge 5+ pixels wide (the several-frame rule)
+    f = scenes.orbit_trajectory(n_frames=100, frames=(0, 8))
+    frames = scenes.Frames("orbit_mixed", f.depth, f.rgb, f.poses, f.K, 0.02, 0.08, 1 << 16, 0, 0)
+    d = frames.depth
+    near = (d > 0) & (0.02 * frames.K[0] >= 5 * d)
+    assert 0.02 < near.sum() / (d > 0).sum() < 0.9, "the batch must hold both kinds of pixel"
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel="adaptive")
+
+
+def test_adaptive_dense_frame(torch_cuda, oracle_mod):
+    # 512 x 512 pixels of 1.5 mm against 2 cm voxels: every tile is dense and
+    # hundreds of samples reach each voxel (summation tolerance)
+    pose = np.eye(4)
+    pose[:3, :3] = scenes.axis_angle([0.0, 1.0, 0.0], np.deg2rad(35.0))
+    frames = _flat_frame("dense_frame", 512, 512, 600.0, 0.9037, pose, 0.02, 0.08, 4096, seed=6)
+    rep = _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel="adaptive")
+    print("dense frame:", rep)
+
+
+def test_pre_reduced_row_table_overflow(torch_cuda, oracle_mod):
+    # 15 cm pixels against 5 mm voxels: each ray's 9 samples lie in 9 different
+    # voxel rows, so an 8 x 8 tile touches ~576 rows, more than the shared
+    # table holds; the rows that find no slot go straight to the pool
+    frames = _flat_frame("wide_rows", 32, 32, 20.0, 3.0011, np.eye(4), 0.005, 0.02, 8192,
+                         seed=5)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="pre_reduced")
 
 
 def test_parity_orbit_prefix_per_frame_vs_batch(torch_cuda, oracle_mod):
