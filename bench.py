@@ -44,6 +44,10 @@ WORKLOADS = {
     "orbit": ("orbit_trajectory", {"n_frames": 100}),
     "vga": ("vga_sphere_plane", {}),
     "tiny": ("tiny_sphere_plane", {}),
+    # the orbit seen through 4 cm voxels: nearly every pixel sees a voxel edge
+    # 5+ pixels wide, the regime the adaptive update pre-reduces
+    "orbit_coarse": ("orbit_trajectory", {"n_frames": 100, "voxel_size": 0.04, "trunc": 0.16,
+                                          "pool_capacity": 1 << 16}),
 }
 
 
@@ -60,18 +64,26 @@ def parse_args():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pool", type=int, default=0,
+                    help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced"],
                     default="adaptive", help="how the library's update reaches the pool")
     return ap.parse_args()
 
 
-def make_frames(workload: str, n_frames: int):
+def make_frames(workload: str, n_frames: int, pool: int = 0):
+    import dataclasses
     from hash_blocked_tsdf_gb300 import scenes
     fn, kw = WORKLOADS[workload]
     kw = dict(kw)
     if n_frames and "n_frames" in kw:
         kw["n_frames"] = n_frames
-    return getattr(scenes, fn)(**kw)
+    frames = getattr(scenes, fn)(**kw)
+    if "voxel_size" in kw:
+        frames = dataclasses.replace(frames, name=f"{frames.name}_voxel{round(kw['voxel_size'] * 1000)}mm")
+    if pool:
+        frames = dataclasses.replace(frames, pool_capacity=pool)
+    return frames
 
 
 def workload_config(frames, args) -> dict:
@@ -228,7 +240,7 @@ def run_reference(args):
     rank, local, world = dist_setup()
     if rank != 0:
         return
-    frames = make_frames(args.workload, args.frames)
+    frames = make_frames(args.workload, args.frames, args.pool)
     per_step = max(1, min(frames.n_frames, 2))
     import oracle
     oracle.build()
@@ -289,7 +301,7 @@ def run_ours(args):
         __graft_entry__.build()
     from hash_blocked_tsdf_gb300 import TsdfVolume, binding
 
-    frames = make_frames(args.workload, args.frames)
+    frames = make_frames(args.workload, args.frames, args.pool)
     n = frames.n_frames
     stream = torch.cuda.current_stream()
     d_dev = torch.from_numpy(frames.depth).cuda()
@@ -385,13 +397,15 @@ def run_ours(args):
     u_frames = distinct["frame_by_frame"]
     bytes_per_launch = (16.0 * points_per_step + 40.0 * u_frames) / ng
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
-    upd_kernel = ("update_kernel" if args.update_kernel == "per_sample"
-                  else "update_rows_kernel")
-    prof_upd = _profile_record(f"{upd_kernel}_room_walk_1280x720.md",
+    # the kernels the update stage launches in the selected mode
+    upd_kernel = {"per_sample": "update_kernel", "pre_reduced": "update_rows_kernel",
+                  "adaptive": "update_kernel+update_rows_kernel"}[args.update_kernel]
+    prof_upd = _profile_record(f"update_{args.update_kernel}_room_walk_1280x720.md",
                                ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md",
                                  ["tsdf_alloc.cu", "tsdf_device.cuh", "tsdf_internal.h"])
-    same_shape = frames.width == 1280 and frames.height == 720 and group == 8
+    same_shape = (args.workload == "room_walk" and frames.width == 1280 and frames.height == 720
+                  and group == 8)
     roofline = {
         "bound": "hbm", "kernel": upd_kernel, "achieved": achieved, "peak": hbm_peak,
         "unit": "GB/s", "frac": achieved / hbm_peak,

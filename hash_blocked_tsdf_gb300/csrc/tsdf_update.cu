@@ -353,7 +353,9 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) update_rows_kern
         rows_tile<kFast>(vol, fb, f, (tile % tiles_x) * kRowTile, (tile / tiles_x) * kRowTile, sm,
                          n_valid, updates, missed);
     } else {
-        const uint32_t n_items = 4u * min(*vol.dense_count, vol.dense_capacity);
+        const uint32_t n_listed = *vol.dense_count;
+        if (n_listed == 0) return;          // nothing listed: nothing taken, nothing to reset
+        const uint32_t n_items = 4u * min(n_listed, vol.dense_capacity);
         const int tiles16_x = (fb.width + 15) / 16;
         uint32_t* s_item = sm + kOffCount + 2;
         for (;;) {
