@@ -118,7 +118,8 @@ def _l2_note(frames) -> str:
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "temperature.gpu")
 
     def __init__(self, device_index: int):
         self.device_index = device_index
@@ -145,7 +146,7 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
+        sm, smax, temp, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [p.strip() for p in line.split(",")]
@@ -156,13 +157,21 @@ class ClockSampler:
                 smax.append(float(parts[2]))
             except ValueError:
                 continue
+            try:
+                temp.append(float(parts[9]))
+            except (ValueError, IndexError):
+                pass
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)),
+               "reasons": sorted(reasons), "samples": len(sm)}
+        if temp:
+            out["temp_c_median"] = float(np.median(temp))
+            out["temp_c_max"] = float(max(temp))
+        return out
 
 
 # ----------------------------------------------------------------------------
@@ -233,7 +242,80 @@ def oracle_sample(frames, seconds_target: float):
     dt = time.perf_counter() - t0
     c = o.counters()
     return (c["valid_points"] / dt, c["passing_samples"] / dt,
-            f"first {n} of {frames.n_frames} frames of {frames.name} ({dt:.1f} s, 1 thread)")
+            f"first {n} of {frames.n_frames} frames of {frames.name} ({dt:.1f} s, 1 thread)",
+            o, n)
+
+
+def parity_gate(torch, vol, frames, d_dev, c_dev, n, ovol) -> dict:
+    """The same first `n` frames the oracle integrated for the CPU baseline,
+    integrated again on the GPU (fresh volume, the bench's own batching), and
+    compared: exact block set, weights and counters; sums within
+    max(1e-5 |x|, 1e-6) plus the float32 summation bound gamma(w - 1) sum |t|."""
+    vol.reset()
+    vol.integrate_batch(d_dev[:n], c_dev[:n], frames.K, frames.poses[:n])
+    torch.cuda.synchronize()
+    st = vol.stats()
+    g = vol.export_blocks()
+    o = ovol.export()
+    oc = ovol.counters()
+    out = {"frames": n, "blocks": int(len(o["coords"]))}
+    order = np.lexsort((g["coords"][:, 2], g["coords"][:, 1], g["coords"][:, 0]))
+    out["block_set_equal"] = bool(g["coords"].shape == o["coords"].shape and
+                                  np.array_equal(g["coords"][order], o["coords"]))
+    out["weights_equal"] = bool(out["block_set_equal"] and
+                                np.array_equal(g["weight"][order], o["weight"]))
+    out["counters_equal"] = bool(st["valid_points"] == oc["valid_points"] and
+                                 st["voxel_updates"] == oc["accumulated"] and
+                                 st["missed_contributions"] == oc["missed_contributions"])
+    worst = float("inf")
+    if out["weights_equal"]:
+        u = 2.0 ** -24
+        m = np.maximum(o["weight"] - 1.0, 0.0)
+        gamma = m * u / (1.0 - m * u)
+        worst = 0.0
+        for k, absum in (("tsdf", o["tsdf_abs"]), ("r", None), ("g", None), ("b", None)):
+            x = o[k]
+            bound = np.maximum(1e-5 * np.abs(x), 1e-6) + gamma * (np.abs(x) if absum is None
+                                                                 else absum)
+            worst = max(worst, float(np.max(np.abs(g[k][order] - x) / bound)))
+    out["sums_worst_error_over_bound"] = worst
+    out["pass"] = bool(out["weights_equal"] and out["counters_equal"] and worst <= 1.0)
+    return out
+
+
+def _percentiles(xs) -> dict:
+    a = np.asarray(xs, dtype=np.float64)
+    return {"p50": float(np.percentile(a, 50)), "p95": float(np.percentile(a, 95)),
+            "p99": float(np.percentile(a, 99)), "n": int(a.size)}
+
+
+def _update_kernels(args, frames, n_frames: int) -> int:
+    """Kernels one update launch runs: the adaptive mode runs the per-sample
+    and the pre-reducing kernel when the launch holds 2^18 pixels or more."""
+    if args.update_kernel == "adaptive" and frames.width * frames.height * n_frames >= 1 << 18:
+        return 2
+    return 1
+
+
+def other_processes_mib(device_index: int):
+    """Device memory held by other processes, from nvidia-smi (None if it
+    cannot tell)."""
+    try:
+        out = subprocess.run(["nvidia-smi", f"--id={device_index}",
+                              "--query-compute-apps=pid,used_memory",
+                              "--format=csv,noheader,nounits"],
+                             capture_output=True, text=True, timeout=20).stdout
+    except (OSError, subprocess.TimeoutExpired):
+        return None
+    total = 0
+    for line in out.splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) == 2 and parts[0].isdigit() and int(parts[0]) != os.getpid():
+            try:
+                total += int(parts[1])
+            except ValueError:
+                pass
+    return total
 
 
 def run_reference(args):
@@ -356,6 +438,7 @@ def run_ours(args):
 
     # timed region
     ng = len(groups)
+    other_mib = other_processes_mib(torch.cuda.current_device())
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     barrier(world)
@@ -373,12 +456,14 @@ def run_ours(args):
     barrier(world)
     clk = clocks.stop()
     elapsed_ms = t_start.elapsed_time(t_end)
-    stage_alloc = 0.0
-    stage_update = 0.0
+    launch_alloc, launch_update, step_ms = [], [], []
     for evk in per_step_events:
         for g in range(ng):
-            stage_alloc += evk[2 * g].elapsed_time(evk[2 * g + 1])
-            stage_update += evk[2 * g + 1].elapsed_time(evk[2 * g + 2])
+            launch_alloc.append(evk[2 * g].elapsed_time(evk[2 * g + 1]))
+            launch_update.append(evk[2 * g + 1].elapsed_time(evk[2 * g + 2]))
+        step_ms.append(evk[0].elapsed_time(evk[2 * ng]))
+    stage_alloc = float(sum(launch_alloc))
+    stage_update = float(sum(launch_update))
     max_ms = max_over_ranks(elapsed_ms, world)
     total_points = sum_over_ranks(points_per_step * args.steps, world)
     value = total_points / (max_ms / 1000.0)
@@ -388,7 +473,7 @@ def run_ours(args):
     # update kernel must read 16 B per valid point and read-modify-write the
     # five 4-byte sums of every distinct voxel the frame touches (40 B), and
     # issue 5 float additions per such voxel; a launch covers `group` frames.
-    red_peaks = measure_red_peaks(torch)
+    red_peaks, cas_peaks = measure_red_peaks(torch)
     red_peak = max(v["adds_per_s"] for v in red_peaks["hbm_4GB"].values())
     hbm_peak, peak_kind = _peaks()
     n_update_launches = ng * args.steps
@@ -450,6 +535,19 @@ def run_ours(args):
                       "warp_instructions_per_launch": ipl,
                       "peak_source": f"{sms} SMs x 4 issue slots x sampled {sm_mhz:.0f} MHz",
                       "traffic": prof_alloc.get("traffic_bytes_per_launch")}
+    # its memory terms, for the record (far from binding): HBM bytes it must
+    # read (4 B of depth per pixel of the launch) and the L2 atomic sectors
+    # ncu counted (compare-and-swaps and pool-counter adds) against the
+    # measured compare-and-swap rate
+    px_launch = frames.width * frames.height * group
+    alloc_mem = {"hbm_bytes_per_launch_alg": 4.0 * px_launch,
+                 "frac_hbm": 4.0 * px_launch / (alloc_ms_avg / 1000.0) / 1e9 / hbm_peak,
+                 "cas_peak_ops_per_s": cas_peaks["hbm_4GB"]["ops_per_s"],
+                 "cas_peak_ops_per_s_l2": cas_peaks["l2_32MB"]["ops_per_s"]}
+    if same_shape and prof_alloc.get("l2_atomic_sectors_per_launch"):
+        at = prof_alloc["l2_atomic_sectors_per_launch"]
+        alloc_mem["l2_atomic_sectors_per_launch"] = at
+        alloc_mem["frac_l2_atomics"] = at / (alloc_ms_avg / 1000.0) / cas_peaks["l2_32MB"]["ops_per_s"]
 
     result = {
         "metric": METRIC, "value": value, "unit": "points/s", "n_gpus": world,
@@ -461,6 +559,14 @@ def run_ours(args):
         "frames_per_launch": group,
         "update_kernel": args.update_kernel,
         "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
+        # each launch is its own timing window (CUDA events around it); steps
+        # in timed order, split in halves to show drift across the run
+        "stage_percentiles_ms": {"allocate": _percentiles(launch_alloc),
+                                 "update": _percentiles(launch_update),
+                                 "step_without_reset": _percentiles(step_ms)},
+        "step_halves_median_ms": [float(np.median(step_ms[:len(step_ms) // 2] or step_ms)),
+                                  float(np.median(step_ms[len(step_ms) // 2:]))],
+        "other_processes_mib": other_mib,
         "stages_ms_per_frame": {"allocate": stage_alloc / (n * args.steps),
                                 "update": stage_update / (n * args.steps)},
         "blocks": blocks, "points_per_step": points_per_step,
@@ -469,21 +575,25 @@ def run_ours(args):
         "distinct_voxels_per_step_frame_by_frame": distinct["frame_by_frame"],
         "fixed_divisor_fast_path": vol.info["fixed_divisor_fast_path"],
         "clocks": clk,
-        "gpu_launches": args.steps * (1 + 2 * ng),
+        "gpu_launches": args.steps * (1 + sum(1 + _update_kernels(args, frames, b - a)
+                                              for a, b in groups)),
         "roofline": roofline,
         "roofline_l2_red": red_roof,
         "roofline_update_combined": combined,
         "roofline_update_launch_union": union,
         "roofline_allocate": alloc_roof,
+        "allocate_memory_terms": alloc_mem,
     }
 
     if not args.no_e2e:
         result["e2e"] = e2e_host(torch, vol, frames, args)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v, u, sample = oracle_sample(frames, args.cpu_baseline_seconds)
+        v, u, sample, ovol, n_sample = oracle_sample(frames, args.cpu_baseline_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "points/s", "cores": 1, "kind": "oracle",
                                   "sample": sample, "voxel_updates_per_s": u,
-                                  "cpu": platform.machine()}
+                                  "cpu": platform.machine(),
+                                  "parity_gate": parity_gate(torch, vol, frames, d_dev, c_dev,
+                                                             n_sample, ovol)}
     vol.close()
     if rank == 0:
         print(json.dumps(result), flush=True)
@@ -491,13 +601,15 @@ def run_ours(args):
 
 RED_MODES = ((0, "scalar_coalesced", 1), (1, "scalar_scattered", 1), (2, "v4_coalesced", 4),
              (3, "v4_scattered", 4), (4, "scalar_sector_grouped", 1))
+CAS_MODE = 5
 
 
 def measure_red_peaks(torch) -> dict:
     """L2 float-reduction throughput (red.global.add), float additions per
     second, for scalar / 4-wide operands and coalesced / scattered addresses,
-    over an L2-resident (32 MB) and an HBM-resident (4 GB) footprint; best of
-    5 launches each."""
+    over an L2-resident (32 MB) and an HBM-resident (4 GB) footprint, and the
+    rate of 64-bit compare-and-swaps on scattered 16-byte entries; best of 6
+    launches each.  Returns (reductions, compare-and-swaps)."""
     import ctypes
     from hash_blocked_tsdf_gb300 import _build
     lib = ctypes.CDLL(_build.peaks_library_path())
@@ -507,6 +619,7 @@ def measure_red_peaks(torch) -> dict:
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     stream = torch.cuda.current_stream()
     out = {}
+    cas_out = {}
     for foot, nbytes in (("l2_32MB", 32 << 20), ("hbm_4GB", 4 << 30)):
         buf = torch.zeros(nbytes // 4, dtype=torch.float32, device="cuda")
         res = {}
@@ -527,9 +640,22 @@ def measure_red_peaks(torch) -> dict:
             ops = blocks * 256 * reps
             res[name] = {"ops_per_s": ops / (best / 1e3), "adds_per_s": width * ops / (best / 1e3)}
         out[foot] = res
+        buf.zero_()
+        best = None
+        for _ in range(6):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = lib.peak_red(buf.data_ptr(), buf.numel(), CAS_MODE, 64, sms * 8,
+                              stream.cuda_stream)
+            b.record(stream)
+            assert rc == 0, rc
+            torch.cuda.synchronize()
+            best = a.elapsed_time(b) if best is None else min(best, a.elapsed_time(b))
+        cas_out[foot] = {"ops_per_s": sms * 8 * 256 * 64 / (best / 1e3)}
         del buf
     torch.cuda.empty_cache()
-    return out
+    return out, cas_out
 
 
 def _profile_record(name: str, sources) -> dict:
@@ -553,7 +679,8 @@ def _profile_record(name: str, sources) -> dict:
     if rec.get("kernel_source_sha256_16") != h.hexdigest()[:16]:
         return {}
     out = {}
-    for k in ("traffic_bytes_per_launch", "warp_instructions_per_launch"):
+    for k in ("traffic_bytes_per_launch", "warp_instructions_per_launch",
+              "l2_atomic_sectors_per_launch"):
         if k in rec:
             out[k] = float(rec[k])
     return out
