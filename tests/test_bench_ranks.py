@@ -32,7 +32,7 @@ def _rank_main(rank, world, port, out):
 
 
 def test_two_rank_timing_reduction():
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     port = _free_port()
     mp.start_processes(_rank_main, args=(2, port, out), nprocs=2, start_method="spawn")
@@ -57,7 +57,7 @@ def _reference_rank(rank, world, port, out):
 
 def test_reference_arm_prints_on_rank_zero_only(oracle_mod):
     import json
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_reference_rank, args=(2, _free_port(), out), nprocs=2,
                        start_method="spawn")
