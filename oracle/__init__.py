@@ -79,6 +79,8 @@ def load(mutant: int = 0):
                                ctypes.c_longlong),
         "oracle_clustered_coords": ([ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64, i32p,
                                      ctypes.c_int32, ctypes.c_longlong, i32p], ctypes.c_longlong),
+        "oracle_extract": ([ctypes.c_void_p, ctypes.c_longlong, f32p], ctypes.c_longlong),
+        "oracle_set_block": ([ctypes.c_void_p, i32p, f64p, f64p, f64p, f64p, f64p], ctypes.c_int),
         "oracle_mutant_id": ([], ctypes.c_int),
     }
     for name, (args, res) in sig.items():
@@ -170,6 +172,24 @@ class OracleVolume:
         out = {"coords": c}
         out.update(arrs)
         return out
+
+    def extract(self) -> np.ndarray:
+        """Marching-tetrahedra triangles of the mean TSDF's zero level set,
+        float32 [n, 3, 3] (triangle, vertex, xyz), in the oracle's cell order."""
+        n = int(self._lib.oracle_extract(self._h, 0, None))
+        out = np.zeros((n, 3, 3), dtype=np.float32)
+        if n:
+            got = self._lib.oracle_extract(self._h, n, _ptr(out, ctypes.c_float))
+            assert got == n
+        return out
+
+    def set_block(self, coord, tsdf, weight, r=None, g=None, b=None) -> None:
+        """Create or overwrite block `coord` with the given [512] sums."""
+        c = np.ascontiguousarray(np.asarray(coord, dtype=np.int32).reshape(3))
+        arrs = [None if a is None else np.ascontiguousarray(np.asarray(a, np.float64).reshape(512))
+                for a in (tsdf, weight, r, g, b)]
+        ptrs = [None if a is None else _ptr(a, ctypes.c_double) for a in arrs]
+        self._lib.oracle_set_block(self._h, _ptr(c, ctypes.c_int32), *ptrs)
 
 
 # ----------------------------------------------------------------------------

@@ -599,6 +599,192 @@ long long oracle_clustered_coords(uint64_t table_size, uint64_t window_start,
     return found;
 }
 
+/* ------------------------------------------------------------------------
+ * Extraction (read-out): the zero level set of the mean TSDF
+ *
+ * The page recovers means only at extraction (design section,
+ * accumulation: sums, divided by the weight when read) and extracts the
+ * surface by marching tetrahedra (design section; its details are not on the
+ * page).  Readings:
+ *   - lattice points are voxel centres, world position ((float)i + 0.5) * voxel
+ *     per axis; the value there is the mean RN(float(tsdf sum) / float(weight)),
+ *     and a voxel is observed iff its weight is > 0;
+ *   - cell (i, j, k) spans the 8 voxels (i..i+1, j..j+1, k..k+1); corner c has
+ *     offset (c & 1, c >> 1 & 1, c >> 2 & 1); a cell is used only when all 8
+ *     corners are observed;
+ *   - the cube is cut into the 6 tetrahedra that share its diagonal 0-7, one
+ *     per order of the axes (x,y,z), (x,z,y), (y,x,z), (y,z,x), (z,x,y),
+ *     (z,y,x): {0, 1, 3, 7}, {0, 1, 5, 7}, {0, 2, 3, 7}, {0, 2, 6, 7},
+ *     {0, 4, 5, 7}, {0, 4, 6, 7} (neighbouring cells then cut their shared
+ *     faces along the same diagonals, so the surface has no cracks);
+ *   - a corner is inside when its value is < 0;
+ *   - a surface vertex sits on every tetrahedron edge whose ends differ, at
+ *     the zero of the linear interpolation, t = fA / (fA - fB) from the lower
+ *     end A (all coordinates <= B's) towards B: p = pA + t * (pB - pA), in
+ *     float32, one rounding per operation;
+ *   - one inside (or one outside) corner o with the others a, b, c in the
+ *     tetrahedron's order: triangle (E(o,a), E(o,b), E(o,c)); two inside
+ *     corners i1, i2 and two outside o1, o2: triangles (E(i1,o1), E(i1,o2),
+ *     E(i2,o2)) and (E(i1,o1), E(i2,o2), E(i2,o1)).
+ * Triangles are written cell by cell, blocks in (x, y, z) order, voxels in
+ * storage order, tetrahedra in the order above.
+ * --------------------------------------------------------------------- */
+
+}  // extern "C"
+
+namespace {
+
+#if ORACLE_MUTANT == 16
+const int kTets[6][4] = {{0, 1, 2, 7}, {0, 1, 5, 7}, {0, 2, 3, 7},   // planted: not a tiling
+                         {0, 2, 6, 7}, {0, 4, 5, 7}, {0, 4, 6, 7}};
+#else
+const int kTets[6][4] = {{0, 1, 3, 7}, {0, 1, 5, 7}, {0, 2, 3, 7},
+                         {0, 2, 6, 7}, {0, 4, 5, 7}, {0, 4, 6, 7}};
+#endif
+
+/* Offset of cell corner c along axis ax (0 = x). */
+int corner_offset(int c, int ax) { return (c >> ax) & 1; }
+
+/* The offset used to fetch a corner's value (the same one). */
+int value_offset(int c, int ax)
+{
+#if ORACLE_MUTANT == 18
+    return (c >> (ax == 0 ? 1 : ax == 1 ? 0 : 2)) & 1;     // planted: x and y swapped
+#else
+    return corner_offset(c, ax);
+#endif
+}
+
+/* Mean TSDF of voxel (ix, iy, iz); false when the voxel is not observed. */
+bool mean_tsdf(const Volume* v, int32_t ix, int32_t iy, int32_t iz, float* f)
+{
+    const BlockCoord b{floor_div8(ix), floor_div8(iy), floor_div8(iz)};
+    auto it = v->blocks.find(b);
+    if (it == v->blocks.end() || !it->second) return false;
+    const int j = (ix - b.x * kEdge) + kEdge * (iy - b.y * kEdge) +
+                  kEdge * kEdge * (iz - b.z * kEdge);
+    const double w = it->second->weight[j];
+    if (!(w > 0.0)) return false;
+    const float sum = (float)it->second->tsdf[j];
+    const float wf = (float)w;
+#if ORACLE_MUTANT == 17
+    *f = sum;                                               // planted: not divided
+    (void)wf;
+#else
+    *f = sum / wf;
+#endif
+    return true;
+}
+
+float centre(int32_t i, float voxel) { return ((float)i + 0.5f) * voxel; }
+
+struct Cell {
+    int32_t i[3];      // corner 0
+    float f[8];        // corner values
+};
+
+/* Surface vertex on the edge between corners a < b of the cell. */
+void edge_vertex(const Cell& c, int a, int b, float voxel, float out[3])
+{
+    const float fa = c.f[a], fb = c.f[b];
+#if ORACLE_MUTANT == 15
+    const float t = fb / (fb - fa);                         // planted: from the wrong end
+#else
+    const float t = fa / (fa - fb);
+#endif
+    for (int ax = 0; ax < 3; ++ax) {
+        const float pa = centre(c.i[ax] + corner_offset(a, ax), voxel);
+        const float pb = centre(c.i[ax] + corner_offset(b, ax), voxel);
+        out[ax] = pa + t * (pb - pa);
+    }
+}
+
+void put_triangle(const Cell& c, const int e[3][2], float voxel, std::vector<float>* out)
+{
+    for (int k = 0; k < 3; ++k) {
+        const int a = std::min(e[k][0], e[k][1]), b = std::max(e[k][0], e[k][1]);
+        float p[3];
+        edge_vertex(c, a, b, voxel, p);
+        out->insert(out->end(), p, p + 3);
+    }
+}
+
+void march_tetrahedron(const Cell& c, const int* t, float voxel, std::vector<float>* out)
+{
+    int in[4], out_[4], n_in = 0, n_out = 0;
+    for (int k = 0; k < 4; ++k) {
+        if (c.f[t[k]] < 0.0f)
+            in[n_in++] = t[k];
+        else
+            out_[n_out++] = t[k];
+    }
+    if (n_in == 1 || n_in == 3) {
+        const int o = n_in == 1 ? in[0] : out_[0];
+        const int* rest = n_in == 1 ? out_ : in;
+        const int e[3][2] = {{o, rest[0]}, {o, rest[1]}, {o, rest[2]}};
+        put_triangle(c, e, voxel, out);
+    } else if (n_in == 2) {
+        const int e1[3][2] = {{in[0], out_[0]}, {in[0], out_[1]}, {in[1], out_[1]}};
+        const int e2[3][2] = {{in[0], out_[0]}, {in[1], out_[1]}, {in[1], out_[0]}};
+        put_triangle(c, e1, voxel, out);
+        put_triangle(c, e2, voxel, out);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+/* Triangles of the zero level set, 9 floats each (three vertices x, y, z);
+ * writes at most max_tris and returns the total number. */
+long long oracle_extract(void* h, long long max_tris, float* out)
+{
+    const Volume* v = static_cast<const Volume*>(h);
+    std::vector<BlockCoord> order;
+    for (const auto& kv : v->blocks)
+        if (kv.second) order.push_back(kv.first);
+    std::sort(order.begin(), order.end());
+    std::vector<float> tris;
+    for (const BlockCoord& b : order) {
+        for (int j = 0; j < kBlockVoxels; ++j) {
+            Cell c;
+            c.i[0] = b.x * kEdge + j % kEdge;
+            c.i[1] = b.y * kEdge + (j / kEdge) % kEdge;
+            c.i[2] = b.z * kEdge + j / (kEdge * kEdge);
+            bool all = true;
+            for (int k = 0; k < 8 && all; ++k)
+                all = mean_tsdf(v, c.i[0] + value_offset(k, 0), c.i[1] + value_offset(k, 1),
+                                c.i[2] + value_offset(k, 2), &c.f[k]);
+            if (!all) continue;
+            for (int t = 0; t < 6; ++t) march_tetrahedron(c, kTets[t], v->voxel, &tris);
+        }
+    }
+    const long long n = (long long)(tris.size() / 9);
+    const long long w = std::min(n, max_tris);
+    if (out && w > 0) std::memcpy(out, tris.data(), sizeof(float) * 9 * (size_t)w);
+    return n;
+}
+
+/* Set (create or overwrite) a block's five sums directly, for building
+ * volumes from a known field in the pins; tsdf_abs becomes |tsdf|. */
+int oracle_set_block(void* h, const int32_t coord[3], const double* tsdf, const double* weight,
+                     const double* r, const double* g, const double* b)
+{
+    Volume* v = static_cast<Volume*>(h);
+    const BlockCoord c{coord[0], coord[1], coord[2]};
+    std::unique_ptr<BlockSums>& s = v->blocks[c];
+    if (!s) s.reset(new BlockSums());
+    for (int j = 0; j < kBlockVoxels; ++j) {
+        s->tsdf[j] = tsdf[j];
+        s->weight[j] = weight[j];
+        s->r[j] = r ? r[j] : 0.0;
+        s->g[j] = g ? g[j] : 0.0;
+        s->b[j] = b ? b[j] : 0.0;
+        s->tsdf_abs[j] = std::fabs(tsdf[j]);
+    }
+    return 0;
+}
+
 int oracle_mutant_id(void) { return ORACLE_MUTANT; }
 
 }  // extern "C"
