@@ -20,7 +20,7 @@ CSRC = os.path.join(PKG_DIR, "csrc")
 INCLUDE = os.path.join(REPO_DIR, "include")
 BUILD_DIR = os.path.join(PKG_DIR, "_build")
 
-CUDA_SOURCES = ["tsdf_volume.cu", "tsdf_alloc.cu", "tsdf_update.cu", "tsdf_table.cu",
+CUDA_SOURCES = ["tsdf_volume.cu", "tsdf_alloc.cu", "tsdf_update.cu", "tsdf_extract.cu", "tsdf_table.cu",
                 "tsdf_noalloc.cu"]
 CUDA_HEADERS = ["tsdf_device.cuh", "tsdf_internal.h"]
 

@@ -78,6 +78,9 @@ SIGNATURES = {
     "tsdf_block_count": ([_VP, _VP, ctypes.POINTER(_U32)], _I),
     "tsdf_export_blocks": ([_VP, _VP, _U32, _U32, _VP, _VP, _VP, _VP, _VP, _VP], _I),
     "tsdf_export_table": ([_VP, _VP, _U32, _VP, _VP], _I),
+    "tsdf_extract_triangles": ([_VP, _VP, _VP, ctypes.c_uint64, ctypes.POINTER(ctypes.c_uint64)],
+                               _I),
+    "tsdf_import_blocks": ([_VP, _VP, _U32, _VP, _VP, _VP, _VP, _VP, _VP], _I),
     "tsdf_export_block_coords_noalloc": ([_VP, _VP, _U32, _U32, _VP], _I),
     "tsdf_get_stats": ([_VP, _VP, ctypes.POINTER(tsdf_stats)], _I),
     "tsdf_clear_stats": ([_VP, _VP], _I),
@@ -328,6 +331,36 @@ def tsdf_export_block_coords_noalloc(h, first: int, count: int, stream=None) -> 
     return out
 
 
+def tsdf_extract_triangles(h, stream=None, capacity=None):
+    """Marching-tetrahedra triangles of the mean TSDF's zero level set, as a
+    CUDA float32 tensor [n, 3, 3] (triangle, vertex, xyz; order unspecified).
+    Without `capacity` the library counts first and the buffer is sized to
+    fit; with it, at most `capacity` are returned."""
+    import torch
+    lib = load_library()
+    n = ctypes.c_uint64()
+    sp = _stream_ptr(stream)
+    if capacity is None:
+        _check(lib.tsdf_extract_triangles(h, sp, None, 0, ctypes.byref(n)), "tsdf_extract_triangles")
+        capacity = int(n.value)
+    out = torch.empty((max(capacity, 1), 3, 3), dtype=torch.float32, device="cuda")
+    _check(lib.tsdf_extract_triangles(h, sp, out.data_ptr(), capacity, ctypes.byref(n)),
+           "tsdf_extract_triangles")
+    return out[:min(capacity, int(n.value))]
+
+
+def tsdf_import_blocks(h, coords, tsdf, weight, r, g, b, stream=None) -> None:
+    """Set blocks from host arrays: coords int32 [n, 3] (distinct), and the
+    five float32 [n, 512] arrays."""
+    c = np.ascontiguousarray(np.asarray(coords, np.int32).reshape(-1, 3))
+    n = c.shape[0]
+    arrs = [np.ascontiguousarray(np.asarray(a, np.float32).reshape(n, 512))
+            for a in (tsdf, weight, r, g, b)]
+    _check(load_library().tsdf_import_blocks(h, _stream_ptr(stream), n, c.ctypes.data,
+                                             *[a.ctypes.data for a in arrs]),
+           "tsdf_import_blocks")
+
+
 def tsdf_export_table(h, stream=None):
     T = tsdf_get_info(h)["table_capacity"]
     keys = np.zeros(T, np.uint64)
@@ -424,6 +457,12 @@ class TsdfVolume:
 
     def export_blocks(self, first=0, count=None, stream=None, **kw) -> dict:
         return tsdf_export_blocks(self.handle, first, count, stream, **kw)
+
+    def extract_triangles(self, stream=None, capacity=None):
+        return tsdf_extract_triangles(self.handle, stream, capacity)
+
+    def import_blocks(self, coords, tsdf, weight, r, g, b, stream=None):
+        tsdf_import_blocks(self.handle, coords, tsdf, weight, r, g, b, stream)
 
     def export_table(self, stream=None):
         return tsdf_export_table(self.handle, stream)

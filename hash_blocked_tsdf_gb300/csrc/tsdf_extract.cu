@@ -1,0 +1,320 @@
+// Read-out kernels: surface extraction and block import.
+//
+// Extraction ("What Irregularity Costs", design section: the arrays hold
+// sums and the mean is recovered at extraction; the surface is extracted by
+// marching tetrahedra, once, in CUDA).  The page gives no further detail;
+// the readings, written out here and in the header:
+//   - lattice points are voxel centres, world position ((float)i + 0.5) *
+//     voxel per axis; the value there is the mean RN(tsdf sum / weight), and
+//     a voxel is observed iff its weight is > 0;
+//   - cell (i, j, k) spans voxels (i..i+1, j..j+1, k..k+1), corner c at offset
+//     (c & 1, c >> 1 & 1, c >> 2 & 1); only cells with 8 observed corners;
+//   - the cube is cut into the 6 tetrahedra around its diagonal 0-7, one per
+//     order of the axes: {0,1,3,7} {0,1,5,7} {0,2,3,7} {0,2,6,7} {0,4,5,7}
+//     {0,4,6,7}, so neighbouring cells cut shared faces alike;
+//   - inside means value < 0; a vertex sits on each tetrahedron edge whose
+//     ends differ, at t = fA / (fA - fB) from the lower end A towards B,
+//     p = pA + t (pB - pA), float32, one rounding per operation;
+//   - one odd corner o, others a, b, c in tetrahedron order: triangle
+//     (E(o,a), E(o,b), E(o,c)); two inside i1, i2 and two outside o1, o2:
+//     (E(i1,o1), E(i1,o2), E(i2,o2)) and (E(i1,o1), E(i2,o2), E(i2,o1)).
+//
+// One block of 256 threads per allocated block: the block's 512 means go to
+// shared memory, its seven upper neighbours (+x, +y, +z and their
+// combinations) are looked up in the table once, and each thread marches two
+// cells, reading corners that fall in a neighbour from the pool.  Threads
+// count their triangles first; a warp takes one range of the output with one
+// atomic and each thread writes its triangles there.
+#include "tsdf_device.cuh"
+
+namespace tsdf {
+namespace {
+
+constexpr int kThreads = 256;
+
+// Corner k (0..3) of tetrahedron `tet`: the path 0, e_p, e_p + e_q, 7 through
+// the cube, with p = tet / 2 the first axis and q the lower (tet even) or
+// higher (tet odd) of the other two -- the sets {0,1,3,7} {0,1,5,7}
+// {0,2,3,7} {0,2,6,7} {0,4,5,7} {0,4,6,7}, corners in ascending order.
+__device__ __forceinline__ int tet_corner(int tet, int k)
+{
+    const int p = tet >> 1;
+    const int lo = p == 0 ? 1 : 0, hi = p == 2 ? 1 : 2;
+    const int q = (tet & 1) ? hi : lo;
+    const int c1 = 1 << p, c2 = c1 | (1 << q);
+    return k == 0 ? 0 : k == 1 ? c1 : k == 2 ? c2 : 7;
+}
+
+// f[k] for a run-time k (0..7) without indexing a register array.
+__device__ __forceinline__ float pick8(const float f[8], int k)
+{
+    const float a = (k & 1) ? f[1] : f[0], b = (k & 1) ? f[3] : f[2];
+    const float c = (k & 1) ? f[5] : f[4], d = (k & 1) ? f[7] : f[6];
+    const float ab = (k & 2) ? b : a, cd = (k & 2) ? d : c;
+    return (k & 4) ? cd : ab;
+}
+
+__device__ __forceinline__ float lattice(int i, float voxel)
+{
+    return __fmul_rn(__fadd_rn((float)i, 0.5f), voxel);
+}
+
+// Element k (0..3, known only at run time) of four values held in registers.
+template <typename T>
+__device__ __forceinline__ T pick(T a, T b, T c, T d, int k)
+{
+    return k == 0 ? a : k == 1 ? b : k == 2 ? c : d;
+}
+
+// The tetrahedron's four corners: ids (0..7) and values, in its own order.
+struct Tet {
+    int id[4];
+    float v[4];
+};
+
+// Vertex on the edge between tetrahedron corners p and q (0..3): from the
+// lower-numbered cell corner A towards B.
+__device__ __forceinline__ void edge_vertex(const Tet& T, const int cell[3], int p, int q,
+                                            float voxel, float* out)
+{
+    int a = pick(T.id[0], T.id[1], T.id[2], T.id[3], p);
+    int b = pick(T.id[0], T.id[1], T.id[2], T.id[3], q);
+    float fa = pick(T.v[0], T.v[1], T.v[2], T.v[3], p);
+    float fb = pick(T.v[0], T.v[1], T.v[2], T.v[3], q);
+    if (a > b) {
+        const int ti = a; a = b; b = ti;
+        const float tf = fa; fa = fb; fb = tf;
+    }
+    const float t = __fdiv_rn(fa, __fsub_rn(fa, fb));
+#pragma unroll
+    for (int ax = 0; ax < 3; ++ax) {
+        const float pa = lattice(cell[ax] + ((a >> ax) & 1), voxel);
+        const float pb = lattice(cell[ax] + ((b >> ax) & 1), voxel);
+        out[ax] = __fadd_rn(pa, __fmul_rn(t, __fsub_rn(pb, pa)));
+    }
+}
+
+__device__ __forceinline__ void write_triangle(const Tet& T, const int cell[3], int p0, int q0,
+                                               int p1, int q1, int p2, int q2, float voxel,
+                                               float* tri)
+{
+    edge_vertex(T, cell, p0, q0, voxel, tri);
+    edge_vertex(T, cell, p1, q1, voxel, tri + 3);
+    edge_vertex(T, cell, p2, q2, voxel, tri + 6);
+}
+
+// Bit mask of the tetrahedron's inside corners (bit k = its corner k).
+__device__ __forceinline__ int inside_mask(const Tet& T)
+{
+    return (T.v[0] < 0.0f ? 1 : 0) | (T.v[1] < 0.0f ? 2 : 0) | (T.v[2] < 0.0f ? 4 : 0) |
+           (T.v[3] < 0.0f ? 8 : 0);
+}
+
+__device__ __forceinline__ int mask_triangles(int m)
+{
+    const int n = __popc(m);
+    return n == 2 ? 2 : (n == 1 || n == 3) ? 1 : 0;
+}
+
+// Writes the tetrahedron's triangles from index `next` on (those at or past
+// `capacity` are dropped); returns the index after them.
+__device__ __forceinline__ uint64_t emit_tet(const Tet& T, const int cell[3], float voxel,
+                                             float* out, uint64_t capacity, uint64_t next)
+{
+    const int in = inside_mask(T);
+    const int ot = ~in & 0xF;
+    const int n_in = __popc(in);
+    if (n_in == 1 || n_in == 3) {
+        // the odd corner, then the other three in tetrahedron order
+        const int odd_set = n_in == 1 ? in : ot;
+        int rest = n_in == 1 ? ot : in;
+        const int o = __ffs(odd_set) - 1;
+        const int r0 = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const int r1 = __ffs(rest) - 1;
+        rest &= rest - 1;
+        const int r2 = __ffs(rest) - 1;
+        if (next < capacity) write_triangle(T, cell, o, r0, o, r1, o, r2, voxel, out + 9 * next);
+        return next + 1;
+    }
+    if (n_in == 2) {
+        const int i0 = __ffs(in) - 1;
+        const int i1 = __ffs(in & (in - 1)) - 1;
+        const int o0 = __ffs(ot) - 1;
+        const int o1 = __ffs(ot & (ot - 1)) - 1;
+        if (next < capacity)
+            write_triangle(T, cell, i0, o0, i0, o1, i1, o1, voxel, out + 9 * next);
+        if (next + 1 < capacity)
+            write_triangle(T, cell, i0, o0, i1, o1, i1, o0, voxel, out + 9 * (next + 1));
+        return next + 2;
+    }
+    return next;
+}
+
+__device__ __forceinline__ Tet make_tet(const float f[8], int tet)
+{
+    Tet T;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        T.id[k] = tet_corner(tet, k);
+        T.v[k] = pick8(f, T.id[k]);
+    }
+    return T;
+}
+
+__global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const int32_t* coords,
+                                                          float* out, uint64_t capacity,
+                                                          unsigned long long* count)
+{
+    __shared__ float s_mean[kBlockVoxels];
+    __shared__ uint8_t s_seen[kBlockVoxels];
+    __shared__ uint32_t s_nb[8];                 // pool index of block + (d & 1, d >> 1 & 1, d >> 2 & 1)
+    const uint32_t b = blockIdx.x;
+    const int t = threadIdx.x;
+    const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
+    for (int j = t; j < kBlockVoxels; j += kThreads) {
+        const size_t e = (size_t)b * kBlockVoxels + j;
+        const float w = vol.weight[e];
+        s_seen[j] = w > 0.0f ? 1 : 0;
+        s_mean[j] = w > 0.0f ? __fdiv_rn(vol.tsdf[e], w) : 0.0f;
+    }
+    if (t < 8) {
+        uint32_t idx = kIndexFailed;
+        if (t == 0) {
+            idx = b;
+        } else {
+            const int nx = bc[0] + (t & 1), ny = bc[1] + ((t >> 1) & 1), nz = bc[2] + ((t >> 2) & 1);
+            const int hi = (1 << 20) - 1;
+            if (nx <= hi && ny <= hi && nz <= hi)
+                idx = lookup(vol.table, vol.table_mask, pack_block(nx, ny, nz));
+        }
+        s_nb[t] = idx;
+    }
+    __syncthreads();
+
+    // the two cells of this thread: corner values, observed or not; ok[c]
+    // marks a cell that is fully observed and crosses the surface
+    const float voxel = vol.div.voxel;
+    float f[2][8];
+    bool ok[2];
+    int n_tris = 0;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+        const int j = t + c * kThreads;
+        const int l[3] = {j & 7, (j >> 3) & 7, j >> 6};
+        ok[c] = true;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            int q[3], d = 0;
+#pragma unroll
+            for (int ax = 0; ax < 3; ++ax) {
+                q[ax] = l[ax] + ((k >> ax) & 1);
+                if (q[ax] == kBlockEdge) {
+                    q[ax] = 0;
+                    d |= 1 << ax;
+                }
+            }
+            const int jj = q[0] | (q[1] << 3) | (q[2] << 6);
+            float v = 0.0f;
+            bool seen;
+            if (d == 0) {
+                seen = s_seen[jj] != 0;
+                v = s_mean[jj];
+            } else {
+                const uint32_t nb = s_nb[d];
+                seen = false;
+                if (nb < vol.pool_capacity) {
+                    const size_t e = (size_t)nb * kBlockVoxels + jj;
+                    const float w = vol.weight[e];
+                    seen = w > 0.0f;
+                    if (seen) v = __fdiv_rn(vol.tsdf[e], w);
+                }
+            }
+            ok[c] = ok[c] && seen;
+            f[c][k] = v;
+        }
+        // a cell whose corners are all inside or all outside holds no surface
+        int n_neg = 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) n_neg += f[c][k] < 0.0f ? 1 : 0;
+        ok[c] = ok[c] && n_neg != 0 && n_neg != 8;
+        if (ok[c]) {
+#pragma unroll 1
+            for (int tet = 0; tet < 6; ++tet)
+                n_tris += mask_triangles(inside_mask(make_tet(f[c], tet)));
+        }
+    }
+
+    // one output range per warp
+    const unsigned lane = lane_id();
+    uint32_t incl = (uint32_t)n_tris;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if ((int)lane >= d) incl += y;
+    }
+    unsigned long long base = 0;
+    if (lane == 31 && incl) base = atomicAdd(count, (unsigned long long)incl);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    uint64_t next = base + incl - (uint32_t)n_tris;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+        if (!ok[c]) continue;
+        const int j = t + c * kThreads;
+        const int cell[3] = {bc[0] * kBlockEdge + (j & 7), bc[1] * kBlockEdge + ((j >> 3) & 7),
+                             bc[2] * kBlockEdge + (j >> 6)};
+        float fc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) fc[k] = c == 0 ? f[0][k] : f[1][k];
+#pragma unroll 1
+        for (int tet = 0; tet < 6; ++tet)
+            next = emit_tet(make_tet(fc, tet), cell, voxel, out, capacity, next);
+    }
+}
+
+// Block b of the input: find its pool index (inserted just before) and copy
+// its five arrays there.
+__global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const int32_t* coords,
+                                                         const float* src)
+{
+    __shared__ uint32_t s_idx;
+    const uint32_t b = blockIdx.x;
+    const uint32_t n = gridDim.x;
+    if (threadIdx.x == 0) {
+        const int x = coords[3 * b], y = coords[3 * b + 1], z = coords[3 * b + 2];
+        const int lo = -(1 << 20), hi = (1 << 20) - 1;
+        uint32_t idx = kIndexFailed;
+        if (x >= lo && x <= hi && y >= lo && y <= hi && z >= lo && z <= hi)
+            idx = lookup(vol.table, vol.table_mask, pack_block(x, y, z));
+        s_idx = idx;
+    }
+    __syncthreads();
+    const uint32_t idx = s_idx;
+    if (idx >= vol.pool_capacity) return;           // refused (pool full) or out of range
+    float* dst[5] = {vol.tsdf, vol.weight, vol.red, vol.green, vol.blue};
+    for (int a = 0; a < 5; ++a)
+        for (int j = threadIdx.x; j < kBlockVoxels; j += kThreads)
+            dst[a][(size_t)idx * kBlockVoxels + j] =
+                src[((size_t)a * n + b) * kBlockVoxels + j];
+}
+
+}  // namespace
+
+cudaError_t launch_extract(const VolumeView& vol, const int32_t* coords, uint32_t n_blocks,
+                           float* out, uint64_t capacity, unsigned long long* count,
+                           cudaStream_t stream)
+{
+    if (n_blocks == 0) return cudaSuccess;
+    extract_kernel<<<n_blocks, kThreads, 0, stream>>>(vol, coords, out, capacity, count);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_import(const VolumeView& vol, const int32_t* coords, uint32_t n,
+                          const float* src, cudaStream_t stream)
+{
+    if (n == 0) return cudaSuccess;
+    import_kernel<<<n, kThreads, 0, stream>>>(vol, coords, src);
+    return cudaGetLastError();
+}
+
+}  // namespace tsdf

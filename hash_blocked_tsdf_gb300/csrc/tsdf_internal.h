@@ -110,6 +110,15 @@ cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
 cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int role,
                                         unsigned long long* mismatches, cudaStream_t stream);
 cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
+// Marching tetrahedra over blocks [0, n_blocks) (coords[idx] = coordinate of
+// pool index idx); triangles past `capacity` are counted, not written.
+cudaError_t launch_extract(const VolumeView& vol, const int32_t* coords, uint32_t n_blocks,
+                           float* out, uint64_t capacity, unsigned long long* count,
+                           cudaStream_t stream);
+// Copy block i's five arrays (src: [5][n][512]) to the pool slot the table
+// gives its coordinate (inserted beforehand).
+cudaError_t launch_import(const VolumeView& vol, const int32_t* coords, uint32_t n,
+                          const float* src, cudaStream_t stream);
 cudaError_t launch_export_coords(const VolumeView& vol, int32_t* coords, cudaStream_t stream);
 
 }  // namespace tsdf

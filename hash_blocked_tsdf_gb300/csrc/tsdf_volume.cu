@@ -1,6 +1,8 @@
 // Host side of libtsdf.so: the C ABI declared in include/tsdf.h.  It owns
 // the volume's device memory, validates every argument before enqueueing
 // anything, and launches the kernels on the caller's stream.
+#include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -20,7 +22,9 @@ struct DeviceState {
     uint32_t dense_count;       // adaptive update: dense tiles listed in this launch,
     uint32_t dense_next;        // ... taken by the pre-reducing kernel,
     uint32_t dense_done;        // ... whose blocks count out here (all three are zero
-    uint32_t pad[4];            //     between launches)
+                                //     between launches)
+    unsigned long long triangles;   // extraction: triangles found
+    uint32_t pad[2];
     DeviceCounters counters;
 };
 
@@ -513,6 +517,71 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
                                   cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(sums)");
     }
     TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    return TSDF_OK;
+}
+
+int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uint64_t capacity,
+                           uint64_t* n_out)
+{
+    uint32_t n = 0;
+    int rc = tsdf_block_count(vol, stream, &n);
+    if (rc) return rc;
+    if (!n_out) return fail(TSDF_ERR_ARG, "n_out is null");
+    if (!triangles && capacity) return fail(TSDF_ERR_ARG, "triangles is null but capacity > 0");
+    cudaStream_t s = as_stream(stream);
+    if (!vol->coords)
+        TSDF_CUDA(cudaMalloc(&vol->coords, (size_t)vol->pool_capacity * 3 * sizeof(int32_t)),
+                  "cudaMalloc(coords)");
+    const VolumeView w = view_of(vol);
+    TSDF_CUDA(launch_export_coords(w, vol->coords, s), "export_coords kernel");
+    TSDF_CUDA(cudaMemsetAsync(&vol->state->triangles, 0, sizeof(unsigned long long), s),
+              "cudaMemsetAsync(triangles)");
+    TSDF_CUDA(launch_extract(w, vol->coords, n, triangles, capacity, &vol->state->triangles, s),
+              "extract kernel");
+    unsigned long long total = 0;
+    TSDF_CUDA(cudaMemcpyAsync(&total, &vol->state->triangles, sizeof(total),
+                              cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(triangles)");
+    TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    *n_out = total;
+    return TSDF_OK;
+}
+
+int tsdf_import_blocks(tsdf_volume* vol, void* stream, uint32_t n, const int32_t* coords,
+                       const float* tsdf_in, const float* weight, const float* r, const float* g,
+                       const float* b)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (n == 0) return TSDF_OK;
+    if (!coords || !tsdf_in || !weight || !r || !g || !b)
+        return fail(TSDF_ERR_ARG, "null host array");
+    {
+        std::vector<std::array<int32_t, 3>> c(n);
+        for (uint32_t i = 0; i < n; ++i) c[i] = {coords[3 * i], coords[3 * i + 1], coords[3 * i + 2]};
+        std::sort(c.begin(), c.end());
+        for (uint32_t i = 1; i < n; ++i)
+            if (c[i] == c[i - 1]) return fail(TSDF_ERR_ARG, "duplicate block coordinate");
+    }
+    cudaStream_t s = as_stream(stream);
+    const size_t n_vals = (size_t)n * kBlockVoxels;
+    int32_t* d_coords = nullptr;
+    float* d_vals = nullptr;
+    cudaError_t e = cudaMalloc(&d_coords, (size_t)n * 3 * sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaMalloc(&d_vals, 5 * n_vals * sizeof(float));
+    const float* src[5] = {tsdf_in, weight, r, g, b};
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(d_coords, coords, (size_t)n * 3 * sizeof(int32_t),
+                            cudaMemcpyHostToDevice, s);
+    for (int a = 0; a < 5 && e == cudaSuccess; ++a)
+        e = cudaMemcpyAsync(d_vals + a * n_vals, src[a], n_vals * sizeof(float),
+                            cudaMemcpyHostToDevice, s);
+    const VolumeView w = view_of(vol);
+    if (e == cudaSuccess) e = launch_allocate_blocks(w, d_coords, n, vol->instrument, s);
+    if (e == cudaSuccess) e = launch_import(w, d_coords, n, d_vals, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (d_coords) cudaFree(d_coords);
+    if (d_vals) cudaFree(d_vals);
+    if (e != cudaSuccess) return cuda_fail(e, "tsdf_import_blocks");
     return TSDF_OK;
 }
 

@@ -250,6 +250,48 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
 int tsdf_export_block_coords_noalloc(tsdf_volume* vol, void* stream, uint32_t first,
                                      uint32_t count, int32_t* coords);
 
+/* Extract the surface: the zero level set of the mean TSDF (tsdf sum /
+ * weight; "What Irregularity Costs", design section: sums are stored and the
+ * mean is recovered at extraction, by marching tetrahedra).  Readings, as the
+ * page gives no detail:
+ *   - lattice points are voxel centres, world ((float)i + 0.5) * voxel_size
+ *     per axis; a voxel is observed iff its weight > 0; its value is the
+ *     float32 quotient tsdf / weight;
+ *   - cell (i, j, k) spans voxels (i..i+1, j..j+1, k..k+1) and is used only if
+ *     all 8 are observed; corner c has offset (c & 1, c >> 1 & 1, c >> 2 & 1);
+ *   - each cell is cut into the 6 tetrahedra {0,1,3,7} {0,1,5,7} {0,2,3,7}
+ *     {0,2,6,7} {0,4,5,7} {0,4,6,7} (watertight across cells);
+ *   - a corner is inside when its value is < 0; a vertex lies on every
+ *     tetrahedron edge whose ends differ, at t = fA / (fA - fB) from the
+ *     lower-numbered end A: p = pA + t (pB - pA), float32;
+ *   - one odd corner o (others a, b, c in tetrahedron order): triangle
+ *     (E(o,a), E(o,b), E(o,c)); two inside i1 < i2, two outside o1 < o2:
+ *     (E(i1,o1), E(i1,o2), E(i2,o2)) and (E(i1,o1), E(i2,o2), E(i2,o1)).
+ * `triangles` is device memory, float32 [capacity][3][3] (triangle, vertex,
+ * xyz), borrowed; the triangle order is unspecified.  *n_out receives the
+ * total number of triangles, which may exceed `capacity`: then only
+ * `capacity` of them are written (call again with a larger buffer).
+ * `triangles` may be NULL with capacity 0 to count only.  Synchronises
+ * `stream`.  TSDF_ERR_ARG for a null n_out, or a null buffer with
+ * capacity > 0. */
+int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uint64_t capacity,
+                           uint64_t* n_out);
+
+/* Set blocks from host arrays (restoring a saved volume, or loading a known
+ * field): for each of the n block coordinates (int32 [n][3], all distinct),
+ * ensure the block exists through the allocate kernel's insert path, then
+ * overwrite its five arrays with tsdf, weight, r, g, b (float32 [n][512]
+ * each, voxel j = lx + 8 ly + 64 lz, the layout tsdf_export_blocks
+ * returns).  Blocks that find the pool full are counted (pool_exhausted) and
+ * left unwritten; coordinates outside [-2^20, 2^20 - 1] are counted as out of
+ * range.  The host arrays are copied before the call returns; the call
+ * allocates and frees device staging and synchronises `stream`.
+ * TSDF_ERR_ARG for a null array or a repeated coordinate (nothing is
+ * enqueued), TSDF_ERR_OOM if staging cannot be allocated. */
+int tsdf_import_blocks(tsdf_volume* vol, void* stream, uint32_t n, const int32_t* coords,
+                       const float* tsdf, const float* weight, const float* r, const float* g,
+                       const float* b);
+
 /* Copy the raw hash table to the host after synchronising `stream`: keys
  * uint64 [table_capacity] (TSDF_EMPTY_KEY for an empty slot) and indices
  * uint32 [table_capacity].  `capacity` must equal the table capacity. Either
