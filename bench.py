@@ -66,7 +66,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--pool", type=int, default=0,
                     help="override the workload's pool capacity in blocks (small profiling runs)")
-    ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced"],
+    ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
                     default="adaptive", help="how the library's update reaches the pool")
     return ap.parse_args()
 
@@ -334,7 +334,11 @@ def _percentiles(xs) -> dict:
 
 def _update_kernels(args, frames, n_frames: int) -> int:
     """Kernels one update launch runs: the adaptive mode runs the per-sample
-    and the pre-reducing kernel when the launch holds 2^18 pixels or more."""
+    and the pre-reducing kernel when the launch holds 2^18 pixels or more;
+    the fused mode runs one kernel for both stages (counted here, with the
+    allocate counted as none)."""
+    if args.update_kernel == "fused":
+        return 0
     if args.update_kernel == "adaptive" and frames.width * frames.height * n_frames >= 1 << 18:
         return 2
     return 1
@@ -448,10 +452,29 @@ def run_ours(args):
     group = args.group or vol.info["max_frames_per_launch"]
     groups = [(a, min(n, a + group)) for a in range(0, n, group)]
 
+    fused = args.update_kernel == "fused"
+
+    def one_fused_step():
+        rc = lib.tsdf_reset(h, sptr)
+        assert rc == 0
+        for a, b in groups:
+            rc = lib.tsdf_integrate_batch(h, b - a, dptr + 4 * a * px, cptr + 12 * a * px,
+                                          frames.width, frames.height, kp, pps[a], sptr)
+            assert rc == 0, lib.tsdf_last_error()
+
     def one_step(events=None):
         rc = lib.tsdf_reset(h, sptr)
         assert rc == 0
         for g, (a, b) in enumerate(groups):
+            if fused:
+                # one call, one kernel: its time is booked as the update stage
+                if events is not None:
+                    events[2 * g].record(stream)
+                    events[2 * g + 1].record(stream)
+                rc = lib.tsdf_integrate_batch(h, b - a, dptr + 4 * a * px, cptr + 12 * a * px,
+                                              frames.width, frames.height, kp, pps[a], sptr)
+                assert rc == 0, lib.tsdf_last_error()
+                continue
             if events is not None:
                 events[2 * g].record(stream)
             rc = lib.tsdf_allocate_batch(h, b - a, dptr + 4 * a * px, frames.width,
@@ -527,7 +550,8 @@ def run_ours(args):
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
     # the kernels the update stage launches in the selected mode
     upd_kernel = {"per_sample": "update_kernel", "pre_reduced": "update_rows_kernel",
-                  "adaptive": "update_kernel+update_rows_kernel"}[args.update_kernel]
+                  "adaptive": "update_kernel+update_rows_kernel",
+                  "fused": "integrate_fused_kernel"}[args.update_kernel]
     prof_upd = _profile_record(f"update_{args.update_kernel}_room_walk_1280x720.md",
                                ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md",
@@ -602,6 +626,8 @@ def run_ours(args):
         "frames_per_launch": group,
         "update_kernel": args.update_kernel,
         "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
+        "stages_note": ("fused: one kernel per group, booked as the update stage" if fused
+                        else "allocate launch, then update launch(es), per group"),
         # each launch is its own timing window (CUDA events around it); steps
         # in timed order, split in halves to show drift across the run
         "stage_percentiles_ms": {"allocate": _percentiles(launch_alloc),
@@ -628,9 +654,30 @@ def run_ours(args):
         "allocate_memory_terms": alloc_mem,
     }
 
-    result["extraction"] = measure_extraction(torch, vol, blocks, hbm_peak)
     if not args.no_e2e:
         result["e2e"] = e2e_host(torch, vol, frames, args)
+    result["extraction"] = measure_extraction(torch, vol, blocks, hbm_peak)
+    if not fused:
+        # the fused allocate+update variant on the same frames, same protocol
+        # (not the headline: integration as specified runs two kernels)
+        vol.set_update_kernel("fused")
+        for _ in range(max(args.warmup, 1)):
+            one_fused_step()
+        torch.cuda.synchronize()
+        fa = torch.cuda.Event(enable_timing=True)
+        fb_ = torch.cuda.Event(enable_timing=True)
+        fa.record(stream)
+        for _ in range(args.steps):
+            one_fused_step()
+        fb_.record(stream)
+        torch.cuda.synchronize()
+        fused_ms = max_over_ranks(fa.elapsed_time(fb_), world)
+        result["variant_fused"] = {
+            "value": sum_over_ranks(points_per_step * args.steps, world) / (fused_ms / 1000.0),
+            "unit": "points/s", "ms_per_step": fused_ms / args.steps,
+            "note": "tsdf_integrate_batch per group with TSDF_UPDATE_FUSED: one kernel "
+                    "allocates and updates (dense tiles pre-reduced by a second)"}
+        vol.set_update_kernel(args.update_kernel)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, u, sample, ovol, n_sample = oracle_sample(frames, args.cpu_baseline_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "points/s", "cores": 1, "kind": "oracle",

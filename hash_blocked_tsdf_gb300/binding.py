@@ -51,7 +51,8 @@ class tsdf_stats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in (
         "blocks_allocated", "pool_exhausted", "probe_overflow", "missed_contributions",
         "out_of_range_samples", "valid_points", "voxel_updates", "probe_inserts",
-        "probe_steps", "probe_max")] + [("probe_hist", ctypes.c_uint64 * PROBE_HIST_BINS)]
+        "probe_steps", "probe_max")] + [("probe_hist", ctypes.c_uint64 * PROBE_HIST_BINS),
+                                         ("publish_timeouts", ctypes.c_uint64)]
 
 
 _VP = ctypes.c_void_p
@@ -390,14 +391,16 @@ def tsdf_set_instrumentation(h, on: bool) -> None:
 UPDATE_ADAPTIVE = 0
 UPDATE_PER_SAMPLE = 1
 UPDATE_PRE_REDUCED = 2
+UPDATE_FUSED = 3
 UPDATE_KERNELS = {"adaptive": UPDATE_ADAPTIVE, "per_sample": UPDATE_PER_SAMPLE,
-                  "pre_reduced": UPDATE_PRE_REDUCED}
+                  "pre_reduced": UPDATE_PRE_REDUCED, "fused": UPDATE_FUSED}
 
 
 def tsdf_set_update_kernel(h, kind) -> None:
     """Select how updates reach the pool: "adaptive" (default: each tile
-    pre-reduces where samples crowd into voxels), "per_sample" or
-    "pre_reduced"; or the header's integer constants."""
+    pre-reduces where samples crowd into voxels), "per_sample",
+    "pre_reduced", or "fused" (integrate calls run allocate and update as one
+    kernel); or the header's integer constants."""
     k = UPDATE_KERNELS[kind] if isinstance(kind, str) else int(kind)
     _check(load_library().tsdf_set_update_kernel(h, k), "tsdf_set_update_kernel")
 

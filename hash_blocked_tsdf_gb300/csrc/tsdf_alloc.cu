@@ -49,20 +49,31 @@ __device__ __forceinline__ void init_probe_stats(ProbeStats* st)
     __syncthreads();
 }
 
+// What an offering lane learns from an insert step: the outcome for its key
+// (found, won or overflow) and the key's slot.
+struct InsertResult {
+    int res;
+    uint32_t slot;
+};
+
 // One warp-wide insert step: lanes with `fresh` set offer `key`; equal keys
 // are merged, one leader per key probes, and the warp's winners take pool
-// indices together.  Must be called by all 32 lanes.
+// indices together and publish them before the step returns.  Every offering
+// lane gets its key's outcome and slot.  Must be called by all 32 lanes.
 template <bool kInstrument>
-__device__ __forceinline__ void warp_insert_step(const VolumeView& vol, bool fresh,
-                                                 unsigned long long key, ProbeStats* st)
+__device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, bool fresh,
+                                                         unsigned long long key, ProbeStats* st)
 {
     const unsigned lane = lane_id();
+    InsertResult out = {kProbeOverflow, 0u};
     const unsigned fresh_mask = __ballot_sync(0xFFFFFFFFu, fresh);
-    if (fresh_mask == 0) return;
+    if (fresh_mask == 0) return out;
     bool leader = false;
+    int leader_lane = (int)lane;
     if (fresh) {
         const unsigned group = __match_any_sync(fresh_mask, key);
-        leader = lane == (unsigned)(__ffs(group) - 1);
+        leader_lane = __ffs(group) - 1;
+        leader = (int)lane == leader_lane;
     }
     int res = kProbeFound;
     uint32_t slot = 0, steps = 0;
@@ -71,9 +82,11 @@ __device__ __forceinline__ void warp_insert_step(const VolumeView& vol, bool fre
         if (kInstrument) record_probe(st, steps);
         if (res == kProbeOverflow) atomicAdd(&vol.counters->probe_overflow, 1ull);
     }
+    out.res = __shfl_sync(0xFFFFFFFFu, res, leader_lane);
+    out.slot = __shfl_sync(0xFFFFFFFFu, slot, leader_lane);
     const bool won = leader && res == kProbeWon;
     const unsigned won_mask = __ballot_sync(0xFFFFFFFFu, won);
-    if (won_mask == 0) return;
+    if (won_mask == 0) return out;
     const int first = __ffs(won_mask) - 1;
     uint32_t base = 0;
     if ((int)lane == first) base = atomicAdd(vol.pool_counter, (uint32_t)__popc(won_mask));
@@ -87,6 +100,7 @@ __device__ __forceinline__ void warp_insert_step(const VolumeView& vol, bool fre
             atomicAdd(&vol.counters->pool_exhausted, 1ull);
         }
     }
+    return out;
 }
 
 // Longest band for which a thread keeps its distinct keys in registers.
@@ -202,6 +216,183 @@ __global__ void __launch_bounds__(kThreads) allocate_blocks_kernel(VolumeView vo
     if (kInstrument) flush_probe_stats(&st, vol.counters);
 }
 
+// ---------------------------------------------------------------------------
+// Fused integrate: allocate and update in one kernel.
+// ---------------------------------------------------------------------------
+
+// Waits for a published index are bounded by this many polls (~64 ns apart).
+constexpr uint32_t kPublishSpinLimit = 1u << 20;
+
+__device__ __forceinline__ void red_add(float* addr, float v)
+{
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// The pool index published in `slot`.  The lane that claimed the slot takes
+// the index from the pool counter and stores it in the same insert step,
+// waiting on nothing, so this wait is short; it is bounded all the same: a
+// wait that gives up reports PENDING and the caller counts it.
+__device__ __forceinline__ uint32_t published_index(const VolumeView& vol, uint32_t slot)
+{
+    const volatile uint32_t* p = &vol.table[slot].idx;
+    uint32_t idx = *p;
+    for (uint32_t n = 0; idx == kIndexPending && n < kPublishSpinLimit; ++n) {
+        __nanosleep(64);
+        idx = *p;
+    }
+    return idx;
+}
+
+// One walk per pixel does both stages: the band's samples (voxel, tsdf) are
+// kept in registers while the distinct block keys go through the allocate
+// kernel's warp insert rounds; each round's result (the key's slot, hence
+// its pool index) then serves the update's reductions for that key's
+// samples, with no second walk and no lookup.  Tiles and warp patches as in
+// the per-sample update kernel (16 x 16, 8 x 4), grid tile-major, frame-minor.
+// With kSparseOnly a dense tile (the adaptive rule) still allocates here but
+// is listed for the pre-reducing update instead of adding its samples.
+template <bool kInstrument, bool kFast, bool kSparseOnly>
+__global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
+    VolumeView vol, const __grid_constant__ FrameBatch fb)
+{
+    __shared__ ProbeStats st;
+    __shared__ uint32_t s_listed;
+    if (kInstrument) init_probe_stats(&st);
+
+    const int f = blockIdx.x % fb.n;
+    const int tile = blockIdx.x / fb.n;
+    const int tiles_x = (fb.width + 15) / 16;
+    const Camera cam = fb.frame[f].cam;
+    const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31u);
+    const int u = (tile % tiles_x) * 16 + (w & 1) * 8 + (l & 7);
+    const int v = (tile / tiles_x) * 16 + (w >> 1) * 4 + (l >> 3);
+    const bool inside = u < fb.width && v < fb.height;
+    const float depth = inside ? __ldg(fb.frame[f].depth + (size_t)v * fb.width + u) : 0.0f;
+    bool listed = false;                    // this tile's samples are left to the pre-reduction
+    if (kSparseOnly) {
+        const uint32_t n_valid = (uint32_t)__syncthreads_count(valid_depth(depth));
+        const uint32_t n_dense =
+            (uint32_t)__syncthreads_count(dense_pixel(depth, vol.div.voxel, cam.fx, fb.n));
+        if (dense_tile(n_valid, n_dense)) {             // uniform over the block
+            if (threadIdx.x == 0) {
+                const uint32_t pos = atomicAdd(vol.dense_count, 1u);
+                s_listed = pos < vol.dense_capacity ? 1u : 0u;
+                if (s_listed) vol.dense_list[pos] = (uint32_t)f << 24 | (uint32_t)tile;
+            }
+            __syncthreads();
+            listed = s_listed != 0;
+        }
+    }
+    RayPoint p;
+    bool valid = false;
+    float cr = 0.0f, cg = 0.0f, cb = 0.0f;
+    if (inside) {
+        const size_t pix = (size_t)v * fb.width + u;
+        valid = back_project(cam, u, v, depth, p);
+        if (valid && !listed) {
+            const float* rgb = fb.frame[f].rgb;
+            cr = __ldg(rgb + 3 * pix);
+            cg = __ldg(rgb + 3 * pix + 1);
+            cb = __ldg(rgb + 3 * pix + 2);
+        }
+    }
+    const int steps = 2 * vol.band_half + 1;
+    // distinct keys, newest first, each with the mask of its band steps; and
+    // per step the sample's voxel in its block and its tsdf
+    unsigned long long keys[kShortBand];
+    uint32_t masks[kShortBand];
+    int lv[kShortBand];
+    float tv[kShortBand];
+    int n_keys = 0;
+    unsigned long long last = kEmptyKey;
+    uint32_t out_of_range = 0;
+#pragma unroll
+    for (int j = 0; j < kShortBand; ++j) {
+        keys[j] = kEmptyKey;
+        masks[j] = 0;
+        lv[j] = 0;
+        tv[j] = 0.0f;
+        if (valid && j < steps) {
+            VoxelSample s;
+            const int status = band_sample<kFast>(cam, vol.div, p, j - vol.band_half, s);
+            if (status == kSamplePass) {
+                lv[j] = local_voxel(s.ix, s.iy, s.iz);
+                tv[j] = s.tsdf;
+                const unsigned long long key = block_key(s.ix, s.iy, s.iz);
+                if (key != last) {          // static indices only
+#pragma unroll
+                    for (int m = kShortBand - 1; m > 0; --m) {
+                        keys[m] = keys[m - 1];
+                        masks[m] = masks[m - 1];
+                    }
+                    keys[0] = key;
+                    masks[0] = 1u << j;
+                    ++n_keys;
+                    last = key;
+                } else {
+                    masks[0] |= 1u << j;
+                }
+            } else if (status == kSampleOutOfRange) {
+                ++out_of_range;
+            }
+        }
+    }
+    uint32_t updates = 0, missed = 0, timeouts = 0;
+    const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)n_keys);
+    for (int r = 0; r < rounds; ++r) {
+        const bool offered = r < n_keys;
+        const InsertResult ins = warp_insert_step<kInstrument>(vol, offered, keys[0], &st);
+        __syncwarp();                       // this warp's winners have published
+        if (offered) {
+            const uint32_t m = masks[0];
+            uint32_t idx = kIndexFailed;
+            if (ins.res != kProbeOverflow) {
+                idx = published_index(vol, ins.slot);
+                if (idx == kIndexPending) ++timeouts;
+            }
+            if (listed) {
+                // allocated here; the pre-reducing update adds the samples
+            } else if (idx < vol.pool_capacity) {
+                const size_t base = (size_t)idx * kBlockVoxels;
+#pragma unroll
+                for (int j = 0; j < kShortBand; ++j) {
+                    if (m & (1u << j)) {
+                        const size_t e = base + (size_t)lv[j];
+                        red_add(vol.tsdf + e, tv[j]);
+                        red_add(vol.weight + e, 1.0f);
+                        red_add(vol.red + e, cr);
+                        red_add(vol.green + e, cg);
+                        red_add(vol.blue + e, cb);
+                        ++updates;
+                    }
+                }
+            } else {
+                missed += (uint32_t)__popc(m);   // absent (overflow), FAILED or timed out
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < kShortBand - 1; ++m) {
+            keys[m] = keys[m + 1];
+            masks[m] = masks[m + 1];
+        }
+    }
+    const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, (valid && !listed) ? 1u : 0u);
+    const uint32_t w_updates = __reduce_add_sync(0xFFFFFFFFu, updates);
+    const uint32_t w_missed = __reduce_add_sync(0xFFFFFFFFu, missed);
+    const uint32_t w_oor = __reduce_add_sync(0xFFFFFFFFu, out_of_range);
+    const uint32_t w_timeouts = __reduce_add_sync(0xFFFFFFFFu, timeouts);
+    if (l == 0) {
+        const int stripe = blockIdx.x % kCounterStripes;
+        if (w_valid) atomicAdd(&vol.counters->valid_points[stripe], (unsigned long long)w_valid);
+        if (w_updates)
+            atomicAdd(&vol.counters->voxel_updates[stripe], (unsigned long long)w_updates);
+        if (w_missed) atomicAdd(&vol.counters->missed[stripe], (unsigned long long)w_missed);
+        if (w_oor) atomicAdd(&vol.counters->out_of_range[stripe], (unsigned long long)w_oor);
+        if (w_timeouts) atomicAdd(&vol.counters->publish_timeouts, (unsigned long long)w_timeouts);
+    }
+    if (kInstrument) flush_probe_stats(&st, vol.counters);
+}
+
 }  // namespace
 
 template <bool kInstrument, bool kFast>
@@ -243,6 +434,36 @@ cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords,
     else
         allocate_blocks_kernel<false><<<grid, kThreads, 0, stream>>>(vol, coords, n);
     return cudaGetLastError();
+}
+
+template <bool kInstrument, bool kFast>
+void launch_fused_t(const VolumeView& vol, const FrameBatch& fb, bool sparse_only, unsigned grid,
+                    cudaStream_t stream)
+{
+    if (sparse_only)
+        integrate_fused_kernel<kInstrument, kFast, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+    else
+        integrate_fused_kernel<kInstrument, kFast, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+}
+
+cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,
+                                   cudaStream_t stream)
+{
+    if (2 * vol.band_half + 1 > kShortBand) return cudaErrorInvalidValue;
+    const unsigned tiles = (unsigned)(((fb.width + 15) / 16) * ((fb.height + 15) / 16));
+    const unsigned grid = tiles * (unsigned)fb.n;
+    const bool sparse_only =
+        (uint64_t)fb.width * (uint64_t)fb.height * (uint64_t)fb.n >= kAdaptiveMinPixels;
+    if (instrument) {
+        if (vol.fast_div) launch_fused_t<true, true>(vol, fb, sparse_only, grid, stream);
+        else launch_fused_t<true, false>(vol, fb, sparse_only, grid, stream);
+    } else {
+        if (vol.fast_div) launch_fused_t<false, true>(vol, fb, sparse_only, grid, stream);
+        else launch_fused_t<false, false>(vol, fb, sparse_only, grid, stream);
+    }
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || !sparse_only) return e;
+    return launch_update_listed(vol, fb, stream);
 }
 
 }  // namespace tsdf

@@ -258,4 +258,33 @@ __device__ __forceinline__ uint32_t lookup(const Entry* __restrict__ table, uint
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
+// Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
+// at least half of its valid pixels (finite depth > 0) see a voxel edge at
+// least w pixels wide (voxel * fx >= w * depth): there samples crowd into few
+// voxels and summing them on chip pays; below, they rarely share a voxel and
+// direct additions are cheaper.  Measured on GB300 the crossing lies near 5
+// pixels for launches of several frames (the frames' samples of a voxel
+// meet in L2 as well) and near 10 for a single frame.  The kernels that add
+// samples one by one (the per-sample update kernel and the fused integrate
+// kernel) apply this rule to their 16 x 16 tiles and list the dense ones for
+// the pre-reducing kernel, so every tile is integrated exactly once.
+// Launches below kAdaptiveMinPixels pixels add every sample directly (there
+// launch latency dominates).
+constexpr uint32_t kAdaptiveMinPixels = 1u << 18;
+
+__device__ __forceinline__ float dense_width(int n_frames) { return n_frames >= 4 ? 5.0f : 10.0f; }
+
+__device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
+
+__device__ __forceinline__ bool dense_pixel(float d, float voxel, float fx, int n_frames)
+{
+    return valid_depth(d) && __fmul_rn(voxel, fx) >= __fmul_rn(dense_width(n_frames), d);
+}
+
+__device__ __forceinline__ bool dense_tile(uint32_t n_valid, uint32_t n_dense)
+{
+    return n_valid != 0 && 2 * n_dense >= n_valid;
+}
+
+
 }  // namespace tsdf

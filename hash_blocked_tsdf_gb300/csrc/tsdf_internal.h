@@ -31,7 +31,8 @@ struct DeviceCounters {
     unsigned long long probe_inserts;
     unsigned long long probe_steps;
     unsigned long long probe_max;
-    unsigned long long reserved[3];
+    unsigned long long reserved[2];
+    unsigned long long publish_timeouts;    // fused integrate: waits for an index that gave up
     unsigned long long probe_hist[TSDF_PROBE_HIST_BINS];
     unsigned long long missed[kCounterStripes];
     unsigned long long out_of_range[kCounterStripes];
@@ -98,6 +99,15 @@ struct FrameBatch {
 
 cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                             cudaStream_t stream);
+// The pre-reducing update of the dense tiles listed in vol.dense_list (by
+// the per-sample update or the fused integrate kernel of the same batch).
+cudaError_t launch_update_listed(const VolumeView& vol, const FrameBatch& fb,
+                                 cudaStream_t stream);
+// Allocate and update in one kernel (bands of at most 9 samples); for
+// launches of 2^18 pixels or more the dense tiles are listed and pre-reduced
+// by a second kernel, as in the adaptive update.
+cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,
+                                   cudaStream_t stream);
 cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,
                                    bool instrument, cudaStream_t stream);
 // kind: TSDF_UPDATE_ADAPTIVE, TSDF_UPDATE_PER_SAMPLE or TSDF_UPDATE_PRE_REDUCED.

@@ -49,32 +49,6 @@ __device__ __forceinline__ void red_add(float* addr, float v)
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
-// Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
-// at least half of its valid pixels (finite depth > 0) see a voxel edge at
-// least w pixels wide (voxel * fx >= w * depth): there samples crowd into few
-// voxels and summing them on chip pays; below, they rarely share a voxel and
-// direct additions are cheaper.  Measured on GB300 the crossing lies near 5
-// pixels for launches of several frames (the frames' samples of a voxel
-// meet in L2 as well) and near 10 for a single frame.  The rule and its
-// inputs are the same in both update kernels, so every tile is integrated by
-// exactly one of them.  Launches below kAdaptiveMinPixels pixels use the
-// per-sample kernel alone (there launch latency dominates).
-constexpr uint32_t kAdaptiveMinPixels = 1u << 18;
-
-__device__ __forceinline__ float dense_width(int n_frames) { return n_frames >= 4 ? 5.0f : 10.0f; }
-
-__device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
-
-__device__ __forceinline__ bool dense_pixel(float d, float voxel, float fx, int n_frames)
-{
-    return valid_depth(d) && __fmul_rn(voxel, fx) >= __fmul_rn(dense_width(n_frames), d);
-}
-
-__device__ __forceinline__ bool dense_tile(uint32_t n_valid, uint32_t n_dense)
-{
-    return n_valid != 0 && 2 * n_dense >= n_valid;
-}
-
 // kSparseOnly: leave dense tiles to update_rows_kernel (adaptive mode).
 template <bool kFast, bool kSparseOnly>
 __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
@@ -491,6 +465,18 @@ cudaError_t launch_rows(const VolumeView& vol, const FrameBatch& fb, unsigned gr
     }
     update_rows_kernel<kFast, kAlways><<<grid, kRowThreads, kRowSmemBytes, stream>>>(vol, fb);
     return cudaGetLastError();
+}
+
+cudaError_t launch_update_listed(const VolumeView& vol, const FrameBatch& fb,
+                                 cudaStream_t stream)
+{
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(sms > 0 ? sms : 1) * kRowBlocksPerSM;
+    return vol.fast_div ? launch_rows<true, false>(vol, fb, grid, stream)
+                        : launch_rows<false, false>(vol, fb, grid, stream);
 }
 
 cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,

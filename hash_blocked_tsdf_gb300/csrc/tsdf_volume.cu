@@ -204,9 +204,19 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
             fb.frame[f].rgb = rgb ? rgb + 3 * (first + f) * px : nullptr;
             fb.frame[f].cam = cams[first + f];
         }
+        if (do_allocate && do_update && v->update_kind == TSDF_UPDATE_FUSED &&
+            2 * v->band_half + 1 <= 9) {
+            TSDF_CUDA(launch_integrate_fused(vol, fb, v->instrument, stream), "fused kernel");
+            continue;
+        }
         if (do_allocate)
             TSDF_CUDA(launch_allocate(vol, fb, v->instrument, stream), "allocate kernel");
-        if (do_update) TSDF_CUDA(launch_update(vol, fb, v->update_kind, stream), "update kernel");
+        if (do_update)
+            TSDF_CUDA(launch_update(vol, fb,
+                                    v->update_kind == TSDF_UPDATE_FUSED ? TSDF_UPDATE_ADAPTIVE
+                                                                        : v->update_kind,
+                                    stream),
+                      "update kernel");
     }
     return TSDF_OK;
 }
@@ -629,6 +639,7 @@ int tsdf_get_stats(tsdf_volume* vol, void* stream, tsdf_stats* out)
     out->probe_steps = c.probe_steps;
     out->probe_max = c.probe_max;
     for (int i = 0; i < TSDF_PROBE_HIST_BINS; ++i) out->probe_hist[i] = c.probe_hist[i];
+    out->publish_timeouts = c.publish_timeouts;
     return TSDF_OK;
 }
 
@@ -654,9 +665,10 @@ int tsdf_set_update_kernel(tsdf_volume* vol, int kind)
     int rc = check_volume(vol);
     if (rc) return rc;
     if (kind != TSDF_UPDATE_ADAPTIVE && kind != TSDF_UPDATE_PER_SAMPLE &&
-        kind != TSDF_UPDATE_PRE_REDUCED)
+        kind != TSDF_UPDATE_PRE_REDUCED && kind != TSDF_UPDATE_FUSED)
         return fail(TSDF_ERR_ARG, "update mode must be TSDF_UPDATE_ADAPTIVE, "
-                                  "TSDF_UPDATE_PER_SAMPLE or TSDF_UPDATE_PRE_REDUCED");
+                                  "TSDF_UPDATE_PER_SAMPLE, TSDF_UPDATE_PRE_REDUCED or "
+                                  "TSDF_UPDATE_FUSED");
     vol->update_kind = kind;
     return TSDF_OK;
 }

@@ -126,6 +126,8 @@ typedef struct tsdf_stats {
     uint64_t probe_steps;           /* slots examined by those probes */
     uint64_t probe_max;             /* longest probe */
     uint64_t probe_hist[TSDF_PROBE_HIST_BINS];  /* bin b: probes of length b + 1; last bin: longer */
+    uint64_t publish_timeouts;      /* fused integrate: waits for a published index that gave up
+                                       (their samples count as missed); 0 in normal operation */
 } tsdf_stats;
 
 /* Create a volume of `pool_capacity` blocks, voxel edge `voxel_size` metres,
@@ -328,10 +330,21 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
  *     memory which of its pixels reached each voxel (once or twice), then sums
  *     every touched voxel's contributions in pixel order and adds the five
  *     sums to the pool once, a row of 8 voxels at a time.
+ *   TSDF_UPDATE_FUSED: calls that both allocate and update (tsdf_integrate and
+ *     its batch forms) run one fused kernel instead of the two: each pixel's
+ *     band is walked once, its samples kept in registers while its block keys
+ *     go through the allocate kernel's insert rounds, and each key's pool
+ *     index then serves the update's additions.  A key claimed by another
+ *     thread of the launch is used once that thread has published its index
+ *     (the wait on PENDING, bounded: a wait that gives up is counted in
+ *     publish_timeouts and its samples in missed_contributions).  Bands longer
+ *     than 9 samples, and update-only calls, use the two-kernel path
+ *     (adaptive).
  * Returns TSDF_ERR_ARG for any other value. */
 #define TSDF_UPDATE_ADAPTIVE 0
 #define TSDF_UPDATE_PER_SAMPLE 1
 #define TSDF_UPDATE_PRE_REDUCED 2
+#define TSDF_UPDATE_FUSED 3
 int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 
 /* Message of the last failure on the calling thread ("" if none). */

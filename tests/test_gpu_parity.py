@@ -70,7 +70,7 @@ def test_smoke_entry(torch_cuda):
     __graft_entry__.smoke()
 
 
-KERNELS = ["adaptive", "pre_reduced", "per_sample"]
+KERNELS = ["adaptive", "pre_reduced", "per_sample", "fused"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -134,7 +134,8 @@ def test_pre_reduced_dense_close_range(torch_cuda, oracle_mod):
     print("dense close range:", rep)
 
 
-def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod, kernel):
     # one 640 x 480 frame, 3 cm voxels at fx = 525: the sphere's front
     # (depth < 1.575 m) sees a voxel edge 10+ pixels wide (the one-frame
     # rule) and is pre-reduced, the plane at 2.5 m is not; each tile is
@@ -144,10 +145,11 @@ def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod):
     d = frames.depth[0]
     near = (d > 0) & (0.03 * frames.K[0] >= 10 * d)
     assert 0.05 < near.mean() < 0.6, "the frame must hold both kinds of pixel"
-    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="adaptive")
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
 
 
-def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod, kernel):
     # eight orbit frames in one launch with 2 cm voxels: objects nearer than
     # 2.1 m see a voxel edge 5+ pixels wide (the several-frame rule)
     f = scenes.orbit_trajectory(n_frames=100, frames=(0, 8))
@@ -155,17 +157,33 @@ def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod):
     d = frames.depth
     near = (d > 0) & (0.02 * frames.K[0] >= 5 * d)
     assert 0.02 < near.sum() / (d > 0).sum() < 0.9, "the batch must hold both kinds of pixel"
-    _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel="adaptive")
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel=kernel)
 
 
-def test_adaptive_dense_frame(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+def test_adaptive_dense_frame(torch_cuda, oracle_mod, kernel):
     # 512 x 512 pixels of 1.5 mm against 2 cm voxels: every tile is dense and
     # hundreds of samples reach each voxel (summation tolerance)
     pose = np.eye(4)
     pose[:3, :3] = scenes.axis_angle([0.0, 1.0, 0.0], np.deg2rad(35.0))
     frames = _flat_frame("dense_frame", 512, 512, 600.0, 0.9037, pose, 0.02, 0.08, 4096, seed=6)
-    rep = _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel="adaptive")
+    rep = _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel=kernel)
     print("dense frame:", rep)
+
+
+def test_fused_room_walk_batch(torch_cuda, oracle_mod):
+    # allocate and update in one kernel, on two 8-frame launches of the room
+    # walk: exact blocks and weights, no wait for a published index gave up
+    frames = scenes.room_random_walk(n_frames=300, frames=(0, 16))
+    vol = _gpu_volume(torch_cuda, frames)
+    vol.set_update_kernel("fused")
+    _integrate_gpu(torch_cuda, frames, vol)
+    st = vol.stats()
+    o = _oracle(oracle_mod, frames)
+    parity.compare_volume(vol.export_blocks(), o.export(), strict=False)
+    parity.check_counters(st, o.counters())
+    assert st["publish_timeouts"] == 0
+    vol.close()
 
 
 def test_pre_reduced_row_table_overflow(torch_cuda, oracle_mod):
