@@ -64,6 +64,9 @@ def parse_args():
     ap.add_argument("--cpu-baseline-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="run the measurement matrix (one JSON line per cell) instead of the "
+                         "headline workload")
     ap.add_argument("--pool", type=int, default=0,
                     help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
@@ -324,6 +327,114 @@ def measure_extraction(torch, vol, blocks: int, hbm_peak: float) -> dict:
             "roofline": {"bound": "hbm", "achieved": alg / (best / 1e3) / 1e9, "peak": hbm_peak,
                          "unit": "GB/s", "frac": alg / (best / 1e3) / 1e9 / hbm_peak,
                          "bytes_alg": alg}}
+
+
+# ----------------------------------------------------------------------------
+# Measurement matrix (the pages time every arm over a matrix of cells, not one
+# scene: point count at fixed geometry, extent at fixed angular resolution,
+# hash load factor, scene shape; per stage p50/p95/p99 with the count, clocks
+# and temperature per cell, and a cell counts only if its block count equals
+# the reference's: every cell's parity with the oracle is asserted by
+# tests/test_gpu_sweep.py on the same cell definitions)
+# ----------------------------------------------------------------------------
+
+def _sweep_cell_specs():
+    """(axis, name, build) for every cell; build() renders its frames."""
+    from hash_blocked_tsdf_gb300 import scenes
+
+    def sp(name, W, H, fx, scale=1.0, voxel=0.01, table=0, pool=1 << 16):
+        def build():
+            d, c, pose, K = scenes.sphere_plane(
+                W, H, fx, fx, noise_sigma=0.002, invalid_frac=0.1, seed=7,
+                sphere_centre=(0.0, 0.0, 1.5 * scale), sphere_radius=0.5 * scale,
+                plane_z=2.5 * scale)
+            return scenes.Frames(name, d[None], c[None], pose[None], K, voxel, 4 * voxel, pool,
+                                 table, 7)
+        return name, build
+
+    specs = []
+    for W, H, fx in ((160, 120, 131.25), (320, 240, 262.5), (640, 480, 525.0),
+                     (1280, 960, 1050.0), (2560, 1920, 2100.0)):
+        specs.append(("points_at_fixed_geometry",) + sp(f"sphere_plane_{W}x{H}", W, H, fx))
+    for sc in (0.5, 1.0, 2.0, 4.0):
+        specs.append(("extent_at_fixed_angular_resolution",) +
+                     sp(f"sphere_plane_640x480_scale{sc}", 640, 480, 525.0, scale=sc,
+                        pool=1 << 17))
+    # the scale-2 scene holds 6,854 blocks: tables of 2^14 .. 2^17 slots give
+    # load factors 0.42 .. 0.05 (the pool, half the table, still holds them)
+    for t in (1 << 14, 1 << 15, 1 << 16, 1 << 17):
+        specs.append(("hash_load_factor",) +
+                     sp(f"sphere_plane_640x480_scale2_table{t}", 640, 480, 525.0, scale=2.0,
+                        table=t, pool=t // 2))
+    specs.append(("scene_shape", "tiny_sphere_plane_160x120", scenes.tiny_sphere_plane))
+    specs.append(("scene_shape", "vga_sphere_plane_640x480", scenes.vga_sphere_plane))
+    specs.append(("scene_shape", "orbit_100x640x480[0:8]",
+                  lambda: scenes.orbit_trajectory(n_frames=100, frames=(0, 8))))
+    specs.append(("scene_shape", "room_walk_300x1280x720[0:8]",
+                  lambda: scenes.room_random_walk(n_frames=300, frames=(0, 8))))
+    return specs
+
+
+def _sweep_cells():
+    return [(axis, build()) for axis, _, build in _sweep_cell_specs()]
+
+
+def run_sweep(args):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    dev = torch.cuda.current_device()
+    stream = torch.cuda.current_stream()
+    reps = 30
+    for axis, fr in _sweep_cells():
+        d = torch.from_numpy(fr.depth).cuda()
+        c = torch.from_numpy(fr.rgb).cuda()
+        vol = TsdfVolume(fr.pool_capacity, fr.voxel_size, fr.trunc, fr.table_capacity)
+        clocks = ClockSampler(dev)
+        clocks.start()
+        times = {"allocate": [], "update": [], "fused": []}
+        for r in range(reps + 3):
+            for mode in ("adaptive", "fused"):
+                vol.set_update_kernel(mode)
+                vol.reset()
+                ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+                ev[0].record(stream)
+                if mode == "fused":
+                    vol.integrate_batch(d, c, fr.K, fr.poses)
+                    ev[1].record(stream)
+                else:
+                    vol.allocate_batch(d, fr.K, fr.poses)
+                    ev[1].record(stream)
+                    vol.update_batch(d, c, fr.K, fr.poses)
+                ev[2].record(stream)
+                torch.cuda.synchronize()
+                if r >= 3:
+                    if mode == "fused":
+                        times["fused"].append(ev[0].elapsed_time(ev[1]))
+                    else:
+                        times["allocate"].append(ev[0].elapsed_time(ev[1]))
+                        times["update"].append(ev[1].elapsed_time(ev[2]))
+        clk = clocks.stop()
+        st = vol.stats()
+        blocks = vol.block_count()
+        table = vol.info["table_capacity"]
+        vol.close()
+        total = [a + u for a, u in zip(times["allocate"], times["update"])]
+        pts = st["valid_points"]
+        print(json.dumps({
+            "sweep": axis, "cell": fr.name, "frames": fr.n_frames,
+            "points": pts, "voxel_updates": st["voxel_updates"], "blocks": blocks,
+            "table_capacity": table, "load_factor": blocks / table,
+            "pool_exhausted": st["pool_exhausted"], "probe_overflow": st["probe_overflow"],
+            "parity": "tests/test_gpu_sweep.py (same cells)",
+            "allocate_ms": _percentiles(times["allocate"]),
+            "update_ms": _percentiles(times["update"]),
+            "allocate_update_ms": _percentiles(total),
+            "fused_ms": _percentiles(times["fused"]),
+            "points_per_s": pts / (float(np.median(total)) / 1e3),
+            "points_per_s_fused": pts / (float(np.median(times["fused"])) / 1e3),
+            "clocks": clk}), flush=True)
 
 
 def _percentiles(xs) -> dict:
@@ -844,6 +955,9 @@ def e2e_host(torch, vol, frames, args) -> dict:
 
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:
