@@ -3,9 +3,11 @@
 //
 // By default (adaptive) both kernels run on every batch and split the frame
 // by 16 x 16 pixel tiles: a tile whose pixels are small against the voxels
-// (at least half of them see a voxel edge 5 or more pixels wide) has its
-// samples crowd into few voxels and is pre-reduced by update_rows_kernel;
-// every other tile is left to update_kernel.
+// (the density rule in tsdf_device.cuh: at least half of them see a voxel
+// edge 5 or more pixels wide, 10 for launches of fewer than 4 frames) has its
+// samples crowd into few voxels; update_kernel lists it and the persistent
+// update_rows_kernel pre-reduces it; update_kernel adds every other tile's
+// samples itself.
 //
 // update_kernel (per sample): every thread walks one pixel's band, looks
 // up each passing sample's block (one lookup per new key, almost always a
@@ -14,8 +16,9 @@
 // 8 x 4 patch.  Where samples rarely share a voxel this is bound by the L2's
 // rate of reduction sectors, and nothing on chip would save much.
 //
-// update_rows_kernel (pre-reducing): a block of 192 threads owns an 8 x 8
-// pixel tile of one frame, three threads per pixel, each walking one third
+// update_rows_kernel (pre-reducing): a block of 192 threads takes an 8 x 8
+// pixel tile of one frame at a time (a listed 16 x 16 tile is four of them;
+// with TSDF_UPDATE_PRE_REDUCED every tile, one per block), three threads per pixel, each walking one third
 // of the pixel's truncation band (a warp covers an 8 x 4 pixel patch).  The
 // block keeps a shared table of the voxel rows its samples fall in (a row is
 // the 8 voxels of a block that share ly and lz: exactly one 32-byte sector of
