@@ -66,6 +66,7 @@ def load(mutant: int = 0):
         "oracle_keep_only": ([ctypes.c_void_p, i32p, ctypes.c_longlong], ctypes.c_int),
         "oracle_integrate": ([ctypes.c_void_p, f32p, f32p, ctypes.c_int, ctypes.c_int, f32p, f32p],
                              ctypes.c_int),
+        "oracle_set_occlusion": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
         "oracle_block_count": ([ctypes.c_void_p], ctypes.c_longlong),
         "oracle_kept_count": ([ctypes.c_void_p], ctypes.c_longlong),
         "oracle_counters": ([ctypes.c_void_p, _p(ctypes.c_ulonglong)], None),
@@ -126,6 +127,13 @@ class OracleVolume:
         c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 3))
         if self._lib.oracle_keep_only(self._h, _ptr(c, ctypes.c_int32), c.shape[0]) != 0:
             raise RuntimeError("keep_only must be called before the first integrate")
+
+    def set_occlusion(self, mode: str) -> None:
+        """Occlusion test of later integrations: "ray" (the ray pixel's depth,
+        the default) or "reproject" (the depth where the voxel centre
+        projects)."""
+        if self._lib.oracle_set_occlusion(self._h, {"ray": 0, "reproject": 1}[mode]) != 0:
+            raise ValueError(mode)
 
     def integrate(self, depth, rgb, K, pose) -> None:
         depth = np.ascontiguousarray(depth, dtype=np.float32)

@@ -31,6 +31,12 @@
  *   - projective signed distance at the voxel centre: sdf = d - z_c, where z_c
  *     is the camera-frame depth of the centre and d the pixel's depth;
  *   - occlusion test: z_c > 0 and sdf >= -trunc;
+ *   - alternative occlusion test (selected per volume): the voxel centre is
+ *     projected into the frame and tested against the depth of the nearest
+ *     pixel, floor(u + 1/2), floor(v + 1/2); the sample passes when that
+ *     pixel lies inside the image with a valid depth d' and d' - z_c >=
+ *     -trunc; it then adds min(1, (d' - z_c) / trunc) and that pixel's
+ *     colour (the walk and its voxels are unchanged);
  *   - value added: tsdf = min(1, sdf / trunc), weight 1, the pixel's colour;
  *   - voxel order inside a block: x fastest, j = lx + 8 ly + 64 lz;
  *   - block coordinates must lie in [-2^20, 2^20 - 1] on every axis (the
@@ -200,6 +206,61 @@ SampleStatus band_sample(const Camera& cam, float voxel, float trunc, float d,
     return SAMPLE_PASS;
 }
 
+/* The alternative occlusion test, by reprojection.  The centre of the
+ * sample's voxel, in camera coordinates c = R^T (centre - t), is projected
+ * through the pinhole, u = fx (c_x / c_z) + cx, v = fy (c_y / c_z) + cy, and
+ * rounded to the nearest pixel centre.  The sample passes when the centre is
+ * in front of the camera, the pixel lies inside the image and holds a valid
+ * depth d', and the centre is no more than one truncation distance behind
+ * it; the value is then min(1, (d' - c_z) / trunc) and *pix is the pixel
+ * whose colour the sample adds.  `d_ray` is the depth of the pixel whose ray
+ * selected the voxel; the test itself does not use it. */
+SampleStatus reprojected_sample(const Camera& cam, float voxel, float trunc, const float* depth,
+                                int W, int H, float d_ray, Sample* s, long long* pix)
+{
+    (void)d_ray;
+    float cxw = ((float)s->ix + 0.5f) * voxel - cam.t[0];
+    float cyw = ((float)s->iy + 0.5f) * voxel - cam.t[1];
+    float czw = ((float)s->iz + 0.5f) * voxel - cam.t[2];
+    // c = R^T (centre - t): component k is column k of R dotted with the centre
+#if ORACLE_MUTANT == 22
+    float x = (cam.R[0][0] * cxw + cam.R[0][1] * cyw) + cam.R[0][2] * czw;  // planted: R, not R^T
+    float y = (cam.R[1][0] * cxw + cam.R[1][1] * cyw) + cam.R[1][2] * czw;
+#else
+    float x = (cam.R[0][0] * cxw + cam.R[1][0] * cyw) + cam.R[2][0] * czw;
+    float y = (cam.R[0][1] * cxw + cam.R[1][1] * cyw) + cam.R[2][1] * czw;
+#endif
+    float z = (cam.R[0][2] * cxw + cam.R[1][2] * cyw) + cam.R[2][2] * czw;
+    if (!(z > 0.0f)) return SAMPLE_OCCLUDED;
+#if ORACLE_MUTANT == 20
+    float u = cam.fx * (y / z) + cam.cx;          // planted: x and y swapped
+    float v = cam.fy * (x / z) + cam.cy;
+#else
+    float u = cam.fx * (x / z) + cam.cx;
+    float v = cam.fy * (y / z) + cam.cy;
+#endif
+    // nearest pixel centre: floor(u + 1/2), inside [0, W) x [0, H)
+#if ORACLE_MUTANT == 19
+    float uh = u, vh = v;                          // planted: rounds down, not to nearest
+#else
+    float uh = u + 0.5f, vh = v + 0.5f;
+#endif
+    if (!(uh >= 0.0f && uh < (float)W && vh >= 0.0f && vh < (float)H)) return SAMPLE_OCCLUDED;
+    long long pu = (long long)std::floor(uh), pv = (long long)std::floor(vh);
+    long long p = pv * W + pu;
+#if ORACLE_MUTANT == 21
+    float d = d_ray;                               // planted: the ray pixel's depth
+#else
+    float d = depth[p];
+#endif
+    if (!(std::isfinite(d) && d > 0.0f)) return SAMPLE_OCCLUDED;
+    float sdf = d - z;
+    if (!(sdf >= -trunc)) return SAMPLE_OCCLUDED;
+    s->tsdf = std::fmin(1.0f, sdf / trunc);
+    *pix = p;
+    return SAMPLE_PASS;
+}
+
 /* Walk the truncation band of pixel (u, v) with depth d, calling
  * visit(status, sample) once per band sample.  Returns false (and visits
  * nothing) for an invalid pixel. */
@@ -239,6 +300,7 @@ struct Volume {
     float trunc;
     int band_half;           // k: samples at offsets -k..k voxels
     long long block_limit;   // < 0: no pool limit
+    bool reproject = false;  // occlusion test by reprojection instead of the ray's depth
 
     bool keep_all = true;    // false: sums are kept only for blocks in `keep`
     std::unordered_set<BlockCoord, BlockCoordHash> keep;
@@ -337,11 +399,15 @@ int oracle_integrate(void* h, const float* depth, const float* rgb, int W, int H
         for (int px = 0; px < W; ++px) {
             float d = depth[(size_t)py * W + px];
             walk_pixel(cam, v->voxel, v->trunc, v->band_half, px, py, d,
-                       [&](SampleStatus st, const Sample& s) {
+                       [&](SampleStatus st, const Sample& s0) {
                 if (st == SAMPLE_OUT_OF_RANGE) {
                     v->out_of_range_samples++;
                     return;
                 }
+                Sample s = s0;
+                long long pix = 0;
+                if (v->reproject) st = reprojected_sample(cam, v->voxel, v->trunc, depth, W, H, d,
+                                                          &s, &pix);
                 bool allocate = (st == SAMPLE_PASS);
 #if ORACLE_MUTANT == 12
                 allocate = true;                   // planted: allocate ignores occlusion
@@ -375,7 +441,20 @@ int oracle_integrate(void* h, const float* depth, const float* rgb, int W, int H
             std::swap(cr, cb);                     // planted: red and blue swapped
 #endif
             bool valid = walk_pixel(cam, v->voxel, v->trunc, v->band_half, px, py, d,
-                                    [&](SampleStatus st, const Sample& s) {
+                                    [&](SampleStatus st, const Sample& s0) {
+                Sample s = s0;
+                float sr = cr, sg = cg, sb = cb;
+                if (v->reproject && st != SAMPLE_OUT_OF_RANGE) {
+                    long long q = 0;
+                    st = reprojected_sample(cam, v->voxel, v->trunc, depth, W, H, d, &s, &q);
+#if ORACLE_MUTANT != 23
+                    if (st == SAMPLE_PASS) {       // the colour of the pixel tested against
+                        sr = rgb[3 * q + 0];
+                        sg = rgb[3 * q + 1];
+                        sb = rgb[3 * q + 2];
+                    }
+#endif                                             // (planted 23: the ray pixel's colour)
+                }
                 if (st != SAMPLE_PASS) return;
                 v->passing_samples++;
                 BlockCoord b = block_of(s);
@@ -399,13 +478,22 @@ int oracle_integrate(void* h, const float* depth, const float* rgb, int W, int H
 #else
                 sums->weight[j] += 1.0;
 #endif
-                sums->r[j] += (double)cr;
-                sums->g[j] += (double)cg;
-                sums->b[j] += (double)cb;
+                sums->r[j] += (double)sr;
+                sums->g[j] += (double)sg;
+                sums->b[j] += (double)sb;
             });
             if (valid) v->valid_points++;
         }
     }
+    return 0;
+}
+
+/* Occlusion test of later integrations: 0 = the ray pixel's depth (default),
+ * 1 = reprojection of the voxel centre.  Returns -1 for any other mode. */
+int oracle_set_occlusion(void* h, int mode)
+{
+    if (mode != 0 && mode != 1) return -1;
+    static_cast<Volume*>(h)->reproject = mode == 1;
     return 0;
 }
 
