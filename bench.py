@@ -71,6 +71,9 @@ def parse_args():
                     help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
                     default="adaptive", help="how the library's update reaches the pool")
+    ap.add_argument("--occlusion", choices=["ray", "reproject"], default="ray",
+                    help="occlusion test: the ray pixel's depth (default) or the depth where "
+                         "the voxel centre projects")
     return ap.parse_args()
 
 
@@ -448,6 +451,8 @@ def _update_kernels(args, frames, n_frames: int) -> int:
     and the pre-reducing kernel when the launch holds 2^18 pixels or more;
     the fused mode runs one kernel for both stages (counted here, with the
     allocate counted as none)."""
+    if getattr(args, "occlusion", "ray") == "reproject":
+        return 1                 # per-sample update, allocate and update as two kernels
     if args.update_kernel == "fused":
         return 0
     if args.update_kernel == "adaptive" and frames.width * frames.height * n_frames >= 1 << 18:
@@ -549,6 +554,7 @@ def run_ours(args):
     vol = TsdfVolume(frames.pool_capacity, frames.voxel_size, frames.trunc,
                      frames.table_capacity)
     vol.set_update_kernel(args.update_kernel)
+    vol.set_occlusion(args.occlusion)
     h = vol.handle
     lib = binding.load_library()
     K = np.ascontiguousarray(frames.K, dtype=np.float32)
@@ -563,7 +569,7 @@ def run_ours(args):
     group = args.group or vol.info["max_frames_per_launch"]
     groups = [(a, min(n, a + group)) for a in range(0, n, group)]
 
-    fused = args.update_kernel == "fused"
+    fused = args.update_kernel == "fused" and args.occlusion == "ray"
 
     def one_fused_step():
         rc = lib.tsdf_reset(h, sptr)
@@ -663,9 +669,14 @@ def run_ours(args):
     upd_kernel = {"per_sample": "update_kernel", "pre_reduced": "update_rows_kernel",
                   "adaptive": "update_kernel+update_rows_kernel",
                   "fused": "integrate_fused_kernel"}[args.update_kernel]
-    prof_upd = _profile_record(f"update_{args.update_kernel}_room_walk_1280x720.md",
+    if args.occlusion == "reproject":
+        upd_kernel = "update_kernel (reprojection test)"
+    mode = args.update_kernel if args.occlusion == "ray" else "reproject"
+    prof_upd = _profile_record(f"update_{mode}_room_walk_1280x720.md",
                                ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
-    prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md",
+    prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md"
+                                 if args.occlusion == "ray" else
+                                 "allocate_kernel_reproject_room_walk_1280x720.md",
                                  ["tsdf_alloc.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     same_shape = (args.workload == "room_walk" and frames.width == 1280 and frames.height == 720
                   and group == 8)
@@ -736,6 +747,7 @@ def run_ours(args):
         "voxel_updates_per_s": upd_rate,
         "frames_per_launch": group,
         "update_kernel": args.update_kernel,
+        "occlusion": args.occlusion,
         "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
         "stages_note": ("fused: one kernel per group, booked as the update stage" if fused
                         else "allocate launch, then update launch(es), per group"),
@@ -789,6 +801,10 @@ def run_ours(args):
             "note": "tsdf_integrate_batch per group with TSDF_UPDATE_FUSED: one kernel "
                     "allocates and updates (dense tiles pre-reduced by a second)"}
         vol.set_update_kernel(args.update_kernel)
+    if not fused and args.occlusion == "ray":
+        result["variant_reproject"] = variant_reproject(
+            torch, vol, frames, d_dev, c_dev, groups, one_step, stream, args, world,
+            hbm_peak, red_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v, u, sample, ovol, n_sample = oracle_sample(frames, args.cpu_baseline_seconds)
         result["cpu_baseline"] = {"value": v, "unit": "points/s", "cores": 1, "kind": "oracle",
@@ -799,6 +815,59 @@ def run_ours(args):
     vol.close()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def variant_reproject(torch, vol, frames, d_dev, c_dev, groups, one_step, stream, args, world,
+                      hbm_peak, red_peak) -> dict:
+    """The reprojection occlusion test on the same frames and protocol: the
+    same step (reset, then allocate and update per group), timed as a whole
+    and per launch; the update's rooflines with the same units as the
+    headline's (16 B per valid point and 40 B / 5 adds per distinct voxel of
+    each frame)."""
+    vol.set_occlusion("reproject")
+    for i in range(max(args.warmup, 1)):
+        one_step()
+        if i == 0:
+            torch.cuda.synchronize()
+            st = vol.stats()
+    distinct = census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups)
+    ng = len(groups)
+    torch.cuda.synchronize()
+    ta = torch.cuda.Event(enable_timing=True)
+    tb = torch.cuda.Event(enable_timing=True)
+    ta.record(stream)
+    evs = []
+    for _ in range(args.steps):
+        evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ng + 1)]
+        one_step(evk)
+        evs.append(evk)
+    tb.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(ta.elapsed_time(tb), world)
+    alloc = [e[2 * g].elapsed_time(e[2 * g + 1]) for e in evs for g in range(ng)]
+    upd = [e[2 * g + 1].elapsed_time(e[2 * g + 2]) for e in evs for g in range(ng)]
+    vol.set_occlusion(args.occlusion)
+    upd_avg = float(np.mean(upd))
+    pts = st["valid_points"]
+    u_frames = distinct["frame_by_frame"]
+    b_launch = (16.0 * pts + 40.0 * u_frames) / ng
+    adds = 5.0 * u_frames / ng
+    return {
+        "value": sum_over_ranks(pts * args.steps, world) / (ms / 1000.0), "unit": "points/s",
+        "ms_per_step": ms / args.steps,
+        "voxel_updates_per_step": st["voxel_updates"],
+        "stages_ms_per_launch": {"allocate": float(np.mean(alloc)), "update": upd_avg},
+        "stage_percentiles_ms": {"allocate": _percentiles(alloc), "update": _percentiles(upd)},
+        "roofline_update": {"bound": "hbm", "achieved": b_launch / (upd_avg / 1000.0) / 1e9,
+                            "peak": hbm_peak, "unit": "GB/s",
+                            "frac": b_launch / (upd_avg / 1000.0) / 1e9 / hbm_peak,
+                            "bytes_per_launch_alg": b_launch},
+        "roofline_update_l2_red": {"achieved": adds / (upd_avg / 1000.0), "peak": red_peak,
+                                   "unit": "float adds/s",
+                                   "frac": adds / (upd_avg / 1000.0) / red_peak},
+        "note": "TSDF_OCCLUSION_REPROJECT: allocate and per-sample update kernels, the depth "
+                "and colour read where each voxel centre projects",
+    }
 
 
 RED_MODES = ((0, "scalar_coalesced", 1), (1, "scalar_scattered", 1), (2, "v4_coalesced", 4),

@@ -87,6 +87,7 @@ SIGNATURES = {
     "tsdf_clear_stats": ([_VP, _VP], _I),
     "tsdf_set_instrumentation": ([_VP, _I], _I),
     "tsdf_set_update_kernel": ([_VP, _I], _I),
+    "tsdf_set_occlusion": ([_VP, _I], _I),
     "tsdf_last_error": ([], ctypes.c_char_p),
 }
 
@@ -405,6 +406,20 @@ def tsdf_set_update_kernel(h, kind) -> None:
     _check(load_library().tsdf_set_update_kernel(h, k), "tsdf_set_update_kernel")
 
 
+OCCLUSION_RAY = 0
+OCCLUSION_REPROJECT = 1
+OCCLUSION_TESTS = {"ray": OCCLUSION_RAY, "reproject": OCCLUSION_REPROJECT}
+
+
+def tsdf_set_occlusion(h, mode) -> None:
+    """Select the occlusion test of later launches: "ray" (default: the depth
+    of the pixel whose ray selected the voxel) or "reproject" (the depth of
+    the pixel nearest to the voxel centre's projection); or the header's
+    integer constants."""
+    m = OCCLUSION_TESTS[mode] if isinstance(mode, str) else int(mode)
+    _check(load_library().tsdf_set_occlusion(h, m), "tsdf_set_occlusion")
+
+
 # ----------------------------------------------------------------------------
 # Convenience wrapper
 # ----------------------------------------------------------------------------
@@ -481,3 +496,6 @@ class TsdfVolume:
 
     def set_update_kernel(self, kind):
         tsdf_set_update_kernel(self.handle, kind)
+
+    def set_occlusion(self, mode):
+        tsdf_set_occlusion(self.handle, mode)

@@ -106,6 +106,21 @@ __device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, 
 // Longest band for which a thread keeps its distinct keys in registers.
 constexpr int kShortBand = 9;
 
+// Whether the sample in voxel s passes the volume's occlusion test (the
+// allocate kernel needs only the decision, not the value).
+template <bool kFast, bool kReproject>
+__device__ __forceinline__ bool allocate_visible(const VolumeView& vol, const Camera& cam,
+                                                 const RayPoint& p, const float* depth,
+                                                 int width, int height, VoxelSample s)
+{
+    if (kReproject) {
+        size_t pix;
+        return reprojected_visible<kFast, false>(cam, vol.div, depth, width, height, s, pix);
+    }
+    float zc;
+    return ray_visible(cam, vol.div, p, s, zc);
+}
+
 // Block b of the grid covers 256 consecutive pixels (chunk b / n) of frame
 // b % n: the batch's frames are interleaved chunk by chunk.
 //
@@ -113,8 +128,11 @@ constexpr int kShortBand = 9;
 // whole band and keeps the distinct block keys of its passing samples in a
 // small register list; the warp then runs one insert round per list entry
 // (usually two or three) instead of one per band sample.  Longer bands insert
-// step by step.
-template <bool kInstrument, bool kFast, bool kShort>
+// step by step.  A sample whose block is the one its thread listed last is
+// not tested: whatever the test says, the list stays the same.  With
+// kReproject the occlusion test is the reprojection of the voxel centre
+// (reprojected_visible), as in the update it pairs with.
+template <bool kInstrument, bool kFast, bool kShort, bool kReproject>
 __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                                                            const __grid_constant__ FrameBatch fb)
 {
@@ -145,18 +163,21 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
             keys[j] = kEmptyKey;
             if (valid && j < steps) {
                 VoxelSample s;
-                const int status = band_sample<kFast, false>(cam, vol.div, p, j - vol.band_half, s);
-                if (status == kSamplePass) {
+                if (!band_voxel<kFast>(cam, vol.div, p, j - vol.band_half, s)) {
+                    ++out_of_range;
+                } else {
                     const unsigned long long key = block_key(s.ix, s.iy, s.iz);
-                    if (key != last) {          // newest key first; static indices only
+                    // a sample of the block listed last cannot change the
+                    // list, so its occlusion test is skipped
+                    if (key != last && allocate_visible<kFast, kReproject>(
+                                           vol, cam, p, depth, fb.width, fb.height, s)) {
+                        // newest key first; static indices only
 #pragma unroll
                         for (int m = kShortBand - 1; m > 0; --m) keys[m] = keys[m - 1];
                         keys[0] = key;
                         ++n_keys;
                         last = key;
                     }
-                } else if (status == kSampleOutOfRange) {
-                    ++out_of_range;
                 }
             }
         }
@@ -171,11 +192,15 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
             unsigned long long key = kEmptyKey;
             if (valid) {
                 VoxelSample s;
-                const int status = band_sample<kFast, false>(cam, vol.div, p, i, s);
-                if (status == kSamplePass)
-                    key = block_key(s.ix, s.iy, s.iz);
-                else if (status == kSampleOutOfRange)
+                if (!band_voxel<kFast>(cam, vol.div, p, i, s)) {
                     ++out_of_range;
+                } else {
+                    const unsigned long long k = block_key(s.ix, s.iy, s.iz);
+                    // (the block of the last passing sample needs no test)
+                    if (k == last || allocate_visible<kFast, kReproject>(vol, cam, p, depth,
+                                                                         fb.width, fb.height, s))
+                        key = k;
+                }
             }
             const bool fresh = key != kEmptyKey && key != last;
             if (key != kEmptyKey) last = key;
@@ -395,14 +420,26 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
 
 }  // namespace
 
+template <bool kInstrument, bool kFast, bool kReproject>
+void launch_allocate_r(const VolumeView& vol, const FrameBatch& fb, unsigned grid,
+                       cudaStream_t stream)
+{
+    if (2 * vol.band_half + 1 <= kShortBand)
+        allocate_kernel<kInstrument, kFast, true, kReproject><<<grid, kThreads, 0, stream>>>(vol,
+                                                                                           fb);
+    else
+        allocate_kernel<kInstrument, kFast, false, kReproject><<<grid, kThreads, 0, stream>>>(vol,
+                                                                                            fb);
+}
+
 template <bool kInstrument, bool kFast>
 void launch_allocate_t(const VolumeView& vol, const FrameBatch& fb, unsigned grid,
                        cudaStream_t stream)
 {
-    if (2 * vol.band_half + 1 <= kShortBand)
-        allocate_kernel<kInstrument, kFast, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+    if (vol.occlusion == TSDF_OCCLUSION_REPROJECT)
+        launch_allocate_r<kInstrument, kFast, true>(vol, fb, grid, stream);
     else
-        allocate_kernel<kInstrument, kFast, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+        launch_allocate_r<kInstrument, kFast, false>(vol, fb, grid, stream);
 }
 
 cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool instrument,
@@ -449,7 +486,9 @@ void launch_fused_t(const VolumeView& vol, const FrameBatch& fb, bool sparse_onl
 cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                                    cudaStream_t stream)
 {
-    if (2 * vol.band_half + 1 > kShortBand) return cudaErrorInvalidValue;
+    // (the fused kernel applies the ray-depth occlusion test only)
+    if (2 * vol.band_half + 1 > kShortBand || vol.occlusion != TSDF_OCCLUSION_RAY)
+        return cudaErrorInvalidValue;
     const unsigned tiles = (unsigned)(((fb.width + 15) / 16) * ((fb.height + 15) / 16));
     const unsigned grid = tiles * (unsigned)fb.n;
     const bool sparse_only =

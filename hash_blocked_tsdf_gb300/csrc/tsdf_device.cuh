@@ -49,6 +49,9 @@ __device__ __forceinline__ bool back_project(const Camera& c, int u, int v, floa
     return true;
 }
 
+// A pixel holds an observation when its depth is finite and positive.
+__device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
+
 // Division by a divisor y that is fixed for the whole volume (the voxel size
 // or the truncation distance), given r = RN(1 / y): Markstein's
 // reciprocal-and-correction scheme (P. Markstein, "Computation of elementary
@@ -111,16 +114,11 @@ __device__ __forceinline__ float truncated_sdf(const DivisorPair& dv, float d, f
     return fminf(1.0f, div_trunc<kFast>(__fsub_rn(d, zc), dv.trunc, dv.inv_trunc));
 }
 
-// Band sample `i` (offset i * voxel along the unit ray, i in -k..k): its
-// voxel and truncated signed distance at the voxel centre, or the reason it
-// is skipped.  The same function serves the allocate and the update kernels,
-// which is what makes their occlusion decisions identical; the allocate
-// kernel, which only needs the voxel, skips the final division.  Written
-// without early exits: every quantity is computed and the status is selected
-// at the end (out-of-range indices are clamped before the integer conversion
-// and never used).
-template <bool kFast, bool kWantTsdf = true>
-__device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
+// The voxel of band sample `i` (offset i * voxel along the unit ray, i in
+// -k..k), and whether its index lies in the packable range.  Out-of-range
+// indices are clamped before the integer conversion and never used.
+template <bool kFast>
+__device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
                                            const RayPoint& p, int i, VoxelSample& s)
 {
     const float voxel = dv.voxel;
@@ -144,13 +142,85 @@ __device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& d
     s.ix = (int)fminf(fmaxf(qx, kVoxelIndexMin), kVoxelIndexMax);
     s.iy = (int)fminf(fmaxf(qy, kVoxelIndexMin), kVoxelIndexMax);
     s.iz = (int)fminf(fmaxf(qz, kVoxelIndexMin), kVoxelIndexMax);
-    const float zc = centre_depth(c, voxel, s.ix, s.iy, s.iz);
-    const float sdf = __fsub_rn(p.d, zc);
-    // occlusion test: in front of the camera, and not more than one
-    // truncation distance behind the observed surface
-    const bool visible = zc > 0.0f && sdf >= -dv.trunc;
-    if (kWantTsdf) s.tsdf = truncated_sdf<kFast>(dv, p.d, zc);
+    return in_range;
+}
+
+// The occlusion test of the sample in voxel s against its own ray's depth:
+// the centre lies in front of the camera and not more than one truncation
+// distance behind the observed surface.  zc is the centre's camera depth.
+__device__ __forceinline__ bool ray_visible(const Camera& c, const DivisorPair& dv,
+                                            const RayPoint& p, const VoxelSample& s, float& zc)
+{
+    zc = centre_depth(c, dv.voxel, s.ix, s.iy, s.iz);
+    return zc > 0.0f && __fsub_rn(p.d, zc) >= -dv.trunc;
+}
+
+// Band sample `i`: its voxel and truncated signed distance at the voxel
+// centre, or the reason it is skipped.  The update kernels use it; the
+// allocate kernel, which only needs the voxel and the test, calls
+// band_voxel and ray_visible itself.  Written without early exits: every
+// quantity is computed and the status is selected at the end.
+template <bool kFast>
+__device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
+                                           const RayPoint& p, int i, VoxelSample& s)
+{
+    const bool in_range = band_voxel<kFast>(c, dv, p, i, s);
+    float zc;
+    const bool visible = ray_visible(c, dv, p, s, zc);
+    s.tsdf = truncated_sdf<kFast>(dv, p.d, zc);
     return !in_range ? kSampleOutOfRange : (visible ? kSamplePass : kSampleOccluded);
+}
+
+// The occlusion test by reprojection (selected per volume; the alternative
+// reading of the design section's occlusion test).  The centre of voxel s,
+// in camera coordinates c = R^T (centre - t), is projected through the
+// pinhole, u = fx (c_x / c_z) + cx, v = fy (c_y / c_z) + cy, and rounded to
+// the nearest pixel centre, floor(u + 1/2), floor(v + 1/2).  The sample
+// passes when the centre is in front of the camera, that pixel lies inside
+// the image and holds a valid depth d', and d' - c_z >= -trunc; then (with
+// kWantTsdf) s.tsdf = min(1, (d' - c_z) / trunc), and `pix` is the pixel
+// whose colour the sample adds.
+template <bool kFast, bool kWantTsdf>
+__device__ __forceinline__ bool reprojected_visible(const Camera& c, const DivisorPair& dv,
+                                                    const float* __restrict__ depth, int width,
+                                                    int height, VoxelSample& s, size_t& pix)
+{
+    const float voxel = dv.voxel;
+    const float cxr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.ix, 0.5f), voxel), c.tx);
+    const float cyr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iy, 0.5f), voxel), c.ty);
+    const float czr = __fsub_rn(__fmul_rn(__fadd_rn((float)s.iz, 0.5f), voxel), c.tz);
+    // component k of R^T (centre - t) is column k of R dotted with the centre
+    const float x = __fadd_rn(__fadd_rn(__fmul_rn(c.r00, cxr), __fmul_rn(c.r10, cyr)),
+                              __fmul_rn(c.r20, czr));
+    const float y = __fadd_rn(__fadd_rn(__fmul_rn(c.r01, cxr), __fmul_rn(c.r11, cyr)),
+                              __fmul_rn(c.r21, czr));
+    const float z = __fadd_rn(__fadd_rn(__fmul_rn(c.r02, cxr), __fmul_rn(c.r12, cyr)),
+                              __fmul_rn(c.r22, czr));
+    if (!(z > 0.0f)) return false;
+    const float uh = __fadd_rn(__fadd_rn(__fmul_rn(c.fx, __fdiv_rn(x, z)), c.cx), 0.5f);
+    const float vh = __fadd_rn(__fadd_rn(__fmul_rn(c.fy, __fdiv_rn(y, z)), c.cy), 0.5f);
+    // (NaN fails every comparison)
+    if (!(uh >= 0.0f && uh < (float)width && vh >= 0.0f && vh < (float)height)) return false;
+    pix = (size_t)floorf(vh) * (size_t)width + (size_t)floorf(uh);
+    const float d = __ldg(depth + pix);
+    if (!valid_depth(d)) return false;
+    if (!(__fsub_rn(d, z) >= -dv.trunc)) return false;
+    if (kWantTsdf) s.tsdf = truncated_sdf<kFast>(dv, d, z);
+    return true;
+}
+
+// Band sample `i` under the reprojection test: its voxel (the walk is the
+// ray test's) and, when it passes, its value and the pixel of its colour.
+template <bool kFast>
+__device__ __forceinline__ int band_sample_reprojected(const Camera& c, const DivisorPair& dv,
+                                                       const RayPoint& p, int i,
+                                                       const float* __restrict__ depth,
+                                                       int width, int height, VoxelSample& s,
+                                                       size_t& pix)
+{
+    if (!band_voxel<kFast>(c, dv, p, i, s)) return kSampleOutOfRange;
+    return reprojected_visible<kFast, true>(c, dv, depth, width, height, s, pix)
+               ? kSamplePass : kSampleOccluded;
 }
 
 // Packed key: block coordinate (voxel index >> 3, an arithmetic shift, i.e.
@@ -273,8 +343,6 @@ __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 constexpr uint32_t kAdaptiveMinPixels = 1u << 18;
 
 __device__ __forceinline__ float dense_width(int n_frames) { return n_frames >= 4 ? 5.0f : 10.0f; }
-
-__device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
 
 __device__ __forceinline__ bool dense_pixel(float d, float voxel, float fx, int n_frames)
 {

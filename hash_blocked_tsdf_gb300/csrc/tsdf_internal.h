@@ -68,6 +68,7 @@ struct VolumeView {
     DivisorPair div;            // voxel size and truncation, with reciprocals
     bool fast_div;              // the fixed-divisor division was verified exact
     int band_half;              // samples at offsets -band_half .. band_half voxels
+    int occlusion;              // TSDF_OCCLUSION_RAY or TSDF_OCCLUSION_REPROJECT
     // Adaptive update: the dense 16 x 16 pixel tiles of the current update
     // launch, (frame << 24 | tile), listed by the per-sample kernel for the
     // pre-reducing one; dense_next is the latter's work counter.
@@ -111,6 +112,7 @@ cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, 
 cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,
                                    bool instrument, cudaStream_t stream);
 // kind: TSDF_UPDATE_ADAPTIVE, TSDF_UPDATE_PER_SAMPLE or TSDF_UPDATE_PRE_REDUCED.
+// With the reprojection occlusion test every kind runs the per-sample kernel.
 cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
                           cudaStream_t stream);
 // Count the float32 x (all 2^32 bit patterns) for which the walk's use of the

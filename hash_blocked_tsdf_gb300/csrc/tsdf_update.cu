@@ -53,7 +53,9 @@ __device__ __forceinline__ void red_add(float* addr, float v)
 }
 
 // kSparseOnly: leave dense tiles to update_rows_kernel (adaptive mode).
-template <bool kFast, bool kSparseOnly>
+// kReproject: the occlusion test by reprojection of the voxel centre; each
+// passing sample adds the colour of the pixel it was tested against.
+template <bool kFast, bool kSparseOnly, bool kReproject>
 __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                                                          const __grid_constant__ FrameBatch fb)
 {
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
         valid = back_project(cam, u, v, depth, p);
-        if (valid) {
+        if (valid && !kReproject) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);
             cg = __ldg(rgb + 3 * pix + 1);
@@ -106,7 +108,18 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
         uint32_t idx = kIndexFailed;
         for (int i = -vol.band_half; i <= vol.band_half; ++i) {
             VoxelSample s;
-            if (band_sample<kFast>(cam, vol.div, p, i, s) != kSamplePass) continue;
+            if (kReproject) {
+                size_t q;
+                if (band_sample_reprojected<kFast>(cam, vol.div, p, i, fb.frame[f].depth,
+                                                   fb.width, fb.height, s, q) != kSamplePass)
+                    continue;
+                const float* rgb = fb.frame[f].rgb;
+                cr = __ldg(rgb + 3 * q);
+                cg = __ldg(rgb + 3 * q + 1);
+                cb = __ldg(rgb + 3 * q + 2);
+            } else if (band_sample<kFast>(cam, vol.div, p, i, s) != kSamplePass) {
+                continue;
+            }
             const unsigned long long key = block_key(s.ix, s.iy, s.iz);
             if (key != last) {
                 idx = lookup(vol.table, vol.table_mask, key);
@@ -490,17 +503,24 @@ cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
     if (kind == TSDF_UPDATE_ADAPTIVE &&
         (uint64_t)fb.width * (uint64_t)fb.height * (uint64_t)fb.n < kAdaptiveMinPixels)
         kind = TSDF_UPDATE_PER_SAMPLE;
+    // the pre-reducing kernel recomputes a sample's value from its ray pixel's
+    // depth, which the reprojection test does not use
+    const bool reproject = vol.occlusion == TSDF_OCCLUSION_REPROJECT;
+    if (reproject) kind = TSDF_UPDATE_PER_SAMPLE;
     if (kind != TSDF_UPDATE_PRE_REDUCED) {
         const unsigned tiles = (unsigned)(((fb.width + kTileW - 1) / kTileW) *
                                           ((fb.height + kTileH - 1) / kTileH));
         const unsigned grid = tiles * (unsigned)fb.n;
         const bool sparse_only = kind == TSDF_UPDATE_ADAPTIVE;
-        if (vol.fast_div) {
-            if (sparse_only) update_kernel<true, true><<<grid, kThreads, 0, stream>>>(vol, fb);
-            else update_kernel<true, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+        if (reproject) {
+            if (vol.fast_div) update_kernel<true, false, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+            else update_kernel<false, false, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+        } else if (vol.fast_div) {
+            if (sparse_only) update_kernel<true, true, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+            else update_kernel<true, false, false><<<grid, kThreads, 0, stream>>>(vol, fb);
         } else {
-            if (sparse_only) update_kernel<false, true><<<grid, kThreads, 0, stream>>>(vol, fb);
-            else update_kernel<false, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+            if (sparse_only) update_kernel<false, true, false><<<grid, kThreads, 0, stream>>>(vol, fb);
+            else update_kernel<false, false, false><<<grid, kThreads, 0, stream>>>(vol, fb);
         }
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess || kind == TSDF_UPDATE_PER_SAMPLE) return e;

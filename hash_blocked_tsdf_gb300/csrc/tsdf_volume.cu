@@ -39,6 +39,7 @@ struct tsdf_volume {
     int band_half = 0;
     bool instrument = false;
     int update_kind = TSDF_UPDATE_ADAPTIVE;
+    int occlusion = TSDF_OCCLUSION_RAY;
     DivisorPair div = {};
     bool fast_div = false;          // the fixed-divisor division was verified for both divisors
 
@@ -98,6 +99,7 @@ VolumeView view_of(const tsdf_volume* v)
     w.counters = &v->state->counters;
     w.div = v->div;
     w.fast_div = v->fast_div;
+    w.occlusion = v->occlusion;
     w.band_half = v->band_half;
     w.dense_list = v->dense_list;
     w.dense_capacity = kDenseListCapacity;
@@ -205,7 +207,7 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
             fb.frame[f].cam = cams[first + f];
         }
         if (do_allocate && do_update && v->update_kind == TSDF_UPDATE_FUSED &&
-            2 * v->band_half + 1 <= 9) {
+            v->occlusion == TSDF_OCCLUSION_RAY && 2 * v->band_half + 1 <= 9) {
             TSDF_CUDA(launch_integrate_fused(vol, fb, v->instrument, stream), "fused kernel");
             continue;
         }
@@ -670,6 +672,17 @@ int tsdf_set_update_kernel(tsdf_volume* vol, int kind)
                                   "TSDF_UPDATE_PER_SAMPLE, TSDF_UPDATE_PRE_REDUCED or "
                                   "TSDF_UPDATE_FUSED");
     vol->update_kind = kind;
+    return TSDF_OK;
+}
+
+int tsdf_set_occlusion(tsdf_volume* vol, int mode)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (mode != TSDF_OCCLUSION_RAY && mode != TSDF_OCCLUSION_REPROJECT)
+        return fail(TSDF_ERR_ARG, "occlusion must be TSDF_OCCLUSION_RAY or "
+                                  "TSDF_OCCLUSION_REPROJECT");
+    vol->occlusion = mode;
     return TSDF_OK;
 }
 

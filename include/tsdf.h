@@ -347,6 +347,28 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
 #define TSDF_UPDATE_FUSED 3
 int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 
+/* The occlusion test of later allocate and update launches.  The design
+ * section (occlusion) fixes that both passes apply the same test but not its
+ * formula; two readings are offered, and both passes always use the same one:
+ *   TSDF_OCCLUSION_RAY (the default): the test above, against the depth of
+ *     the pixel whose ray selected the voxel.
+ *   TSDF_OCCLUSION_REPROJECT: the centre of the sample's voxel, in camera
+ *     coordinates c = R^T (centre - t), is projected through the pinhole,
+ *     u = fx (c_x / c_z) + cx, v = fy (c_y / c_z) + cy (IEEE float32, one
+ *     rounding per operation), and rounded to the nearest pixel centre
+ *     (floor(u + 1/2), floor(v + 1/2)).  The sample passes iff c_z > 0, that
+ *     pixel lies inside the image with a valid depth d', and
+ *     d' - c_z >= -trunc; it then adds (min(1, (d' - c_z) / trunc), 1, and
+ *     that pixel's colour).  The band walk and its voxels are unchanged.
+ *     Updates under this test always add their samples one by one
+ *     (TSDF_UPDATE_PER_SAMPLE) whatever the update mode, and allocate and
+ *     update run as two kernels.
+ * Switching between launches is allowed; each sample is added under the test
+ * in force when its update ran.  Returns TSDF_ERR_ARG for any other value. */
+#define TSDF_OCCLUSION_RAY 0
+#define TSDF_OCCLUSION_REPROJECT 1
+int tsdf_set_occlusion(tsdf_volume* vol, int mode);
+
 /* Message of the last failure on the calling thread ("" if none). */
 const char* tsdf_last_error(void);
 

@@ -89,26 +89,28 @@ def check_counters(stats: dict, oracle_counters: dict):
 # ----------------------------------------------------------------------------
 
 def _oracle_chunk(args):
-    scene_name, scene_kw, start, stop, keep = args
+    scene_name, scene_kw, start, stop, keep, occlusion = args
     os.environ["OMP_NUM_THREADS"] = "1"
     import oracle
     from hash_blocked_tsdf_gb300 import scenes
     frames = getattr(scenes, scene_name)(frames=(start, stop), **scene_kw)
     o = oracle.OracleVolume(frames.voxel_size, frames.trunc)
+    o.set_occlusion(occlusion)
     if keep is not None:
         o.keep_only(keep)
     o.integrate_frames(frames)
     return o.coords(), o.counters(), o.export()
 
 
-def parallel_oracle(scene_name: str, scene_kw: dict, n_frames: int, keep, workers: int):
+def parallel_oracle(scene_name: str, scene_kw: dict, n_frames: int, keep, workers: int,
+                    occlusion: str = "ray"):
     """Union of per-chunk oracle results: every block coordinate, summed
     counters, and summed kept-block sums (sums commute, so the union over
     frame chunks equals one sequential run up to double rounding)."""
     import multiprocessing as mp
     bounds = np.linspace(0, n_frames, workers + 1).round().astype(int)
-    jobs = [(scene_name, scene_kw, int(a), int(b), keep) for a, b in zip(bounds[:-1], bounds[1:])
-            if b > a]
+    jobs = [(scene_name, scene_kw, int(a), int(b), keep, occlusion)
+            for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
     ctx = mp.get_context("spawn")
     with ctx.Pool(len(jobs)) as pool:
         results = pool.map(_oracle_chunk, jobs)

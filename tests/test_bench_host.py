@@ -27,6 +27,10 @@ def test_update_kernel_count_per_launch():
     assert bench._update_kernels(adaptive, small, 8) == 1        # 153,600 px < 2^18
     assert bench._update_kernels(adaptive, small, 16) == 2
     assert bench._update_kernels(per_sample, big, 8) == 1
+    # the reprojection test always runs the per-sample update as its own kernel
+    for kind in ("adaptive", "pre_reduced", "fused"):
+        reproject = types.SimpleNamespace(update_kernel=kind, occlusion="reproject")
+        assert bench._update_kernels(reproject, big, 8) == 1
 
 
 class _FakeVolume:
