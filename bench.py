@@ -964,8 +964,10 @@ def census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups) -> dict:
     from hash_blocked_tsdf_gb300 import binding
     ptrs = binding.tsdf_get_pool(vol.handle)
     cap = vol.info["pool_capacity"]
-    weight = _as_tensor(torch, ptrs["weight"], cap * 512)
-    prev = torch.empty_like(weight)
+    # the weight sums: every 4th float of the interleaved voxel records
+    weight = _as_tensor(torch, ptrs["tsdf"], cap * 512 * ptrs["stride"]).view(
+        -1, ptrs["stride"])[:, 1]
+    prev = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
     out = {}
     for name, grp in (("total", groups), ("frame_by_frame",
                                           [(f, f + 1) for f in range(frames.n_frames)])):

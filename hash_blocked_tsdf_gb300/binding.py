@@ -44,7 +44,7 @@ class tsdf_info(ctypes.Structure):
 class tsdf_pool_view(ctypes.Structure):
     _fields_ = [("tsdf", ctypes.c_void_p), ("weight", ctypes.c_void_p), ("r", ctypes.c_void_p),
                 ("g", ctypes.c_void_p), ("b", ctypes.c_void_p),
-                ("pool_capacity", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+                ("pool_capacity", ctypes.c_uint32), ("stride", ctypes.c_uint32)]
 
 
 class tsdf_stats(ctypes.Structure):
@@ -177,11 +177,14 @@ def tsdf_get_info(h) -> dict:
 
 
 def tsdf_get_pool(h) -> dict:
-    """Device pointers (ints) of the five pool arrays, float32 [capacity][512]."""
+    """Device pointers (ints) of the five pool sums.  Voxel v = 512 b + j
+    (block b, voxel j) has its tsdf, weight, r and g sums at float index
+    stride * v from the respective pointer (interleaved records, stride 4)
+    and its blue sum at float index v from b."""
     v = tsdf_pool_view()
     _check(load_library().tsdf_get_pool(h, ctypes.byref(v)), "tsdf_get_pool")
     return {"tsdf": v.tsdf, "weight": v.weight, "r": v.r, "g": v.g, "b": v.b,
-            "pool_capacity": v.pool_capacity}
+            "pool_capacity": v.pool_capacity, "stride": v.stride}
 
 
 tsdf_pool_arrays = tsdf_get_pool

@@ -248,11 +248,6 @@ __global__ void __launch_bounds__(kThreads) allocate_blocks_kernel(VolumeView vo
 // Waits for a published index are bounded by this many polls (~64 ns apart).
 constexpr uint32_t kPublishSpinLimit = 1u << 20;
 
-__device__ __forceinline__ void red_add(float* addr, float v)
-{
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 // The pool index published in `slot`.  The lane that claimed the slot takes
 // the index from the pool counter and stores it in the same insert step,
 // waiting on nothing, so this wait is short; it is bounded all the same: a
@@ -382,12 +377,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
 #pragma unroll
                 for (int j = 0; j < kShortBand; ++j) {
                     if (m & (1u << j)) {
-                        const size_t e = base + (size_t)lv[j];
-                        red_add(vol.tsdf + e, tv[j]);
-                        red_add(vol.weight + e, 1.0f);
-                        red_add(vol.red + e, cr);
-                        red_add(vol.green + e, cg);
-                        red_add(vol.blue + e, cb);
+                        add_to_voxel(vol, base + (size_t)lv[j], tv[j], 1.0f, cr, cg, cb);
                         ++updates;
                     }
                 }

@@ -328,6 +328,26 @@ __device__ __forceinline__ uint32_t lookup(const Entry* __restrict__ table, uint
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
+// The tsdf and weight sums of voxel e (the first half of its record).
+__device__ __forceinline__ float2 tsdf_and_weight(const VolumeView& vol, size_t e)
+{
+    return __ldg(reinterpret_cast<const float2*>(vol.voxel4 + e));
+}
+
+// Add one observation's terms to voxel e of the pool: (tsdf, weight, red,
+// green) with one 4-wide float reduction into the voxel's 16-byte record,
+// blue with one scalar reduction.  L2 executes a reduction request at about
+// the same rate whether it carries one float or four, so this takes two
+// requests where five separate arrays took five.
+__device__ __forceinline__ void add_to_voxel(const VolumeView& vol, size_t e, float tsdf,
+                                             float weight, float r, float g, float b)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(vol.voxel4 + e),
+                 "f"(tsdf), "f"(weight), "f"(r), "f"(g)
+                 : "memory");
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(vol.blue + e), "f"(b) : "memory");
+}
+
 // Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
 // at least half of its valid pixels (finite depth > 0) see a voxel edge at
 // least w pixels wide (voxel * fx >= w * depth): there samples crowd into few

@@ -173,10 +173,9 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
     const int t = threadIdx.x;
     const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
     for (int j = t; j < kBlockVoxels; j += kThreads) {
-        const size_t e = (size_t)b * kBlockVoxels + j;
-        const float w = vol.weight[e];
-        s_seen[j] = w > 0.0f ? 1 : 0;
-        s_mean[j] = w > 0.0f ? __fdiv_rn(vol.tsdf[e], w) : 0.0f;
+        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + j);
+        s_seen[j] = tw.y > 0.0f ? 1 : 0;
+        s_mean[j] = tw.y > 0.0f ? __fdiv_rn(tw.x, tw.y) : 0.0f;
     }
     if (t < 8) {
         uint32_t idx = kIndexFailed;
@@ -224,10 +223,9 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
                 const uint32_t nb = s_nb[d];
                 seen = false;
                 if (nb < vol.pool_capacity) {
-                    const size_t e = (size_t)nb * kBlockVoxels + jj;
-                    const float w = vol.weight[e];
-                    seen = w > 0.0f;
-                    if (seen) v = __fdiv_rn(vol.tsdf[e], w);
+                    const float2 tw = tsdf_and_weight(vol, (size_t)nb * kBlockVoxels + jj);
+                    seen = tw.y > 0.0f;
+                    if (seen) v = __fdiv_rn(tw.x, tw.y);
                 }
             }
             ok[c] = ok[c] && seen;
@@ -273,7 +271,7 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
 }
 
 // Block b of the input: find its pool index (inserted just before) and copy
-// its five arrays there.
+// its five sums there.
 __global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const int32_t* coords,
                                                          const float* src)
 {
@@ -291,11 +289,14 @@ __global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const 
     __syncthreads();
     const uint32_t idx = s_idx;
     if (idx >= vol.pool_capacity) return;           // refused (pool full) or out of range
-    float* dst[5] = {vol.tsdf, vol.weight, vol.red, vol.green, vol.blue};
-    for (int a = 0; a < 5; ++a)
-        for (int j = threadIdx.x; j < kBlockVoxels; j += kThreads)
-            dst[a][(size_t)idx * kBlockVoxels + j] =
-                src[((size_t)a * n + b) * kBlockVoxels + j];
+    for (int j = threadIdx.x; j < kBlockVoxels; j += kThreads) {
+        const size_t e = (size_t)idx * kBlockVoxels + j;
+        float v[5];
+#pragma unroll
+        for (int a = 0; a < 5; ++a) v[a] = src[((size_t)a * n + b) * kBlockVoxels + j];
+        vol.voxel4[e] = make_float4(v[0], v[1], v[2], v[3]);
+        vol.blue[e] = v[4];
+    }
 }
 
 }  // namespace

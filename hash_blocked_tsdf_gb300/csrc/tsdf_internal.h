@@ -58,11 +58,12 @@ struct VolumeView {
     Entry* table;
     uint32_t table_mask;        // table_capacity - 1
     uint32_t pool_capacity;
-    float* tsdf;                // the five SoA arrays, [pool_capacity][512] each
-    float* weight;
-    float* red;
-    float* green;
-    float* blue;
+    // The pool's five sums per voxel, voxel j of block b at index b * 512 + j:
+    // tsdf, weight, red and green interleaved in one 16-byte record (so a
+    // sample reaches them with one 4-wide reduction), blue in an array of
+    // its own.
+    float4* voxel4;             // [pool_capacity][512] (tsdf, weight, red, green)
+    float* blue;                // [pool_capacity][512]
     uint32_t* pool_counter;     // bump allocator for pool indices
     DeviceCounters* counters;
     DivisorPair div;            // voxel size and truncation, with reciprocals
@@ -127,11 +128,16 @@ cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 cudaError_t launch_extract(const VolumeView& vol, const int32_t* coords, uint32_t n_blocks,
                            float* out, uint64_t capacity, unsigned long long* count,
                            cudaStream_t stream);
-// Copy block i's five arrays (src: [5][n][512]) to the pool slot the table
-// gives its coordinate (inserted beforehand).
+// Copy block i's five sums (src: [5][n][512], the order tsdf, weight, red,
+// green, blue) to the pool slot the table gives its coordinate (inserted
+// beforehand).
 cudaError_t launch_import(const VolumeView& vol, const int32_t* coords, uint32_t n,
                           const float* src, cudaStream_t stream);
 cudaError_t launch_export_coords(const VolumeView& vol, int32_t* coords, cudaStream_t stream);
+// Split voxel records [first, first + n) into four planes of n floats each
+// (tsdf, weight, red, green) at out.
+cudaError_t launch_split_records(const VolumeView& vol, size_t first, size_t n, float* out,
+                                 cudaStream_t stream);
 
 }  // namespace tsdf
 

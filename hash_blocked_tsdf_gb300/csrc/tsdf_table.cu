@@ -7,20 +7,35 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Zero blocks [0, min(*pool_counter, capacity)) of all five arrays.  The
-// count is read on the device, so a reset needs no host round trip.
+// Zero blocks [0, min(*pool_counter, capacity)) of the pool (the voxel
+// records and the blue array).  The count is read on the device, so a reset
+// needs no host round trip.
 __global__ void __launch_bounds__(kThreads) zero_used_blocks_kernel(VolumeView vol)
 {
     const uint32_t used = min(*vol.pool_counter, vol.pool_capacity);
-    const size_t n4 = (size_t)used * (kBlockVoxels / 4);
-    float4* arrays[5] = {reinterpret_cast<float4*>(vol.tsdf), reinterpret_cast<float4*>(vol.weight),
-                         reinterpret_cast<float4*>(vol.red), reinterpret_cast<float4*>(vol.green),
-                         reinterpret_cast<float4*>(vol.blue)};
+    const size_t n_rec = (size_t)used * kBlockVoxels;       // 16-byte voxel records
+    const size_t n_blue = n_rec / 4;                         // blue, as float4
+    float4* blue4 = reinterpret_cast<float4*>(vol.blue);
     const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const size_t stride = (size_t)gridDim.x * kThreads;
-    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < n4; e += stride) {
-#pragma unroll
-        for (int a = 0; a < 5; ++a) arrays[a][e] = z;
+    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < n_rec; e += stride) {
+        vol.voxel4[e] = z;
+        if (e < n_blue) blue4[e] = z;
+    }
+}
+
+// Voxel records [first, first + n) of the pool split into four planes:
+// out[k * n + i] = component k (tsdf, weight, red, green) of record first + i.
+__global__ void __launch_bounds__(kThreads) split_records_kernel(VolumeView vol, size_t first,
+                                                                 size_t n, float* out)
+{
+    const size_t stride = (size_t)gridDim.x * kThreads;
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        const float4 r = vol.voxel4[first + i];
+        out[i] = r.x;
+        out[n + i] = r.y;
+        out[2 * n + i] = r.z;
+        out[3 * n + i] = r.w;
     }
 }
 
@@ -85,6 +100,16 @@ cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream)
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
     zero_used_blocks_kernel<<<(unsigned)(sms * 8), kThreads, 0, stream>>>(vol);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_split_records(const VolumeView& vol, size_t first, size_t n, float* out,
+                                 cudaStream_t stream)
+{
+    if (n == 0) return cudaSuccess;
+    const size_t want = (n + kThreads - 1) / kThreads;
+    const unsigned grid = (unsigned)(want < 4096 ? want : 4096);
+    split_records_kernel<<<grid, kThreads, 0, stream>>>(vol, first, n, out);
     return cudaGetLastError();
 }
 

@@ -11,18 +11,21 @@
 //
 // update_kernel (per sample): every thread walks one pixel's band, looks
 // up each passing sample's block (one lookup per new key, almost always a
-// first-probe hit) and adds (tsdf, 1, r, g, b) with five red.global.add.f32.
-// Blocks of 256 threads own 16 x 16 pixel tiles of one frame, each warp an
-// 8 x 4 patch.  Where samples rarely share a voxel this is bound by the L2's
-// rate of reduction sectors, and nothing on chip would save much.
+// first-probe hit) and adds (tsdf, 1, r, g, b) with two reductions: one
+// 4-wide into the voxel's (tsdf, weight, red, green) record, one scalar into
+// the blue array.  Blocks of 256 threads own 16 x 16 pixel tiles of one
+// frame, each warp an 8 x 4 patch.  Where samples rarely share a voxel this
+// is bound by the L2's rate of reduction requests, and nothing on chip would
+// save much.
 //
 // update_rows_kernel (pre-reducing): a block of 192 threads takes an 8 x 8
 // pixel tile of one frame at a time (a listed 16 x 16 tile is four of them;
 // with TSDF_UPDATE_PRE_REDUCED every tile, one per block), three threads per pixel, each walking one third
 // of the pixel's truncation band (a warp covers an 8 x 4 pixel patch).  The
 // block keeps a shared table of the voxel rows its samples fall in (a row is
-// the 8 voxels of a block that share ly and lz: exactly one 32-byte sector of
-// each pool array), and for every voxel of a row two 64-bit masks: which of
+// the 8 voxels of a block that share ly and lz: 128 contiguous bytes of
+// voxel records and one 32-byte sector of the blue array), and for every
+// voxel of a row two 64-bit masks: which of
 // the tile's pixels put a sample in it, and which put a second one (a ray
 // puts at most two samples in a voxel: samples are one voxel edge apart and a
 // voxel is sqrt(3) edges across).  That takes one shared atomicOr per sample.
@@ -30,9 +33,9 @@
 // from the pixel depths and its own centre -- the walk's arithmetic, so the
 // same values -- sums them with the pixels' colours in pixel order, and adds
 // its five sums to the pool; the voxels of a row are flushed by adjacent
-// lanes, so each row reaches L2 as one reduction per array instead of one
-// per sample and array.  Rows that find no slot in the shared table add
-// their samples directly.
+// lanes, so each row reaches L2 as five sectors instead of two reductions per
+// sample.  Rows that find no slot in the shared table add their samples
+// directly.
 //
 // Both grids run tile-major, frame-minor, so the frames' updates of the same
 // voxels meet in L2.
@@ -47,11 +50,6 @@ constexpr int kTileW = 16;
 constexpr int kTileH = 16;
 constexpr int kThreads = kTileW * kTileH;
 
-__device__ __forceinline__ void red_add(float* addr, float v)
-{
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
-}
-
 // kSparseOnly: leave dense tiles to update_rows_kernel (adaptive mode).
 // kReproject: the occlusion test by reprojection of the voxel centre; each
 // passing sample adds the colour of the pixel it was tested against.
@@ -65,7 +63,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     const Camera cam = fb.frame[f].cam;
     // each warp takes an 8 x 4 pixel patch of the tile (8 warps: 2 across,
     // 4 down): a squarer footprint puts more of a warp's samples in common
-    // voxel rows (one 32-byte sector per array) than a 16 x 2 strip
+    // voxel rows than a 16 x 2 strip
     const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31u);
     const int u = (tile % tiles_x) * kTileW + (w & 1) * 8 + (l & 7);
     const int v = (tile / tiles_x) * kTileH + (w >> 1) * 4 + (l >> 3);
@@ -130,11 +128,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                 continue;
             }
             const size_t e = (size_t)idx * kBlockVoxels + (size_t)local_voxel(s.ix, s.iy, s.iz);
-            red_add(vol.tsdf + e, s.tsdf);
-            red_add(vol.weight + e, 1.0f);
-            red_add(vol.red + e, cr);
-            red_add(vol.green + e, cg);
-            red_add(vol.blue + e, cb);
+            add_to_voxel(vol, e, s.tsdf, 1.0f, cr, cg, cb);
             ++updates;
         }
     }
@@ -315,11 +309,8 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
         }
         if (direct) {
             const size_t e = (size_t)idx * kBlockVoxels + row * 8 + lx;
-            red_add(vol.tsdf + e, s.tsdf);
-            red_add(vol.weight + e, 1.0f);
-            red_add(vol.red + e, s_pixf[kPxR * kRowPix + q]);
-            red_add(vol.green + e, s_pixf[kPxG * kRowPix + q]);
-            red_add(vol.blue + e, s_pixf[kPxB * kRowPix + q]);
+            add_to_voxel(vol, e, s.tsdf, 1.0f, s_pixf[kPxR * kRowPix + q],
+                         s_pixf[kPxG * kRowPix + q], s_pixf[kPxB * kRowPix + q]);
         }
     }
     flush_rows<kFast>(vol, cam, sm);
@@ -419,9 +410,8 @@ __device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& 
     // flush: each listed cell recomputes its samples' tsdf from the pixel
     // depths and its voxel centre (the walk's own arithmetic), sums them with
     // the colours in pixel order, and adds the five sums to the pool; cells of
-    // one row sit next to each other, so a row reaches L2 as one sector per array
+    // one row sit next to each other, so a row reaches L2 as five sectors
     const int n_cells = (int)sm[kOffCount + 1];
-    float* arrays[5] = {vol.tsdf, vol.weight, vol.red, vol.green, vol.blue};
     for (int k = t; k < n_cells; k += kRowThreads) {
         const uint32_t code = s_cell_list[k];
         const uint32_t slot = code >> 3;
@@ -455,8 +445,7 @@ __device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& 
             }
         }
         const size_t e = (size_t)(row_key >> 6) * kBlockVoxels + (size_t)row * 8 + lx;
-#pragma unroll
-        for (int a = 0; a < 5; ++a) red_add(arrays[a] + e, sum[a]);
+        add_to_voxel(vol, e, sum[0], sum[1], sum[2], sum[3], sum[4]);
     }
 }
 

@@ -16,6 +16,10 @@ using namespace tsdf;
 
 namespace {
 
+// Blocks per chunk when export splits the interleaved voxel records into
+// planes (16,384 blocks: a 128 MB scratch buffer).
+constexpr uint32_t kExportChunkBlocks = 1u << 14;
+
 // Device-resident mutable state: the pool's bump counter and the counters.
 struct DeviceState {
     uint32_t pool_counter;
@@ -45,9 +49,11 @@ struct tsdf_volume {
 
     Entry* table = nullptr;
     uint32_t* dense_list = nullptr;  // [kDenseListCapacity] adaptive update's dense tiles
-    float* pool = nullptr;          // five arrays of pool_capacity * 512 floats, back to back
+    float* pool = nullptr;          // pool_capacity * 512 voxel records of 4 floats, then
+                                    // pool_capacity * 512 blue sums
     DeviceState* state = nullptr;
     int32_t* coords = nullptr;      // [pool_capacity][3], allocated on first export
+    float* export_scratch = nullptr;  // [kExportChunkBlocks][512][4], allocated on first export
 
     // host-batch staging: two buffers of (depth, rgb) frames
     float* stage[2] = {nullptr, nullptr};
@@ -90,10 +96,7 @@ VolumeView view_of(const tsdf_volume* v)
     w.table_mask = v->table_capacity - 1;
     w.pool_capacity = v->pool_capacity;
     const size_t n = array_floats(v);
-    w.tsdf = v->pool;
-    w.weight = v->pool + n;
-    w.red = v->pool + 2 * n;
-    w.green = v->pool + 3 * n;
+    w.voxel4 = reinterpret_cast<float4*>(v->pool);      // n records of 4 floats
     w.blue = v->pool + 4 * n;
     w.pool_counter = &v->state->pool_counter;
     w.counters = &v->state->counters;
@@ -175,6 +178,7 @@ void release(tsdf_volume* v)
     if (v->table) cudaFree(v->table);
     if (v->dense_list) cudaFree(v->dense_list);
     if (v->pool) cudaFree(v->pool);
+    if (v->export_scratch) cudaFree(v->export_scratch);
     if (v->state) cudaFree(v->state);
     if (v->coords) cudaFree(v->coords);
     for (int b = 0; b < 2; ++b) {
@@ -370,13 +374,14 @@ int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out)
 {
     if (!vol || !out) return fail(TSDF_ERR_ARG, "null argument");
     const VolumeView w = view_of(vol);
-    out->tsdf = w.tsdf;
-    out->weight = w.weight;
-    out->r = w.red;
-    out->g = w.green;
+    float* rec = reinterpret_cast<float*>(w.voxel4);
+    out->tsdf = rec;
+    out->weight = rec + 1;
+    out->r = rec + 2;
+    out->g = rec + 3;
     out->b = w.blue;
     out->pool_capacity = vol->pool_capacity;
-    out->reserved = 0;
+    out->stride = 4;
     return TSDF_OK;
 }
 
@@ -520,13 +525,31 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
                   "cudaMemcpyAsync(coords)");
     }
     const VolumeView w = view_of(vol);
-    float* src[5] = {w.tsdf, w.weight, w.red, w.green, w.blue};
-    float* dst[5] = {tsdf_out, weight, r, g, b};
-    for (int a = 0; a < 5; ++a) {
-        if (!dst[a]) continue;
-        TSDF_CUDA(cudaMemcpyAsync(dst[a], src[a] + (size_t)first * kBlockVoxels,
+    if (b)
+        TSDF_CUDA(cudaMemcpyAsync(b, w.blue + (size_t)first * kBlockVoxels,
                                   (size_t)count * kBlockVoxels * sizeof(float),
-                                  cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(sums)");
+                                  cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(blue)");
+    float* dst[4] = {tsdf_out, weight, r, g};
+    if (tsdf_out || weight || r || g) {
+        // the interleaved records are split into planes on the device, a
+        // chunk of blocks at a time, and each plane is copied out whole
+        if (!vol->export_scratch)
+            TSDF_CUDA(cudaMalloc(&vol->export_scratch,
+                                 (size_t)kExportChunkBlocks * kBlockVoxels * 4 * sizeof(float)),
+                      "cudaMalloc(export scratch)");
+        for (uint32_t c0 = 0; c0 < count; c0 += kExportChunkBlocks) {
+            const uint32_t nb = count - c0 < kExportChunkBlocks ? count - c0 : kExportChunkBlocks;
+            const size_t nv = (size_t)nb * kBlockVoxels;
+            TSDF_CUDA(launch_split_records(w, ((size_t)first + c0) * kBlockVoxels, nv,
+                                           vol->export_scratch, s), "split_records kernel");
+            for (int a = 0; a < 4; ++a) {
+                if (!dst[a]) continue;
+                TSDF_CUDA(cudaMemcpyAsync(dst[a] + (size_t)c0 * kBlockVoxels,
+                                          vol->export_scratch + (size_t)a * nv,
+                                          nv * sizeof(float), cudaMemcpyDeviceToHost, s),
+                          "cudaMemcpyAsync(sums)");
+            }
+        }
     }
     TSDF_CUDA(cudaStreamSynchronize(s), "cudaStreamSynchronize");
     return TSDF_OK;

@@ -8,8 +8,8 @@
  *     8^3 = 512 voxels.  An open-addressed, linear-probing hash table of
  *     16-byte entries (a packed 64-bit block key, a 32-bit pool index, 4 bytes
  *     of padding), sized to a power of two at least twice the pool capacity,
- *     maps a block coordinate to an index into a flat pool of five float
- *     arrays: TSDF sum, weight sum, red, green and blue sums.
+ *     maps a block coordinate to an index into a flat pool holding five
+ *     float sums per voxel: TSDF, weight, red, green and blue.
  *   design section, integration: two kernels run over the same
  *     back-projected depth points.  ALLOCATE walks each point's truncation
  *     band and inserts every missing block with a single 64-bit
@@ -39,8 +39,14 @@
  *   - block coordinates must lie in [-2^20, 2^20 - 1] per axis (the 21-bit
  *     key fields); samples outside are counted (out_of_range_samples) and
  *     skipped.
- *   - pool layout: for each of the five arrays, block b's voxel
- *     j = lx + 8 * ly + 64 * lz lives at element b * 512 + j.
+ *   - pool layout: block b's voxel j = lx + 8 * ly + 64 * lz is record
+ *     v = b * 512 + j.  Its TSDF, weight, red and green sums are interleaved
+ *     in one 16-byte record, floats 4v .. 4v + 3 of the record array; its
+ *     blue sum is element v of a separate blue array.  (The pages keep five
+ *     separate arrays; the record lets a sample's update reach four of its
+ *     five sums with one 4-wide reduction, and L2 executes reduction
+ *     requests at about the same rate whether they carry one float or four.)
+ *     tsdf_export_blocks returns the five sums as separate arrays.
  *
  * Ownership and synchronisation
  *   - A tsdf_volume owns its device memory (table, pool, counters), allocated
@@ -99,9 +105,12 @@ typedef struct tsdf_info {
     int32_t max_frames_per_launch;    /* frames a batch call packs into one launch */
 } tsdf_info;
 
-/* Device pointers to the pool's five arrays, each float32
- * [pool_capacity][512] (block b, voxel j at b * 512 + j).  They stay valid
- * until tsdf_destroy; reading them races with kernels still running. */
+/* Device pointers to the pool's five sums.  Record v = b * 512 + j (block b,
+ * voxel j) holds tsdf[stride * v], weight[stride * v], r[stride * v] and
+ * g[stride * v] (the four interleaved: weight = tsdf + 1, r = tsdf + 2,
+ * g = tsdf + 3, stride = 4), and b[v].  Each field spans pool_capacity * 512
+ * voxels.  They stay valid until tsdf_destroy; reading them races with
+ * kernels still running. */
 typedef struct tsdf_pool_view {
     float* tsdf;
     float* weight;
@@ -109,7 +118,7 @@ typedef struct tsdf_pool_view {
     float* g;
     float* b;
     uint32_t pool_capacity;
-    uint32_t reserved;
+    uint32_t stride;            /* floats between voxels in tsdf, weight, r, g: 4 */
 } tsdf_pool_view;
 
 /* Counters accumulated since create / reset / tsdf_clear_stats. */
@@ -154,7 +163,7 @@ int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out);
 int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out);
 
 /* Empty the volume on `stream`: zero the used prefix of the pool (the first
- * min(blocks_allocated, pool_capacity) blocks of all five arrays), empty the
+ * min(blocks_allocated, pool_capacity) blocks' records and blue sums), empty the
  * table and zero every counter. */
 int tsdf_reset(tsdf_volume* vol, void* stream);
 
@@ -225,8 +234,11 @@ int tsdf_block_count(tsdf_volume* vol, void* stream, uint32_t* out);
 
 /* Copy pool blocks [first, first + count) to the host, after synchronising
  * `stream`: coords int32 [count][3] (block coordinates, recovered from the
- * table) and the five sum arrays float32 [count][512].  Any output pointer may
- * be NULL to skip it.  first + count must not exceed tsdf_block_count.  Pool
+ * table) and the five sums as separate arrays float32 [count][512] each.  Any
+ * output pointer may be NULL to skip it.  first + count must not exceed
+ * tsdf_block_count.  The first call that asks for tsdf, weight, r or g
+ * allocates a 128 MB device scratch buffer (kept until tsdf_destroy) in
+ * which the interleaved records are split, 16,384 blocks at a time.  Pool
  * order is the order in which blocks won their pool index, which is not
  * deterministic: compare by coordinate. */
 int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t count,

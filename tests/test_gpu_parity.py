@@ -227,6 +227,39 @@ def test_host_batch_matches_device_batch(torch_cuda, oracle_mod):
     b.close()
 
 
+def test_pool_view_matches_export(torch_cuda):
+    """The zero-copy pool view: tsdf, weight, r and g interleaved per voxel
+    (stride 4), blue plain; the same numbers as the export's separate arrays."""
+    from hash_blocked_tsdf_gb300 import binding
+    torch = torch_cuda
+    frames = scenes.tiny_sphere_plane()
+    vol = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, vol)
+    n = vol.block_count()
+    g = vol.export_blocks()
+    p = binding.tsdf_get_pool(vol.handle)
+    cap = p["pool_capacity"]
+    assert p["stride"] == 4
+    assert (p["weight"] - p["tsdf"], p["r"] - p["tsdf"], p["g"] - p["tsdf"]) == (4, 8, 12)
+
+    class _View:
+        def __init__(self, ptr, count):
+            self.__cuda_array_interface__ = {"shape": (count,), "typestr": "<f4",
+                                             "data": (ptr, False), "version": 3,
+                                             "strides": None}
+    rec = torch.as_tensor(_View(p["tsdf"], cap * 512 * 4), device="cuda").view(cap, 512, 4)
+    blue = torch.as_tensor(_View(p["b"], cap * 512), device="cuda").view(cap, 512)
+    for k, key in enumerate(("tsdf", "weight", "r", "g")):
+        np.testing.assert_array_equal(rec[:n, :, k].cpu().numpy(), g[key])
+    np.testing.assert_array_equal(blue[:n].cpu().numpy(), g["b"])
+    assert float(rec[n:].abs().sum()) == 0.0 and float(blue[n:].abs().sum()) == 0.0
+    # export of a sub-range (offset into the records)
+    part = vol.export_blocks(first=n // 3, count=n // 2)
+    for key in ("tsdf", "weight", "r", "g", "b"):
+        np.testing.assert_array_equal(part[key], g[key][n // 3:n // 3 + n // 2])
+    vol.close()
+
+
 def test_reset_gives_a_fresh_volume(torch_cuda, oracle_mod):
     torch = torch_cuda
     frames = scenes.vga_sphere_plane()
