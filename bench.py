@@ -70,7 +70,7 @@ def parse_args():
     ap.add_argument("--pool", type=int, default=0,
                     help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
-                    default="adaptive", help="how the library's update reaches the pool")
+                    default="per_sample", help="how the library's update reaches the pool")
     ap.add_argument("--occlusion", choices=["ray", "reproject"], default="ray",
                     help="occlusion test: the ray pixel's depth (default) or the depth where "
                          "the voxel centre projects")
@@ -398,7 +398,7 @@ def run_sweep(args):
         clocks.start()
         times = {"allocate": [], "update": [], "fused": []}
         for r in range(reps + 3):
-            for mode in ("adaptive", "fused"):
+            for mode in ("per_sample", "fused"):
                 vol.set_update_kernel(mode)
                 vol.reset()
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
@@ -450,7 +450,7 @@ def _update_kernels(args, frames, n_frames: int) -> int:
     """Kernels one update launch runs: the adaptive mode runs the per-sample
     and the pre-reducing kernel when the launch holds 2^18 pixels or more;
     the fused mode runs one kernel for both stages (counted here, with the
-    allocate counted as none)."""
+    allocate counted as none); the others one."""
     if getattr(args, "occlusion", "ray") == "reproject":
         return 1                 # per-sample update, allocate and update as two kernels
     if args.update_kernel == "fused":

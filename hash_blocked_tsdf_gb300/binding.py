@@ -401,10 +401,11 @@ UPDATE_KERNELS = {"adaptive": UPDATE_ADAPTIVE, "per_sample": UPDATE_PER_SAMPLE,
 
 
 def tsdf_set_update_kernel(h, kind) -> None:
-    """Select how updates reach the pool: "adaptive" (default: each tile
-    pre-reduces where samples crowd into voxels), "per_sample",
-    "pre_reduced", or "fused" (integrate calls run allocate and update as one
-    kernel); or the header's integer constants."""
+    """Select how updates reach the pool: "per_sample" (default: each warp
+    merges its lanes' samples of one voxel, then reduces into the pool),
+    "adaptive" (tiles whose samples crowd into voxels pre-reduce in shared
+    memory), "pre_reduced" (every tile does), or "fused" (integrate calls run
+    allocate and update as one kernel); or the header's integer constants."""
     k = UPDATE_KERNELS[kind] if isinstance(kind, str) else int(kind)
     _check(load_library().tsdf_set_update_kernel(h, k), "tsdf_set_update_kernel")
 

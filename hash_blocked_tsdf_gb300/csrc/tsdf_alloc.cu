@@ -266,17 +266,16 @@ __device__ __forceinline__ uint32_t published_index(const VolumeView& vol, uint3
 // One walk per pixel does both stages: the band's samples (voxel, tsdf) are
 // kept in registers while the distinct block keys go through the allocate
 // kernel's warp insert rounds; each round's result (the key's slot, hence
-// its pool index) then serves the update's reductions for that key's
-// samples, with no second walk and no lookup.  Tiles and warp patches as in
-// the per-sample update kernel (16 x 16, 8 x 4), grid tile-major, frame-minor.
-// With kSparseOnly a dense tile (the adaptive rule) still allocates here but
-// is listed for the pre-reducing update instead of adding its samples.
-template <bool kInstrument, bool kFast, bool kSparseOnly>
+// its pool index) gives the pool index of that key's samples, with no second
+// walk and no lookup.  The samples are then added band step by band step,
+// the warp merging the samples of one step that fall in the same voxel, as
+// in the per-sample update kernel.  Tiles and warp patches as in that kernel
+// (16 x 16, 8 x 4), grid tile-major, frame-minor.
+template <bool kInstrument, bool kFast>
 __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     VolumeView vol, const __grid_constant__ FrameBatch fb)
 {
     __shared__ ProbeStats st;
-    __shared__ uint32_t s_listed;
     if (kInstrument) init_probe_stats(&st);
 
     const int f = blockIdx.x % fb.n;
@@ -288,28 +287,13 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     const int v = (tile / tiles_x) * 16 + (w >> 1) * 4 + (l >> 3);
     const bool inside = u < fb.width && v < fb.height;
     const float depth = inside ? __ldg(fb.frame[f].depth + (size_t)v * fb.width + u) : 0.0f;
-    bool listed = false;                    // this tile's samples are left to the pre-reduction
-    if (kSparseOnly) {
-        const uint32_t n_valid = (uint32_t)__syncthreads_count(valid_depth(depth));
-        const uint32_t n_dense =
-            (uint32_t)__syncthreads_count(dense_pixel(depth, vol.div.voxel, cam.fx, fb.n));
-        if (dense_tile(n_valid, n_dense)) {             // uniform over the block
-            if (threadIdx.x == 0) {
-                const uint32_t pos = atomicAdd(vol.dense_count, 1u);
-                s_listed = pos < vol.dense_capacity ? 1u : 0u;
-                if (s_listed) vol.dense_list[pos] = (uint32_t)f << 24 | (uint32_t)tile;
-            }
-            __syncthreads();
-            listed = s_listed != 0;
-        }
-    }
     RayPoint p;
     bool valid = false;
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
         valid = back_project(cam, u, v, depth, p);
-        if (valid && !listed) {
+        if (valid) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);
             cg = __ldg(rgb + 3 * pix + 1);
@@ -318,11 +302,13 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     }
     const int steps = 2 * vol.band_half + 1;
     // distinct keys, newest first, each with the mask of its band steps; and
-    // per step the sample's voxel in its block and its tsdf
+    // per step the sample's voxel in its block, its tsdf and (after the
+    // insert rounds) its block's pool index
     unsigned long long keys[kShortBand];
     uint32_t masks[kShortBand];
     int lv[kShortBand];
     float tv[kShortBand];
+    uint32_t sidx[kShortBand];
     int n_keys = 0;
     unsigned long long last = kEmptyKey;
     uint32_t out_of_range = 0;
@@ -332,6 +318,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
         masks[j] = 0;
         lv[j] = 0;
         tv[j] = 0.0f;
+        sidx[j] = kIndexFailed;
         if (valid && j < steps) {
             VoxelSample s;
             const int status = band_sample<kFast>(cam, vol.div, p, j - vol.band_half, s);
@@ -357,33 +344,24 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
             }
         }
     }
-    uint32_t updates = 0, missed = 0, timeouts = 0;
+    uint32_t passed = 0;                    // band steps whose sample passed
+#pragma unroll
+    for (int m = 0; m < kShortBand; ++m) passed |= masks[m];
+    uint32_t updates = 0, timeouts = 0;
     const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)n_keys);
     for (int r = 0; r < rounds; ++r) {
         const bool offered = r < n_keys;
         const InsertResult ins = warp_insert_step<kInstrument>(vol, offered, keys[0], &st);
         __syncwarp();                       // this warp's winners have published
         if (offered) {
-            const uint32_t m = masks[0];
             uint32_t idx = kIndexFailed;
             if (ins.res != kProbeOverflow) {
                 idx = published_index(vol, ins.slot);
                 if (idx == kIndexPending) ++timeouts;
             }
-            if (listed) {
-                // allocated here; the pre-reducing update adds the samples
-            } else if (idx < vol.pool_capacity) {
-                const size_t base = (size_t)idx * kBlockVoxels;
 #pragma unroll
-                for (int j = 0; j < kShortBand; ++j) {
-                    if (m & (1u << j)) {
-                        add_to_voxel(vol, base + (size_t)lv[j], tv[j], 1.0f, cr, cg, cb);
-                        ++updates;
-                    }
-                }
-            } else {
-                missed += (uint32_t)__popc(m);   // absent (overflow), FAILED or timed out
-            }
+            for (int j = 0; j < kShortBand; ++j)
+                if (masks[0] & (1u << j)) sidx[j] = idx;
         }
 #pragma unroll
         for (int m = 0; m < kShortBand - 1; ++m) {
@@ -391,7 +369,18 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
             masks[m] = masks[m + 1];
         }
     }
-    const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, (valid && !listed) ? 1u : 0u);
+    // the update, one band step at a time for the whole warp
+#pragma unroll
+    for (int j = 0; j < kShortBand; ++j) {
+        // (pool indices are below 2^23, so e fits in 32 bits)
+        const bool add = (passed >> j & 1u) && sidx[j] < vol.pool_capacity;
+        const uint32_t e = add ? sidx[j] * (uint32_t)kBlockVoxels + (uint32_t)lv[j] : 0u;
+        warp_add_samples(vol, add, e, tv[j], cr, cg, cb);
+        updates += add ? 1u : 0u;
+    }
+    // absent (overflow), FAILED or timed out
+    const uint32_t missed = (uint32_t)__popc(passed) - updates;
+    const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, valid ? 1u : 0u);
     const uint32_t w_updates = __reduce_add_sync(0xFFFFFFFFu, updates);
     const uint32_t w_missed = __reduce_add_sync(0xFFFFFFFFu, missed);
     const uint32_t w_oor = __reduce_add_sync(0xFFFFFFFFu, out_of_range);
@@ -463,16 +452,6 @@ cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords,
     return cudaGetLastError();
 }
 
-template <bool kInstrument, bool kFast>
-void launch_fused_t(const VolumeView& vol, const FrameBatch& fb, bool sparse_only, unsigned grid,
-                    cudaStream_t stream)
-{
-    if (sparse_only)
-        integrate_fused_kernel<kInstrument, kFast, true><<<grid, kThreads, 0, stream>>>(vol, fb);
-    else
-        integrate_fused_kernel<kInstrument, kFast, false><<<grid, kThreads, 0, stream>>>(vol, fb);
-}
-
 cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                                    cudaStream_t stream)
 {
@@ -481,18 +460,14 @@ cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, 
         return cudaErrorInvalidValue;
     const unsigned tiles = (unsigned)(((fb.width + 15) / 16) * ((fb.height + 15) / 16));
     const unsigned grid = tiles * (unsigned)fb.n;
-    const bool sparse_only =
-        (uint64_t)fb.width * (uint64_t)fb.height * (uint64_t)fb.n >= kAdaptiveMinPixels;
     if (instrument) {
-        if (vol.fast_div) launch_fused_t<true, true>(vol, fb, sparse_only, grid, stream);
-        else launch_fused_t<true, false>(vol, fb, sparse_only, grid, stream);
+        if (vol.fast_div) integrate_fused_kernel<true, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+        else integrate_fused_kernel<true, false><<<grid, kThreads, 0, stream>>>(vol, fb);
     } else {
-        if (vol.fast_div) launch_fused_t<false, true>(vol, fb, sparse_only, grid, stream);
-        else launch_fused_t<false, false>(vol, fb, sparse_only, grid, stream);
+        if (vol.fast_div) integrate_fused_kernel<false, true><<<grid, kThreads, 0, stream>>>(vol, fb);
+        else integrate_fused_kernel<false, false><<<grid, kThreads, 0, stream>>>(vol, fb);
     }
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || !sparse_only) return e;
-    return launch_update_listed(vol, fb, stream);
+    return cudaGetLastError();
 }
 
 }  // namespace tsdf

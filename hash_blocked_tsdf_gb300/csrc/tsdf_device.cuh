@@ -348,6 +348,41 @@ __device__ __forceinline__ void add_to_voxel(const VolumeView& vol, size_t e, fl
     asm volatile("red.global.add.f32 [%0], %1;" ::"l"(vol.blue + e), "f"(b) : "memory");
 }
 
+// Add one band step's samples of a warp (lane: add, voxel e, its terms).
+// Lanes whose samples fall in the same voxel are summed on the lowest of
+// them first (the rays of a tile's neighbouring pixels often meet in a
+// voxel), and that lane adds the group's sums with one pair of reductions.
+// Must be called by all 32 lanes of the warp.
+__device__ __forceinline__ void warp_add_samples(const VolumeView& vol, bool add, uint32_t e,
+                                                 float tsdf, float r, float g, float b)
+{
+    const unsigned act = __ballot_sync(0xFFFFFFFFu, add);
+    if (act == 0) return;
+    const int lane = (int)(threadIdx.x & 31u);
+    unsigned grp = 0;
+    if (add) grp = __match_any_sync(act, e);
+    const bool leader = add && __ffs(grp) - 1 == lane;
+    unsigned rest = leader ? grp & (grp - 1u) : 0u;       // the group's other lanes
+    const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)__popc(rest));
+    float st = tsdf, sr = r, sg = g, sb = b;
+    for (int k = 0; k < rounds; ++k) {
+        const int src = rest ? __ffs(rest) - 1 : lane;
+        rest &= rest - 1u;
+        const float a_t = __shfl_sync(0xFFFFFFFFu, tsdf, src);
+        const float a_r = __shfl_sync(0xFFFFFFFFu, r, src);
+        const float a_g = __shfl_sync(0xFFFFFFFFu, g, src);
+        const float a_b = __shfl_sync(0xFFFFFFFFu, b, src);
+        if (src != lane) {
+            st = __fadd_rn(st, a_t);
+            sr = __fadd_rn(sr, a_r);
+            sg = __fadd_rn(sg, a_g);
+            sb = __fadd_rn(sb, a_b);
+        }
+    }
+    if (leader) add_to_voxel(vol, e, st, (float)__popc(grp), sr, sg, sb);
+}
+
+
 // Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
 // at least half of its valid pixels (finite depth > 0) see a voxel edge at
 // least w pixels wide (voxel * fx >= w * depth): there samples crowd into few

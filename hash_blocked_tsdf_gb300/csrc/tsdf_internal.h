@@ -105,9 +105,8 @@ cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool in
 // the per-sample update or the fused integrate kernel of the same batch).
 cudaError_t launch_update_listed(const VolumeView& vol, const FrameBatch& fb,
                                  cudaStream_t stream);
-// Allocate and update in one kernel (bands of at most 9 samples); for
-// launches of 2^18 pixels or more the dense tiles are listed and pre-reduced
-// by a second kernel, as in the adaptive update.
+// Allocate and update in one kernel (bands of at most 9 samples, the ray
+// occlusion test).
 cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                                    cudaStream_t stream);
 cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords, uint32_t n,

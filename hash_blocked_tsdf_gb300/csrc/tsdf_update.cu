@@ -13,8 +13,11 @@
 // up each passing sample's block (one lookup per new key, almost always a
 // first-probe hit) and adds (tsdf, 1, r, g, b) with two reductions: one
 // 4-wide into the voxel's (tsdf, weight, red, green) record, one scalar into
-// the blue array.  Blocks of 256 threads own 16 x 16 pixel tiles of one
-// frame, each warp an 8 x 4 patch.  Where samples rarely share a voxel this
+// the blue array.  The lanes of a warp take the band steps together, and the
+// samples of one step that fall in the same voxel are summed in registers
+// first (warp_add_samples), so such a group costs one pair of reductions.
+// Blocks of 256 threads own 16 x 16 pixel tiles of one frame, each warp an
+// 8 x 4 patch.  Where samples rarely share a voxel this
 // is bound by the L2's rate of reduction requests, and nothing on chip would
 // save much.
 //
@@ -101,36 +104,46 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
         }
     }
     uint32_t updates = 0, missed = 0;
-    if (valid) {
-        unsigned long long last = kEmptyKey;
-        uint32_t idx = kIndexFailed;
-        for (int i = -vol.band_half; i <= vol.band_half; ++i) {
-            VoxelSample s;
+    unsigned long long last = kEmptyKey;
+    uint32_t idx = kIndexFailed;
+    // every lane runs every band step (the warp merges each step's samples)
+    for (int i = -vol.band_half; i <= vol.band_half; ++i) {
+        VoxelSample s;
+        s.tsdf = 0.0f;
+        bool add = false;
+        uint32_t e = 0;
+        if (valid) {
+            int status;
             if (kReproject) {
                 size_t q;
-                if (band_sample_reprojected<kFast>(cam, vol.div, p, i, fb.frame[f].depth,
-                                                   fb.width, fb.height, s, q) != kSamplePass)
-                    continue;
-                const float* rgb = fb.frame[f].rgb;
-                cr = __ldg(rgb + 3 * q);
-                cg = __ldg(rgb + 3 * q + 1);
-                cb = __ldg(rgb + 3 * q + 2);
-            } else if (band_sample<kFast>(cam, vol.div, p, i, s) != kSamplePass) {
-                continue;
+                status = band_sample_reprojected<kFast>(cam, vol.div, p, i, fb.frame[f].depth,
+                                                        fb.width, fb.height, s, q);
+                if (status == kSamplePass) {
+                    const float* rgb = fb.frame[f].rgb;
+                    cr = __ldg(rgb + 3 * q);
+                    cg = __ldg(rgb + 3 * q + 1);
+                    cb = __ldg(rgb + 3 * q + 2);
+                }
+            } else {
+                status = band_sample<kFast>(cam, vol.div, p, i, s);
             }
-            const unsigned long long key = block_key(s.ix, s.iy, s.iz);
-            if (key != last) {
-                idx = lookup(vol.table, vol.table_mask, key);
-                last = key;
+            if (status == kSamplePass) {
+                const unsigned long long key = block_key(s.ix, s.iy, s.iz);
+                if (key != last) {
+                    idx = lookup(vol.table, vol.table_mask, key);
+                    last = key;
+                }
+                if (idx < vol.pool_capacity) {
+                    // (pool indices are below 2^23, so e fits in 32 bits)
+                    e = idx * (uint32_t)kBlockVoxels + (uint32_t)local_voxel(s.ix, s.iy, s.iz);
+                    add = true;
+                    ++updates;
+                } else {
+                    ++missed;                   // absent, FAILED or never published
+                }
             }
-            if (idx >= vol.pool_capacity) {     // absent, FAILED or never published
-                ++missed;
-                continue;
-            }
-            const size_t e = (size_t)idx * kBlockVoxels + (size_t)local_voxel(s.ix, s.iy, s.iz);
-            add_to_voxel(vol, e, s.tsdf, 1.0f, cr, cg, cb);
-            ++updates;
         }
+        warp_add_samples(vol, add, e, s.tsdf, cr, cg, cb);
     }
     const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, valid ? 1u : 0u);
     const uint32_t w_updates = __reduce_add_sync(0xFFFFFFFFu, updates);

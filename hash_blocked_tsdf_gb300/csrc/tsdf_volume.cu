@@ -42,7 +42,7 @@ struct tsdf_volume {
     float trunc = 0.0f;
     int band_half = 0;
     bool instrument = false;
-    int update_kind = TSDF_UPDATE_ADAPTIVE;
+    int update_kind = TSDF_UPDATE_PER_SAMPLE;
     int occlusion = TSDF_OCCLUSION_RAY;
     DivisorPair div = {};
     bool fast_div = false;          // the fixed-divisor division was verified for both divisors
@@ -219,7 +219,7 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
             TSDF_CUDA(launch_allocate(vol, fb, v->instrument, stream), "allocate kernel");
         if (do_update)
             TSDF_CUDA(launch_update(vol, fb,
-                                    v->update_kind == TSDF_UPDATE_FUSED ? TSDF_UPDATE_ADAPTIVE
+                                    v->update_kind == TSDF_UPDATE_FUSED ? TSDF_UPDATE_PER_SAMPLE
                                                                         : v->update_kind,
                                     stream),
                       "update kernel");

@@ -327,17 +327,20 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
 /* How later update launches (integrate, update and their batch forms) add
  * the samples to the pool.  Every mode computes the same sums ("What
  * Irregularity Costs", design section, integration: the update adds tsdf, 1
- * and the pixel colour into the five arrays for every passing sample); they
+ * and the pixel colour into the five sums for every passing sample); they
  * differ in how the additions reach memory:
- *   TSDF_UPDATE_ADAPTIVE (the default): each 16 x 16 pixel tile of a frame
- *     chooses for itself.  Where at least half of its valid pixels see a voxel
- *     edge w or more pixels wide (voxel_size * fx >= w * depth; w = 5 when a
- *     launch holds 4 or more frames, else 10), many samples share a voxel
- *     and the tile pre-reduces (below); elsewhere its samples are added one by
- *     one, as with TSDF_UPDATE_PER_SAMPLE.  Launches of fewer than 2^18
- *     pixels in all are always added one by one.
- *   TSDF_UPDATE_PER_SAMPLE: every passing sample is added to the pool with
- *     five float reductions of its own (16 x 16 pixel tiles).
+ *   TSDF_UPDATE_PER_SAMPLE (the default): each thread walks one pixel's band
+ *     (16 x 16 pixel tiles, 8 x 4 per warp); at every band step the warp sums
+ *     in registers the samples of its lanes that fall in the same voxel, and
+ *     one lane adds them with two reductions (a 4-wide one into the voxel's
+ *     tsdf, weight, red, green record, a scalar one into blue).
+ *   TSDF_UPDATE_ADAPTIVE: each 16 x 16 pixel tile of a frame chooses between
+ *     the per-sample path and the pre-reduction below.  Where at least half of
+ *     its valid pixels see a voxel edge w or more pixels wide
+ *     (voxel_size * fx >= w * depth; w = 5 when a launch holds 4 or more
+ *     frames, else 10), the tile pre-reduces; launches of fewer than 2^18
+ *     pixels in all never do.  (On GB300 the per-sample path with its warp
+ *     merge is faster in every regime measured, dense ones included.)
  *   TSDF_UPDATE_PRE_REDUCED: every tile pre-reduces: it records in shared
  *     memory which of its pixels reached each voxel (once or twice), then sums
  *     every touched voxel's contributions in pixel order and adds the five
@@ -346,12 +349,13 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
  *     its batch forms) run one fused kernel instead of the two: each pixel's
  *     band is walked once, its samples kept in registers while its block keys
  *     go through the allocate kernel's insert rounds, and each key's pool
- *     index then serves the update's additions.  A key claimed by another
- *     thread of the launch is used once that thread has published its index
- *     (the wait on PENDING, bounded: a wait that gives up is counted in
- *     publish_timeouts and its samples in missed_contributions).  Bands longer
- *     than 9 samples, and update-only calls, use the two-kernel path
- *     (adaptive).
+ *     index then serves the update's additions (merged per warp and band step
+ *     as in the per-sample path).  A key claimed by another thread of the
+ *     launch is used once that thread has published its index (the wait on
+ *     PENDING, bounded: a wait that gives up is counted in publish_timeouts
+ *     and its samples in missed_contributions).  Bands longer than 9 samples,
+ *     update-only calls and the reprojection occlusion test use the
+ *     two-kernel path (per sample).
  * Returns TSDF_ERR_ARG for any other value. */
 #define TSDF_UPDATE_ADAPTIVE 0
 #define TSDF_UPDATE_PER_SAMPLE 1

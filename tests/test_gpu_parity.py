@@ -134,7 +134,7 @@ def test_pre_reduced_dense_close_range(torch_cuda, oracle_mod):
     print("dense close range:", rep)
 
 
-@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+@pytest.mark.parametrize("kernel", ["per_sample", "adaptive", "fused"])
 def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod, kernel):
     # one 640 x 480 frame, 3 cm voxels at fx = 525: the sphere's front
     # (depth < 1.575 m) sees a voxel edge 10+ pixels wide (the one-frame
@@ -145,10 +145,13 @@ def test_adaptive_mixes_dense_and_sparse_tiles(torch_cuda, oracle_mod, kernel):
     d = frames.depth[0]
     near = (d > 0) & (0.03 * frames.K[0] >= 10 * d)
     assert 0.05 < near.mean() < 0.6, "the frame must hold both kinds of pixel"
-    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
+    # the near tiles put 100+ samples of one frame in a voxel; their float32
+    # sums, merged in registers in any grouping, are held to the a-priori
+    # summation bound (tests/parity.py), as in the trajectories
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+@pytest.mark.parametrize("kernel", ["per_sample", "adaptive", "fused"])
 def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod, kernel):
     # eight orbit frames in one launch with 2 cm voxels: objects nearer than
     # 2.1 m see a voxel edge 5+ pixels wide (the several-frame rule)
@@ -160,7 +163,7 @@ def test_adaptive_eight_frame_batch(torch_cuda, oracle_mod, kernel):
     _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel=kernel)
 
 
-@pytest.mark.parametrize("kernel", ["adaptive", "fused"])
+@pytest.mark.parametrize("kernel", ["per_sample", "adaptive", "fused"])
 def test_adaptive_dense_frame(torch_cuda, oracle_mod, kernel):
     # 512 x 512 pixels of 1.5 mm against 2 cm voxels: every tile is dense and
     # hundreds of samples reach each voxel (summation tolerance)

@@ -32,7 +32,7 @@ def test_sweep_cell_matches_oracle(torch_cuda, oracle_mod, cell):
     want, counters = o.export(), o.counters()
     d = torch.from_numpy(fr.depth).cuda()
     c = torch.from_numpy(fr.rgb).cuda()
-    for mode in ("adaptive", "fused"):
+    for mode in ("per_sample", "fused"):
         vol = TsdfVolume(fr.pool_capacity, fr.voxel_size, fr.trunc, fr.table_capacity)
         vol.set_update_kernel(mode)
         vol.integrate_batch(d, c, fr.K, fr.poses)
