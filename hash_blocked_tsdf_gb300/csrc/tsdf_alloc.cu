@@ -269,13 +269,15 @@ __device__ __forceinline__ uint32_t published_index(const VolumeView& vol, uint3
 // its pool index) gives the pool index of that key's samples, with no second
 // walk and no lookup.  The samples are then added band step by band step,
 // the warp merging the samples of one step that fall in the same voxel, as
-// in the per-sample update kernel.  Tiles and warp patches as in that kernel
-// (16 x 16, 8 x 4), grid tile-major, frame-minor.
+// in the per-sample update kernel (here through shared-memory slots).
+// Tiles and warp patches as in that kernel (16 x 16, 8 x 4), grid
+// tile-major, frame-minor.
 template <bool kInstrument, bool kFast>
 __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     VolumeView vol, const __grid_constant__ FrameBatch fb)
 {
     __shared__ ProbeStats st;
+    __shared__ float4 s_stage[kThreads];    // each warp's merge slots
     if (kInstrument) init_probe_stats(&st);
 
     const int f = blockIdx.x % fb.n;
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
         // (pool indices are below 2^23, so e fits in 32 bits)
         const bool add = (passed >> j & 1u) && sidx[j] < vol.pool_capacity;
         const uint32_t e = add ? sidx[j] * (uint32_t)kBlockVoxels + (uint32_t)lv[j] : 0u;
-        warp_add_samples(vol, add, e, tv[j], cr, cg, cb);
+        warp_add_samples<true>(vol, s_stage + (threadIdx.x & ~31u), add, e, tv[j], cr, cg, cb);
         updates += add ? 1u : 0u;
     }
     // absent (overflow), FAILED or timed out

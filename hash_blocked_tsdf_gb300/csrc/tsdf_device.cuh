@@ -351,10 +351,19 @@ __device__ __forceinline__ void add_to_voxel(const VolumeView& vol, size_t e, fl
 // Add one band step's samples of a warp (lane: add, voxel e, its terms).
 // Lanes whose samples fall in the same voxel are summed on the lowest of
 // them first (the rays of a tile's neighbouring pixels often meet in a
-// voxel), and that lane adds the group's sums with one pair of reductions.
-// Must be called by all 32 lanes of the warp.
-__device__ __forceinline__ void warp_add_samples(const VolumeView& vol, bool add, uint32_t e,
-                                                 float tsdf, float r, float g, float b)
+// voxel), and that lane adds the group's sums with one pair of reductions;
+// the leader adds its members' terms in lane order.  The members' terms
+// reach the leader either by shuffles, four per member and round, the rounds
+// running to the largest group of the warp (kStaged false), or through
+// `stage`, the warp's 32 float4 slots in shared memory: one 16-byte store per
+// lane and one 16-byte load per member (kStaged true).  Measured on GB300:
+// shuffles are faster in the per-sample update kernel on sparse scenes,
+// the slots in the fused kernel, whose registers are scarcer.  Must be
+// called by all 32 lanes.
+template <bool kStaged>
+__device__ __forceinline__ void warp_add_samples(const VolumeView& vol, float4* stage, bool add,
+                                                 uint32_t e, float tsdf, float r, float g,
+                                                 float b)
 {
     const unsigned act = __ballot_sync(0xFFFFFFFFu, add);
     if (act == 0) return;
@@ -363,20 +372,35 @@ __device__ __forceinline__ void warp_add_samples(const VolumeView& vol, bool add
     if (add) grp = __match_any_sync(act, e);
     const bool leader = add && __ffs(grp) - 1 == lane;
     unsigned rest = leader ? grp & (grp - 1u) : 0u;       // the group's other lanes
-    const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)__popc(rest));
     float st = tsdf, sr = r, sg = g, sb = b;
-    for (int k = 0; k < rounds; ++k) {
-        const int src = rest ? __ffs(rest) - 1 : lane;
-        rest &= rest - 1u;
-        const float a_t = __shfl_sync(0xFFFFFFFFu, tsdf, src);
-        const float a_r = __shfl_sync(0xFFFFFFFFu, r, src);
-        const float a_g = __shfl_sync(0xFFFFFFFFu, g, src);
-        const float a_b = __shfl_sync(0xFFFFFFFFu, b, src);
-        if (src != lane) {
-            st = __fadd_rn(st, a_t);
-            sr = __fadd_rn(sr, a_r);
-            sg = __fadd_rn(sg, a_g);
-            sb = __fadd_rn(sb, a_b);
+    if (kStaged) {
+        if (__any_sync(0xFFFFFFFFu, rest != 0u)) {
+            stage[lane] = make_float4(tsdf, r, g, b);
+            __syncwarp();
+            for (; rest != 0u; rest &= rest - 1u) {
+                const float4 m = stage[__ffs(rest) - 1];
+                st = __fadd_rn(st, m.x);
+                sr = __fadd_rn(sr, m.y);
+                sg = __fadd_rn(sg, m.z);
+                sb = __fadd_rn(sb, m.w);
+            }
+            __syncwarp();                   // the slots are rewritten at the next step
+        }
+    } else {
+        const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)__popc(rest));
+        for (int k = 0; k < rounds; ++k) {
+            const int src = rest ? __ffs(rest) - 1 : lane;
+            rest &= rest - 1u;
+            const float a_t = __shfl_sync(0xFFFFFFFFu, tsdf, src);
+            const float a_r = __shfl_sync(0xFFFFFFFFu, r, src);
+            const float a_g = __shfl_sync(0xFFFFFFFFu, g, src);
+            const float a_b = __shfl_sync(0xFFFFFFFFu, b, src);
+            if (src != lane) {
+                st = __fadd_rn(st, a_t);
+                sr = __fadd_rn(sr, a_r);
+                sg = __fadd_rn(sg, a_g);
+                sb = __fadd_rn(sb, a_b);
+            }
         }
     }
     if (leader) add_to_voxel(vol, e, st, (float)__popc(grp), sr, sg, sb);

@@ -15,7 +15,8 @@
 // 4-wide into the voxel's (tsdf, weight, red, green) record, one scalar into
 // the blue array.  The lanes of a warp take the band steps together, and the
 // samples of one step that fall in the same voxel are summed in registers
-// first (warp_add_samples), so such a group costs one pair of reductions.
+// first (warp_add_samples, by shuffles), so such a group costs one pair of
+// reductions.
 // Blocks of 256 threads own 16 x 16 pixel tiles of one frame, each warp an
 // 8 x 4 patch.  Where samples rarely share a voxel this
 // is bound by the L2's rate of reduction requests, and nothing on chip would
@@ -143,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                 }
             }
         }
-        warp_add_samples(vol, add, e, s.tsdf, cr, cg, cb);
+        warp_add_samples<false>(vol, nullptr, add, e, s.tsdf, cr, cg, cb);
     }
     const uint32_t w_valid = __reduce_add_sync(0xFFFFFFFFu, valid ? 1u : 0u);
     const uint32_t w_updates = __reduce_add_sync(0xFFFFFFFFu, updates);
