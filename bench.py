@@ -71,6 +71,9 @@ def parse_args():
                     help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
                     default="per_sample", help="how the library's update reaches the pool")
+    ap.add_argument("--layout", choices=["interleaved", "planar"], default="interleaved",
+                    help="pool layout: tsdf, weight, r, g interleaved per voxel (default) or "
+                         "five separate arrays")
     ap.add_argument("--occlusion", choices=["ray", "reproject"], default="ray",
                     help="occlusion test: the ray pixel's depth (default) or the depth where "
                          "the voxel centre projects")
@@ -553,6 +556,7 @@ def run_ours(args):
     c_dev = torch.from_numpy(frames.rgb).cuda()
     vol = TsdfVolume(frames.pool_capacity, frames.voxel_size, frames.trunc,
                      frames.table_capacity)
+    vol.set_pool_layout(args.layout)
     vol.set_update_kernel(args.update_kernel)
     vol.set_occlusion(args.occlusion)
     h = vol.handle
@@ -748,6 +752,7 @@ def run_ours(args):
         "frames_per_launch": group,
         "update_kernel": args.update_kernel,
         "occlusion": args.occlusion,
+        "pool_layout": args.layout,
         "stages_ms_per_launch": {"allocate": alloc_ms_avg, "update": upd_ms_avg},
         "stages_note": ("fused: one kernel per group, booked as the update stage" if fused
                         else "allocate launch, then update launch(es), per group"),
@@ -801,6 +806,9 @@ def run_ours(args):
             "note": "tsdf_integrate_batch per group with TSDF_UPDATE_FUSED: one kernel "
                     "allocates and updates (dense tiles pre-reduced by a second)"}
         vol.set_update_kernel(args.update_kernel)
+    if not fused and args.occlusion == "ray" and args.layout == "interleaved":
+        result["variant_planar"] = variant_planar(torch, vol, frames, groups, one_step, stream,
+                                                  args, world)
     if not fused and args.occlusion == "ray":
         result["variant_reproject"] = variant_reproject(
             torch, vol, frames, d_dev, c_dev, groups, one_step, stream, args, world,
@@ -815,6 +823,42 @@ def run_ours(args):
     vol.close()
     if rank == 0:
         print(json.dumps(result), flush=True)
+
+
+def variant_planar(torch, vol, frames, groups, one_step, stream, args, world) -> dict:
+    """The same step with the pool as five separate arrays (the pages' own
+    layout), same protocol: what the interleaved records gain."""
+    vol.reset()
+    torch.cuda.synchronize()
+    vol.set_pool_layout("planar")
+    for _ in range(max(args.warmup, 1)):
+        one_step()
+    ng = len(groups)
+    torch.cuda.synchronize()
+    ta = torch.cuda.Event(enable_timing=True)
+    tb = torch.cuda.Event(enable_timing=True)
+    ta.record(stream)
+    evs = []
+    for _ in range(args.steps):
+        evk = [torch.cuda.Event(enable_timing=True) for _ in range(2 * ng + 1)]
+        one_step(evk)
+        evs.append(evk)
+    tb.record(stream)
+    torch.cuda.synchronize()
+    st = vol.stats()
+    ms = max_over_ranks(ta.elapsed_time(tb), world)
+    alloc = [e[2 * g].elapsed_time(e[2 * g + 1]) for e in evs for g in range(ng)]
+    upd = [e[2 * g + 1].elapsed_time(e[2 * g + 2]) for e in evs for g in range(ng)]
+    vol.reset()
+    torch.cuda.synchronize()
+    vol.set_pool_layout(args.layout)
+    return {
+        "value": sum_over_ranks(st["valid_points"] * args.steps, world) / (ms / 1000.0),
+        "unit": "points/s", "ms_per_step": ms / args.steps,
+        "stages_ms_per_launch": {"allocate": float(np.mean(alloc)), "update": float(np.mean(upd))},
+        "note": "TSDF_LAYOUT_PLANAR: the five sums as separate arrays, five scalar reductions "
+                "per merged sample",
+    }
 
 
 def variant_reproject(torch, vol, frames, d_dev, c_dev, groups, one_step, stream, args, world,
@@ -964,9 +1008,8 @@ def census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups) -> dict:
     from hash_blocked_tsdf_gb300 import binding
     ptrs = binding.tsdf_get_pool(vol.handle)
     cap = vol.info["pool_capacity"]
-    # the weight sums: every 4th float of the interleaved voxel records
-    weight = _as_tensor(torch, ptrs["tsdf"], cap * 512 * ptrs["stride"]).view(
-        -1, ptrs["stride"])[:, 1]
+    # the weight sums (every 4th float in the interleaved layout)
+    weight = _as_tensor(torch, ptrs["weight"], cap * 512, stride=ptrs["stride"])
     prev = torch.empty(weight.shape, dtype=weight.dtype, device=weight.device)
     out = {}
     for name, grp in (("total", groups), ("frame_by_frame",
@@ -987,10 +1030,11 @@ def census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups) -> dict:
     return out
 
 
-def _as_tensor(torch, ptr: int, n: int):
+def _as_tensor(torch, ptr: int, n: int, stride: int = 1):
     class _Arr:
         __cuda_array_interface__ = {"shape": (n,), "typestr": "<f4", "data": (ptr, False),
-                                    "version": 3, "strides": None}
+                                    "version": 3,
+                                    "strides": None if stride == 1 else (4 * stride,)}
     return torch.as_tensor(_Arr(), device="cuda")
 
 

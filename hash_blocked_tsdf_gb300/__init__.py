@@ -11,7 +11,7 @@ from .binding import (TsdfError, TsdfVolume, load_library, tsdf_allocate, tsdf_a
                       tsdf_import_blocks, tsdf_get_info, tsdf_get_pool, tsdf_get_stats,
                       tsdf_integrate, tsdf_integrate_batch, tsdf_integrate_batch_host,
                       tsdf_reset, tsdf_set_instrumentation, tsdf_set_occlusion,
-                      tsdf_set_update_kernel, tsdf_update)
+                      tsdf_set_pool_layout, tsdf_set_update_kernel, tsdf_update)
 
 __all__ = [
     "TsdfError", "TsdfVolume", "load_library", "tsdf_allocate", "tsdf_allocate_batch",
@@ -19,5 +19,6 @@ __all__ = [
     "tsdf_block_count", "tsdf_clear_stats", "tsdf_create", "tsdf_destroy", "tsdf_export_blocks",
     "tsdf_export_table", "tsdf_extract_triangles", "tsdf_import_blocks", "tsdf_get_info", "tsdf_get_pool", "tsdf_get_stats", "tsdf_integrate",
     "tsdf_integrate_batch", "tsdf_integrate_batch_host", "tsdf_reset",
-    "tsdf_set_instrumentation", "tsdf_set_occlusion", "tsdf_set_update_kernel", "tsdf_update",
+    "tsdf_set_instrumentation", "tsdf_set_occlusion", "tsdf_set_pool_layout",
+    "tsdf_set_update_kernel", "tsdf_update",
 ]

@@ -38,7 +38,7 @@ class tsdf_info(ctypes.Structure):
                 ("voxel_size", ctypes.c_float), ("trunc", ctypes.c_float),
                 ("band_samples", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("fixed_divisor_fast_path", ctypes.c_int32),
-                ("max_frames_per_launch", ctypes.c_int32)]
+                ("max_frames_per_launch", ctypes.c_int32), ("pool_layout", ctypes.c_int32)]
 
 
 class tsdf_pool_view(ctypes.Structure):
@@ -88,6 +88,7 @@ SIGNATURES = {
     "tsdf_set_instrumentation": ([_VP, _I], _I),
     "tsdf_set_update_kernel": ([_VP, _I], _I),
     "tsdf_set_occlusion": ([_VP, _I], _I),
+    "tsdf_set_pool_layout": ([_VP, _I], _I),
     "tsdf_last_error": ([], ctypes.c_char_p),
 }
 
@@ -415,6 +416,17 @@ OCCLUSION_REPROJECT = 1
 OCCLUSION_TESTS = {"ray": OCCLUSION_RAY, "reproject": OCCLUSION_REPROJECT}
 
 
+POOL_LAYOUTS = {"interleaved": 0, "planar": 1}
+
+
+def tsdf_set_pool_layout(h, layout) -> None:
+    """Store the five sums "interleaved" (default: tsdf, weight, r, g in one
+    16-byte record per voxel, blue apart) or "planar" (five separate arrays);
+    only while the volume holds no block."""
+    k = POOL_LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    _check(load_library().tsdf_set_pool_layout(h, k), "tsdf_set_pool_layout")
+
+
 def tsdf_set_occlusion(h, mode) -> None:
     """Select the occlusion test of later launches: "ray" (default: the depth
     of the pixel whose ray selected the voxel) or "reproject" (the depth of
@@ -503,3 +515,7 @@ class TsdfVolume:
 
     def set_occlusion(self, mode):
         tsdf_set_occlusion(self.handle, mode)
+
+    def set_pool_layout(self, layout):
+        tsdf_set_pool_layout(self.handle, layout)
+        self.info = tsdf_get_info(self.handle)

@@ -328,24 +328,43 @@ __device__ __forceinline__ uint32_t lookup(const Entry* __restrict__ table, uint
 
 __device__ __forceinline__ unsigned lane_id() { return threadIdx.x & 31u; }
 
+// Field k (0 tsdf, 1 weight, 2 red, 3 green) of the planar layout.
+__device__ __forceinline__ float* planar_field(const VolumeView& vol, int k)
+{
+    return reinterpret_cast<float*>(vol.voxel4) + (size_t)k * vol.plane;
+}
+
 // The tsdf and weight sums of voxel e (the first half of its record).
 __device__ __forceinline__ float2 tsdf_and_weight(const VolumeView& vol, size_t e)
 {
+    if (vol.planar) return make_float2(__ldg(planar_field(vol, 0) + e), __ldg(planar_field(vol, 1) + e));
     return __ldg(reinterpret_cast<const float2*>(vol.voxel4 + e));
 }
 
-// Add one observation's terms to voxel e of the pool: (tsdf, weight, red,
-// green) with one 4-wide float reduction into the voxel's 16-byte record,
-// blue with one scalar reduction.  L2 executes a reduction request at about
-// the same rate whether it carries one float or four, so this takes two
-// requests where five separate arrays took five.
+__device__ __forceinline__ void red_add_f32(float* addr, float v)
+{
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
+}
+
+// Add one observation's terms to voxel e of the pool.  Interleaved layout:
+// (tsdf, weight, red, green) with one 4-wide float reduction into the
+// voxel's 16-byte record, blue with one scalar reduction; L2 executes a
+// reduction request at about the same rate whether it carries one float or
+// four, so this takes two requests where the planar layout takes five.
 __device__ __forceinline__ void add_to_voxel(const VolumeView& vol, size_t e, float tsdf,
                                              float weight, float r, float g, float b)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(vol.voxel4 + e),
-                 "f"(tsdf), "f"(weight), "f"(r), "f"(g)
-                 : "memory");
-    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(vol.blue + e), "f"(b) : "memory");
+    if (vol.planar) {
+        red_add_f32(planar_field(vol, 0) + e, tsdf);
+        red_add_f32(planar_field(vol, 1) + e, weight);
+        red_add_f32(planar_field(vol, 2) + e, r);
+        red_add_f32(planar_field(vol, 3) + e, g);
+    } else {
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(vol.voxel4 + e),
+                     "f"(tsdf), "f"(weight), "f"(r), "f"(g)
+                     : "memory");
+    }
+    red_add_f32(vol.blue + e, b);
 }
 
 // Add one band step's samples of a warp (lane: add, voxel e, its terms).

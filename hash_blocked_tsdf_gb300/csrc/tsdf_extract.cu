@@ -294,7 +294,12 @@ __global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const 
         float v[5];
 #pragma unroll
         for (int a = 0; a < 5; ++a) v[a] = src[((size_t)a * n + b) * kBlockVoxels + j];
-        vol.voxel4[e] = make_float4(v[0], v[1], v[2], v[3]);
+        if (vol.planar) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) planar_field(vol, a)[e] = v[a];
+        } else {
+            vol.voxel4[e] = make_float4(v[0], v[1], v[2], v[3]);
+        }
         vol.blue[e] = v[4];
     }
 }

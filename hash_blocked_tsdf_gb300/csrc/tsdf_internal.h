@@ -58,12 +58,16 @@ struct VolumeView {
     Entry* table;
     uint32_t table_mask;        // table_capacity - 1
     uint32_t pool_capacity;
-    // The pool's five sums per voxel, voxel j of block b at index b * 512 + j:
-    // tsdf, weight, red and green interleaved in one 16-byte record (so a
-    // sample reaches them with one 4-wide reduction), blue in an array of
-    // its own.
-    float4* voxel4;             // [pool_capacity][512] (tsdf, weight, red, green)
+    // The pool's five sums per voxel; voxel j of block b is v = b * 512 + j.
+    // Interleaved layout (the default): tsdf, weight, red and green of voxel
+    // v in one 16-byte record voxel4[v] (a sample reaches them with one
+    // 4-wide reduction).  Planar layout (five separate arrays): field k
+    // (tsdf, weight, red, green) of voxel v at float k * plane + v from
+    // voxel4.  Blue is blue[v] in both.
+    float4* voxel4;             // [pool_capacity][512] records, or the planar arrays' base
     float* blue;                // [pool_capacity][512]
+    size_t plane;               // voxels per array: pool_capacity * 512
+    bool planar;                // TSDF_LAYOUT_PLANAR
     uint32_t* pool_counter;     // bump allocator for pool indices
     DeviceCounters* counters;
     DivisorPair div;            // voxel size and truncation, with reciprocals

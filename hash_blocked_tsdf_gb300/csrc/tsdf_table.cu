@@ -7,20 +7,28 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Zero blocks [0, min(*pool_counter, capacity)) of the pool (the voxel
-// records and the blue array).  The count is read on the device, so a reset
-// needs no host round trip.
+// Zero blocks [0, min(*pool_counter, capacity)) of the pool, in either
+// layout.  The count is read on the device, so a reset needs no host round
+// trip.
 __global__ void __launch_bounds__(kThreads) zero_used_blocks_kernel(VolumeView vol)
 {
     const uint32_t used = min(*vol.pool_counter, vol.pool_capacity);
-    const size_t n_rec = (size_t)used * kBlockVoxels;       // 16-byte voxel records
-    const size_t n_blue = n_rec / 4;                         // blue, as float4
+    const size_t n = (size_t)used * (kBlockVoxels / 4);     // float4s per field in use
+    const size_t plane4 = vol.plane / 4;                     // float4s per planar array
+    float4* base = vol.voxel4;
     float4* blue4 = reinterpret_cast<float4*>(vol.blue);
     const float4 z = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
     const size_t stride = (size_t)gridDim.x * kThreads;
-    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < n_rec; e += stride) {
-        vol.voxel4[e] = z;
-        if (e < n_blue) blue4[e] = z;
+    for (size_t e = (size_t)blockIdx.x * kThreads + threadIdx.x; e < n; e += stride) {
+        if (vol.planar) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a) base[(size_t)a * plane4 + e] = z;
+        } else {
+            // the interleaved records of the used blocks: 4 n float4s
+#pragma unroll
+            for (int a = 0; a < 4; ++a) base[4 * e + a] = z;
+        }
+        blue4[e] = z;
     }
 }
 

@@ -44,6 +44,7 @@ struct tsdf_volume {
     bool instrument = false;
     int update_kind = TSDF_UPDATE_PER_SAMPLE;
     int occlusion = TSDF_OCCLUSION_RAY;
+    int layout = TSDF_LAYOUT_INTERLEAVED;
     DivisorPair div = {};
     bool fast_div = false;          // the fixed-divisor division was verified for both divisors
 
@@ -96,8 +97,10 @@ VolumeView view_of(const tsdf_volume* v)
     w.table_mask = v->table_capacity - 1;
     w.pool_capacity = v->pool_capacity;
     const size_t n = array_floats(v);
-    w.voxel4 = reinterpret_cast<float4*>(v->pool);      // n records of 4 floats
+    w.voxel4 = reinterpret_cast<float4*>(v->pool);      // n records, or 4 planar arrays
     w.blue = v->pool + 4 * n;
+    w.plane = n;
+    w.planar = v->layout == TSDF_LAYOUT_PLANAR;
     w.pool_counter = &v->state->pool_counter;
     w.counters = &v->state->counters;
     w.div = v->div;
@@ -367,6 +370,7 @@ int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out)
     out->device = vol->device;
     out->fixed_divisor_fast_path = vol->fast_div ? 1 : 0;
     out->max_frames_per_launch = kMaxBatch;
+    out->pool_layout = vol->layout;
     return TSDF_OK;
 }
 
@@ -374,14 +378,16 @@ int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out)
 {
     if (!vol || !out) return fail(TSDF_ERR_ARG, "null argument");
     const VolumeView w = view_of(vol);
-    float* rec = reinterpret_cast<float*>(w.voxel4);
-    out->tsdf = rec;
-    out->weight = rec + 1;
-    out->r = rec + 2;
-    out->g = rec + 3;
+    float* base = reinterpret_cast<float*>(w.voxel4);
+    // interleaved: field k of voxel v at base + 4 v + k; planar: base + k n + v
+    const size_t step = w.planar ? w.plane : 1;
+    out->tsdf = base;
+    out->weight = base + step;
+    out->r = base + 2 * step;
+    out->g = base + 3 * step;
     out->b = w.blue;
     out->pool_capacity = vol->pool_capacity;
-    out->stride = 4;
+    out->stride = w.planar ? 1 : 4;
     return TSDF_OK;
 }
 
@@ -530,7 +536,16 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
                                   (size_t)count * kBlockVoxels * sizeof(float),
                                   cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(blue)");
     float* dst[4] = {tsdf_out, weight, r, g};
-    if (tsdf_out || weight || r || g) {
+    if (w.planar) {
+        for (int a = 0; a < 4; ++a) {
+            if (!dst[a]) continue;
+            TSDF_CUDA(cudaMemcpyAsync(dst[a],
+                                      reinterpret_cast<float*>(w.voxel4) + a * w.plane +
+                                          (size_t)first * kBlockVoxels,
+                                      (size_t)count * kBlockVoxels * sizeof(float),
+                                      cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(sums)");
+        }
+    } else if (tsdf_out || weight || r || g) {
         // the interleaved records are split into planes on the device, a
         // chunk of blocks at a time, and each plane is copied out whole
         if (!vol->export_scratch)
@@ -706,6 +721,19 @@ int tsdf_set_occlusion(tsdf_volume* vol, int mode)
         return fail(TSDF_ERR_ARG, "occlusion must be TSDF_OCCLUSION_RAY or "
                                   "TSDF_OCCLUSION_REPROJECT");
     vol->occlusion = mode;
+    return TSDF_OK;
+}
+
+int tsdf_set_pool_layout(tsdf_volume* vol, int layout)
+{
+    int rc = check_volume(vol);
+    if (rc) return rc;
+    if (layout != TSDF_LAYOUT_INTERLEAVED && layout != TSDF_LAYOUT_PLANAR)
+        return fail(TSDF_ERR_ARG, "layout must be TSDF_LAYOUT_INTERLEAVED or TSDF_LAYOUT_PLANAR");
+    uint32_t n = 0;
+    if ((rc = tsdf_block_count(vol, nullptr, &n))) return rc;
+    if (n != 0) return fail(TSDF_ERR_ARG, "the pool layout can only change while the volume is empty");
+    vol->layout = layout;
     return TSDF_OK;
 }
 

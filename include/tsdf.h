@@ -40,13 +40,14 @@
  *     key fields); samples outside are counted (out_of_range_samples) and
  *     skipped.
  *   - pool layout: block b's voxel j = lx + 8 * ly + 64 * lz is record
- *     v = b * 512 + j.  Its TSDF, weight, red and green sums are interleaved
- *     in one 16-byte record, floats 4v .. 4v + 3 of the record array; its
- *     blue sum is element v of a separate blue array.  (The pages keep five
- *     separate arrays; the record lets a sample's update reach four of its
- *     five sums with one 4-wide reduction, and L2 executes reduction
- *     requests at about the same rate whether they carry one float or four.)
- *     tsdf_export_blocks returns the five sums as separate arrays.
+ *     v = b * 512 + j.  By default its TSDF, weight, red and green sums are
+ *     interleaved in one 16-byte record, floats 4v .. 4v + 3 of the record
+ *     array, and its blue sum is element v of a separate blue array; the
+ *     pages' five separate arrays are available as TSDF_LAYOUT_PLANAR
+ *     (tsdf_set_pool_layout).  The record lets a sample's update reach four
+ *     of its five sums with one 4-wide reduction, and L2 executes reduction
+ *     requests at about the same rate whether they carry one float or four.
+ *     tsdf_export_blocks returns the five sums as separate arrays in both.
  *
  * Ownership and synchronisation
  *   - A tsdf_volume owns its device memory (table, pool, counters), allocated
@@ -103,13 +104,14 @@ typedef struct tsdf_info {
                                           checked at create to equal IEEE division for
                                           every float32 dividend; 0: IEEE division */
     int32_t max_frames_per_launch;    /* frames a batch call packs into one launch */
+    int32_t pool_layout;              /* TSDF_LAYOUT_INTERLEAVED or TSDF_LAYOUT_PLANAR */
 } tsdf_info;
 
 /* Device pointers to the pool's five sums.  Record v = b * 512 + j (block b,
  * voxel j) holds tsdf[stride * v], weight[stride * v], r[stride * v] and
- * g[stride * v] (the four interleaved: weight = tsdf + 1, r = tsdf + 2,
- * g = tsdf + 3, stride = 4), and b[v].  Each field spans pool_capacity * 512
- * voxels.  They stay valid until tsdf_destroy; reading them races with
+ * g[stride * v], and b[v]: stride 4 in the interleaved layout (weight =
+ * tsdf + 1, r = tsdf + 2, g = tsdf + 3), stride 1 in the planar one (five
+ * separate arrays).  Each field spans pool_capacity * 512 voxels.  They stay valid until tsdf_destroy; reading them races with
  * kernels still running. */
 typedef struct tsdf_pool_view {
     float* tsdf;
@@ -118,7 +120,7 @@ typedef struct tsdf_pool_view {
     float* g;
     float* b;
     uint32_t pool_capacity;
-    uint32_t stride;            /* floats between voxels in tsdf, weight, r, g: 4 */
+    uint32_t stride;            /* floats between voxels in tsdf, weight, r, g: 4 or 1 */
 } tsdf_pool_view;
 
 /* Counters accumulated since create / reset / tsdf_clear_stats. */
@@ -384,6 +386,22 @@ int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 #define TSDF_OCCLUSION_RAY 0
 #define TSDF_OCCLUSION_REPROJECT 1
 int tsdf_set_occlusion(tsdf_volume* vol, int mode);
+
+/* How the pool stores the five sums of a voxel (record v = b * 512 + j):
+ *   TSDF_LAYOUT_INTERLEAVED (the default): TSDF, weight, red and green sums
+ *     in one 16-byte record per voxel, blue in an array of its own; an
+ *     update adds a sample with one 4-wide and one scalar reduction.
+ *   TSDF_LAYOUT_PLANAR: five separate float arrays [pool_capacity][512]
+ *     (the pages' own layout, "design section, data structure"); an update
+ *     adds a sample with five scalar reductions, a row of 8 voxels being one
+ *     32-byte sector of each array.
+ * Every mode and kernel works in both; the sums are the same.  The layout can
+ * only change while the volume holds no block (after create, or after
+ * tsdf_reset; the call synchronises the legacy default stream to check),
+ * else TSDF_ERR_ARG.  tsdf_get_pool reports the layout through its stride. */
+#define TSDF_LAYOUT_INTERLEAVED 0
+#define TSDF_LAYOUT_PLANAR 1
+int tsdf_set_pool_layout(tsdf_volume* vol, int layout);
 
 /* Message of the last failure on the calling thread ("" if none). */
 const char* tsdf_last_error(void);

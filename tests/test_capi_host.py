@@ -73,6 +73,7 @@ def test_calls_on_a_null_volume_are_rejected(lib):
     assert lib.tsdf_integrate_batch(None, 2, 1, 1, 640, 480, K, pose, None) == -1
     assert lib.tsdf_allocate_blocks(None, 1, 4, None) == -1
     assert lib.tsdf_set_occlusion(None, 1) == -1
+    assert lib.tsdf_set_pool_layout(None, 1) == -1
     assert "null" in _err(lib)
 
 

@@ -31,11 +31,13 @@ def _sorted_rows(tris):
     return a[np.lexsort(a.T[::-1])]
 
 
-def _import_oracle(torch, o, voxel, trunc, pool=None):
+def _import_oracle(torch, o, voxel, trunc, pool=None, layout=None):
     from hash_blocked_tsdf_gb300 import TsdfVolume
     e = o.export()
     n = len(e["coords"])
     vol = TsdfVolume(pool or max(4096, 2 * n), voxel, trunc)
+    if layout is not None:
+        vol.set_pool_layout(layout)
     vol.import_blocks(e["coords"], *(e[k].astype(np.float32) for k in ("tsdf", "weight", "r",
                                                                           "g", "b")))
     return vol, e
@@ -48,11 +50,12 @@ def _assert_same_triangles(gpu, oracle_tris):
     np.testing.assert_array_equal(g, o)
 
 
-def test_import_round_trip(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("layout", ["interleaved", "planar"])
+def test_import_round_trip(torch_cuda, oracle_mod, layout):
     f = scenes.tiny_sphere_plane()
     o = oracle_mod.OracleVolume(f.voxel_size, f.trunc)
     o.integrate_frames(f)
-    vol, e = _import_oracle(torch_cuda, o, f.voxel_size, f.trunc)
+    vol, e = _import_oracle(torch_cuda, o, f.voxel_size, f.trunc, layout=layout)
     g = vol.export_blocks()
     order = np.lexsort((g["coords"][:, 2], g["coords"][:, 1], g["coords"][:, 0]))
     np.testing.assert_array_equal(g["coords"][order], e["coords"])
@@ -61,11 +64,12 @@ def test_import_round_trip(torch_cuda, oracle_mod):
     vol.close()
 
 
-def test_extract_equals_oracle_on_the_sphere_scene(torch_cuda, oracle_mod):
+@pytest.mark.parametrize("layout", ["interleaved", "planar"])
+def test_extract_equals_oracle_on_the_sphere_scene(torch_cuda, oracle_mod, layout):
     f = scenes.tiny_sphere_plane()
     o = oracle_mod.OracleVolume(f.voxel_size, f.trunc)
     o.integrate_frames(f)
-    vol, _ = _import_oracle(torch_cuda, o, f.voxel_size, f.trunc)
+    vol, _ = _import_oracle(torch_cuda, o, f.voxel_size, f.trunc, layout=layout)
     tris = vol.extract_triangles()
     assert len(tris) > 50000
     _assert_same_triangles(tris, o.extract())

@@ -47,8 +47,10 @@ def _oracle(oracle_mod, frames, block_limit=-1):
     return o
 
 
-def _full_parity(torch, oracle_mod, frames, strict, batch=True, kernel=None):
+def _full_parity(torch, oracle_mod, frames, strict, batch=True, kernel=None, layout=None):
     vol = _gpu_volume(torch, frames)
+    if layout is not None:
+        vol.set_pool_layout(layout)
     if kernel is not None:
         vol.set_update_kernel(kernel)
     _integrate_gpu(torch, frames, vol, batch)
@@ -230,27 +232,37 @@ def test_host_batch_matches_device_batch(torch_cuda, oracle_mod):
     b.close()
 
 
-def test_pool_view_matches_export(torch_cuda):
+@pytest.mark.parametrize("layout", ["interleaved", "planar"])
+def test_pool_view_matches_export(torch_cuda, layout):
     """The zero-copy pool view: tsdf, weight, r and g interleaved per voxel
-    (stride 4), blue plain; the same numbers as the export's separate arrays."""
+    (stride 4) or planar (stride 1), blue plain; the same numbers as the
+    export's separate arrays."""
     from hash_blocked_tsdf_gb300 import binding
     torch = torch_cuda
     frames = scenes.tiny_sphere_plane()
     vol = _gpu_volume(torch, frames)
+    vol.set_pool_layout(layout)
+    assert vol.info["pool_layout"] == binding.POOL_LAYOUTS[layout]
     _integrate_gpu(torch, frames, vol)
     n = vol.block_count()
     g = vol.export_blocks()
     p = binding.tsdf_get_pool(vol.handle)
     cap = p["pool_capacity"]
-    assert p["stride"] == 4
-    assert (p["weight"] - p["tsdf"], p["r"] - p["tsdf"], p["g"] - p["tsdf"]) == (4, 8, 12)
+    step = 4 if layout == "interleaved" else 4 * cap * 512    # bytes between fields
+    assert p["stride"] == (4 if layout == "interleaved" else 1)
+    assert (p["weight"] - p["tsdf"], p["r"] - p["tsdf"], p["g"] - p["tsdf"]) == \
+        (step, 2 * step, 3 * step)
 
     class _View:
         def __init__(self, ptr, count):
             self.__cuda_array_interface__ = {"shape": (count,), "typestr": "<f4",
                                              "data": (ptr, False), "version": 3,
                                              "strides": None}
-    rec = torch.as_tensor(_View(p["tsdf"], cap * 512 * 4), device="cuda").view(cap, 512, 4)
+    if layout == "interleaved":
+        rec = torch.as_tensor(_View(p["tsdf"], cap * 512 * 4), device="cuda").view(cap, 512, 4)
+    else:
+        rec = torch.as_tensor(_View(p["tsdf"], 4 * cap * 512), device="cuda").view(
+            4, cap, 512).permute(1, 2, 0)
     blue = torch.as_tensor(_View(p["b"], cap * 512), device="cuda").view(cap, 512)
     for k, key in enumerate(("tsdf", "weight", "r", "g")):
         np.testing.assert_array_equal(rec[:n, :, k].cpu().numpy(), g[key])
@@ -260,6 +272,33 @@ def test_pool_view_matches_export(torch_cuda):
     part = vol.export_blocks(first=n // 3, count=n // 2)
     for key in ("tsdf", "weight", "r", "g", "b"):
         np.testing.assert_array_equal(part[key], g[key][n // 3:n // 3 + n // 2])
+    vol.close()
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_planar_layout_parity(torch_cuda, oracle_mod, kernel):
+    # the pages' five separate arrays, under every update mode: same sums
+    _full_parity(torch_cuda, oracle_mod, scenes.tiny_sphere_plane(), strict=True, kernel=kernel,
+                 layout="planar")
+    _full_parity(torch_cuda, oracle_mod, scenes.orbit_trajectory(n_frames=100, frames=(0, 8)),
+                 strict=False, kernel=kernel, layout="planar")
+
+
+def test_pool_layout_changes_only_while_empty(torch_cuda, oracle_mod):
+    from hash_blocked_tsdf_gb300 import TsdfError
+    torch = torch_cuda
+    frames = scenes.tiny_sphere_plane()
+    vol = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, vol)
+    with pytest.raises(TsdfError):
+        vol.set_pool_layout("planar")
+    with pytest.raises(KeyError):
+        vol.set_pool_layout("tiled")
+    vol.reset()
+    vol.set_pool_layout("planar")             # empty again: allowed
+    _integrate_gpu(torch, frames, vol)
+    o = _oracle(oracle_mod, frames)
+    parity.compare_volume(vol.export_blocks(), o.export(), strict=True)
     vol.close()
 
 

@@ -24,13 +24,15 @@ def torch_cuda():
     return torch
 
 
-def _run(torch, oracle_mod, frames, strict, kernel=None, batch=True, modes=None):
+def _run(torch, oracle_mod, frames, strict, kernel=None, batch=True, modes=None, layout=None):
     """Integrate `frames` on the GPU and in the oracle; modes[f] is the
     occlusion test of frame f (default: reprojection for every frame)."""
     from hash_blocked_tsdf_gb300 import TsdfVolume
     modes = modes or ["reproject"] * frames.n_frames
     vol = TsdfVolume(frames.pool_capacity, frames.voxel_size, frames.trunc,
                      frames.table_capacity)
+    if layout is not None:
+        vol.set_pool_layout(layout)
     if kernel is not None:
         vol.set_update_kernel(kernel)
     d = torch.from_numpy(frames.depth).cuda()
@@ -81,8 +83,9 @@ def test_reproject_tiny_sphere_plane(torch_cuda, oracle_mod, kernel):
     assert rep["blocks"] > 500
 
 
-def test_reproject_slanted_step_rotated(torch_cuda, oracle_mod):
-    _run(torch_cuda, oracle_mod, _slanted_step(), strict=True)
+@pytest.mark.parametrize("layout", ["interleaved", "planar"])
+def test_reproject_slanted_step_rotated(torch_cuda, oracle_mod, layout):
+    _run(torch_cuda, oracle_mod, _slanted_step(), strict=True, layout=layout)
 
 
 def test_reproject_vga_sphere_plane(torch_cuda, oracle_mod):
