@@ -27,7 +27,9 @@
  *     z forward; pose = camera-to-world [R | t], R row-major;
  *   - the band is walked along the unit ray through the observed point, in
  *     steps of one voxel, S = 2k + 1 samples at offsets (i - k) * voxel with
- *     k = round(trunc / voxel);
+ *     k = round(trunc / voxel); evaluated in voxel units: per pixel the
+ *     observed point p' = (R p + t) / voxel and the world direction e = R dir,
+ *     per sample p' + j e (j = i - k), whose floor is the voxel;
  *   - projective signed distance at the voxel centre: sdf = d - z_c, where z_c
  *     is the camera-frame depth of the centre and d the pixel's depth;
  *   - occlusion test: z_c > 0 and sdf >= -trunc;
@@ -140,26 +142,35 @@ int32_t floor_div8(int32_t a)
 #endif
 }
 
-/* One sample of the truncation band: the point on the unit ray at signed
- * offset `off` from the observed point p, its voxel, and the truncated
- * signed distance at that voxel's centre. */
-SampleStatus band_sample(const Camera& cam, float voxel, float trunc, float d,
-                         float px, float py, float pz, float dx, float dy, float dz,
-                         float off, Sample* s)
+/* The part of the band walk shared by a pixel's samples: the observed point
+ * in world coordinates divided by the voxel edge, p' = (R p + t) / voxel, and
+ * the unit ray direction in world coordinates, e = R dir.  Sample i lies at
+ * p + i voxel dir, i.e. at p' + i e in voxel units. */
+struct WalkRay {
+    float d;              // the pixel's depth
+    float vx, vy, vz;     // p'
+    float ex, ey, ez;     // e
+    float pz, dz;         // camera-frame z of p and of dir (planted mistake 1 only)
+};
+
+/* One sample of the truncation band: band step i (offset i voxels from the
+ * observed point along the unit ray), its voxel, and the truncated signed
+ * distance at that voxel's centre. */
+SampleStatus band_sample(const Camera& cam, float voxel, float trunc, const WalkRay& r, int i,
+                         Sample* s)
 {
-    // sample point, camera frame
-    float sx = px + off * dx;
-    float sy = py + off * dy;
-    float sz = pz + off * dz;
-    // to the world frame: w = R s + t
-    float wx = ((cam.R[0][0] * sx + cam.R[0][1] * sy) + cam.R[0][2] * sz) + cam.t[0];
-    float wy = ((cam.R[1][0] * sx + cam.R[1][1] * sy) + cam.R[1][2] * sz) + cam.t[1];
-    float wz = ((cam.R[2][0] * sx + cam.R[2][1] * sy) + cam.R[2][2] * sz) + cam.t[2];
-    // voxel index = floor(w / voxel), kept inside the packable block range
+    const float d = r.d;
+    // the sample in voxel units: p' + i e
+    float fi = (float)i;
+    float wx = r.vx + fi * r.ex;
+    float wy = r.vy + fi * r.ey;
+    float wz = r.vz + fi * r.ez;
+    // voxel index = floor of the sample in voxel units, kept inside the
+    // packable block range
 #if ORACLE_MUTANT == 8
-    float qx = std::trunc(wx / voxel), qy = std::trunc(wy / voxel), qz = std::trunc(wz / voxel);
+    float qx = std::trunc(wx), qy = std::trunc(wy), qz = std::trunc(wz);   // planted
 #else
-    float qx = std::floor(wx / voxel), qy = std::floor(wy / voxel), qz = std::floor(wz / voxel);
+    float qx = std::floor(wx), qy = std::floor(wy), qz = std::floor(wz);
 #endif
     const float lo = (float)kCoordMin * kEdge;           // -2^23
     const float hi = (float)(kCoordMax * kEdge + (kEdge - 1));  // 2^23 - 1
@@ -186,7 +197,7 @@ SampleStatus band_sample(const Camera& cam, float voxel, float trunc, float d,
 #endif
     // projective signed distance at the centre (positive in front of the surface)
 #if ORACLE_MUTANT == 1
-    float sdf = d - sz;                     // planted: distance at the sample, not the centre
+    float sdf = d - (r.pz + ((float)i * voxel) * r.dz);   // planted: at the sample, not the centre
 #elif ORACLE_MUTANT == 2
     float sdf = zc - d;                     // planted: sign flipped
 #else
@@ -281,15 +292,27 @@ bool walk_pixel(const Camera& cam, float voxel, float trunc, int band_half,
 #else
     float dx = xn / len, dy = yn / len, dz = 1.0f / len;
 #endif
+    // the observed point and the direction in world coordinates, the point
+    // in voxel units: p' = (R p + t) / voxel, e = R dir (rows of R summed
+    // left to right)
+    WalkRay r;
+    r.d = d;
+    r.vx = (((cam.R[0][0] * px + cam.R[0][1] * py) + cam.R[0][2] * pz) + cam.t[0]) / voxel;
+    r.vy = (((cam.R[1][0] * px + cam.R[1][1] * py) + cam.R[1][2] * pz) + cam.t[1]) / voxel;
+    r.vz = (((cam.R[2][0] * px + cam.R[2][1] * py) + cam.R[2][2] * pz) + cam.t[2]) / voxel;
+    r.ex = (cam.R[0][0] * dx + cam.R[0][1] * dy) + cam.R[0][2] * dz;
+    r.ey = (cam.R[1][0] * dx + cam.R[1][1] * dy) + cam.R[1][2] * dz;
+    r.ez = (cam.R[2][0] * dx + cam.R[2][1] * dy) + cam.R[2][2] * dz;
+    r.pz = pz;
+    r.dz = dz;
 #if ORACLE_MUTANT == 13
     int steps_half = band_half + 1;         // planted: band one voxel too wide
 #else
     int steps_half = band_half;
 #endif
     for (int i = -steps_half; i <= steps_half; ++i) {
-        float off = (float)i * voxel;
         Sample s;
-        SampleStatus st = band_sample(cam, voxel, trunc, d, px, py, pz, dx, dy, dz, off, &s);
+        SampleStatus st = band_sample(cam, voxel, trunc, r, i, &s);
         visit(st, s);
     }
     return true;

@@ -20,7 +20,9 @@ def dense_bruteforce(depth, rgb, K, pose, voxel, trunc):
     """Dense-grid integration of one frame, vectorised over pixels.
 
     Walks the same band samples as the method (float32, one rounding per
-    operation, in the same order) but accumulates straight into a dense
+    operation, in the same order: per pixel the observed point in voxel
+    units and the world direction, per sample their combination) but
+    accumulates straight into a dense
     voxel grid with np.add.at in float64, with no blocks and no hash map.
     Returns (origin[3] int, dict of dense float64 arrays weight/tsdf/r/g/b,
     n_passing).
@@ -45,12 +47,12 @@ def dense_bruteforce(depth, rgb, K, pose, voxel, trunc):
     px, py, pz = xn * d, yn * d, d
     ln = np.sqrt((xn * xn + yn * yn) + F32(1))
     dx, dy, dz = xn / ln, yn / ln, F32(1) / ln
+    # the observed point in voxel units and the world direction, per pixel
+    pv = [(((R[a, 0] * px + R[a, 1] * py) + R[a, 2] * pz) + t[a]) / v for a in range(3)]
+    e = [(R[a, 0] * dx + R[a, 1] * dy) + R[a, 2] * dz for a in range(3)]
     idx_l, val_l, col_l = [], [], []
     for i in range(-k, k + 1):
-        off = F32(i) * v
-        sx, sy, sz = px + off * dx, py + off * dy, pz + off * dz
-        w = [((R[a, 0] * sx + R[a, 1] * sy) + R[a, 2] * sz) + t[a] for a in range(3)]
-        q = [np.floor(wa / v) for wa in w]
+        q = [np.floor(pv[a] + F32(i) * e[a]) for a in range(3)]
         ok = np.ones(q[0].shape, dtype=bool)
         for qa in q:
             ok &= (qa >= F32(-8388608.0)) & (qa <= F32(8388607.0))
