@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
     if (pix < n_pix) {
         const int v = pix / fb.width;
         const int u = pix - v * fb.width;
-        valid = back_project(cam, u, v, __ldg(depth + pix), p);
+        valid = back_project(cam, vol.div, u, v, __ldg(depth + pix), p);
     }
     const int steps = 2 * vol.band_half + 1;
     unsigned long long last = kEmptyKey;
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
-        valid = back_project(cam, u, v, depth, p);
+        valid = back_project(cam, vol.div, u, v, depth, p);
         if (valid) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);

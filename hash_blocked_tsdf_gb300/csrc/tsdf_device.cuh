@@ -19,12 +19,14 @@ namespace tsdf {
 
 enum SampleStatus { kSamplePass = 0, kSampleOccluded = 1, kSampleOutOfRange = 2 };
 
-// A valid pixel's back-projected point p = d * (xn, yn, 1) and the unit ray
-// direction through it.
+// What the band walk of a valid pixel needs: its depth d, the back-projected
+// point p = d (xn, yn, 1) moved to the world and divided by the voxel edge,
+// p' = (R p + t) / voxel, and the unit ray direction in world coordinates,
+// e = R dir.  Band step j lies at p' + j e in voxel units.
 struct RayPoint {
     float d;
-    float px, py, pz;
-    float dx, dy, dz;
+    float vx, vy, vz;       // p'
+    float ex, ey, ez;       // e
 };
 
 struct VoxelSample {
@@ -32,51 +34,53 @@ struct VoxelSample {
     float tsdf;         // min(1, sdf / trunc)
 };
 
-__device__ __forceinline__ bool back_project(const Camera& c, int u, int v, float d,
-                                             RayPoint& p)
+__device__ __forceinline__ bool back_project(const Camera& c, const DivisorPair& dv, int u, int v,
+                                             float d, RayPoint& p)
 {
     if (!(isfinite(d) && d > 0.0f)) return false;
     const float xn = __fdiv_rn(__fsub_rn((float)u, c.cx), c.fx);
     const float yn = __fdiv_rn(__fsub_rn((float)v, c.cy), c.fy);
-    p.d = d;
-    p.px = __fmul_rn(xn, d);
-    p.py = __fmul_rn(yn, d);
-    p.pz = d;
+    const float px = __fmul_rn(xn, d);
+    const float py = __fmul_rn(yn, d);
+    const float pz = d;
     const float len = __fsqrt_rn(__fadd_rn(__fadd_rn(__fmul_rn(xn, xn), __fmul_rn(yn, yn)), 1.0f));
-    p.dx = __fdiv_rn(xn, len);
-    p.dy = __fdiv_rn(yn, len);
-    p.dz = __fdiv_rn(1.0f, len);
+    const float dx = __fdiv_rn(xn, len);
+    const float dy = __fdiv_rn(yn, len);
+    const float dz = __fdiv_rn(1.0f, len);
+    // rows of R summed left to right, then t; one IEEE division per axis
+    p.d = d;
+    p.vx = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r00, px), __fmul_rn(c.r01, py)),
+                                         __fmul_rn(c.r02, pz)), c.tx), dv.voxel);
+    p.vy = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r10, px), __fmul_rn(c.r11, py)),
+                                         __fmul_rn(c.r12, pz)), c.ty), dv.voxel);
+    p.vz = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, px), __fmul_rn(c.r21, py)),
+                                         __fmul_rn(c.r22, pz)), c.tz), dv.voxel);
+    p.ex = __fadd_rn(__fadd_rn(__fmul_rn(c.r00, dx), __fmul_rn(c.r01, dy)), __fmul_rn(c.r02, dz));
+    p.ey = __fadd_rn(__fadd_rn(__fmul_rn(c.r10, dx), __fmul_rn(c.r11, dy)), __fmul_rn(c.r12, dz));
+    p.ez = __fadd_rn(__fadd_rn(__fmul_rn(c.r20, dx), __fmul_rn(c.r21, dy)), __fmul_rn(c.r22, dz));
     return true;
 }
 
 // A pixel holds an observation when its depth is finite and positive.
 __device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
 
-// Division by a divisor y that is fixed for the whole volume (the voxel size
-// or the truncation distance), given r = RN(1 / y): Markstein's
+// Division by a divisor y that is fixed for the whole volume (the
+// truncation distance), given r = RN(1 / y): Markstein's
 // reciprocal-and-correction scheme (P. Markstein, "Computation of elementary
 // functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
 // 1990): q0 = RN(x r) is within an ulp of x / y, the residual x - q0 y is
 // exact in one fused multiply-add, and one more fused multiply-add rounds
 // q0 + r (x - q0 y) to the correctly rounded quotient.  At volume creation the
 // host has the GPU check, for every one of the 2^32 float32 bit patterns x,
-// that what the walk makes of the quotient is the same as with IEEE
-// division: floor(x / voxel) and whether it is a packable voxel index, and
-// min(1, x / trunc) for every x >= -trunc.  Only then is the scheme used.
+// that min(1, x / trunc) comes out the same as with IEEE division for every
+// x >= -trunc (the only dividends the walk divides).  Only then is the
+// scheme used.  (The walk divides by the voxel edge once per pixel, with
+// IEEE division.)
 __device__ __forceinline__ float div_fixed(float x, float y, float r)
 {
     const float q0 = __fmul_rn(x, r);
     const float e = __fmaf_rn(-q0, y, x);
     return __fmaf_rn(e, r, q0);
-}
-
-// floor(x / voxel) as the walk uses it (checked exhaustively: same floored
-// value and same range decision as IEEE division for every float32 x).
-template <bool kFast>
-__device__ __forceinline__ float div_voxel(float x, float y, float r)
-{
-    if (kFast) return div_fixed(x, y, r);
-    return __fdiv_rn(x, y);
 }
 
 // x / trunc as the walk uses it (checked exhaustively for x >= -trunc).  The
@@ -114,28 +118,18 @@ __device__ __forceinline__ float truncated_sdf(const DivisorPair& dv, float d, f
     return fminf(1.0f, div_trunc<kFast>(__fsub_rn(d, zc), dv.trunc, dv.inv_trunc));
 }
 
-// The voxel of band sample `i` (offset i * voxel along the unit ray, i in
-// -k..k), and whether its index lies in the packable range.  Out-of-range
-// indices are clamped before the integer conversion and never used.
+// The voxel of band sample `i` (offset i voxels along the unit ray, i in
+// -k..k): the floor of p' + i e, and whether it lies in the packable range.
+// Out-of-range indices are clamped before the integer conversion and never
+// used.
 template <bool kFast>
 __device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
                                            const RayPoint& p, int i, VoxelSample& s)
 {
-    const float voxel = dv.voxel;
-    const float off = __fmul_rn((float)i, voxel);
-    const float sx = __fadd_rn(p.px, __fmul_rn(off, p.dx));
-    const float sy = __fadd_rn(p.py, __fmul_rn(off, p.dy));
-    const float sz = __fadd_rn(p.pz, __fmul_rn(off, p.dz));
-    // world = R s + t, summed left to right
-    const float wx = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r00, sx), __fmul_rn(c.r01, sy)),
-                                         __fmul_rn(c.r02, sz)), c.tx);
-    const float wy = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r10, sx), __fmul_rn(c.r11, sy)),
-                                         __fmul_rn(c.r12, sz)), c.ty);
-    const float wz = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, sx), __fmul_rn(c.r21, sy)),
-                                         __fmul_rn(c.r22, sz)), c.tz);
-    const float qx = floorf(div_voxel<kFast>(wx, voxel, dv.inv_voxel));
-    const float qy = floorf(div_voxel<kFast>(wy, voxel, dv.inv_voxel));
-    const float qz = floorf(div_voxel<kFast>(wz, voxel, dv.inv_voxel));
+    const float fi = (float)i;
+    const float qx = floorf(__fadd_rn(p.vx, __fmul_rn(fi, p.ex)));
+    const float qy = floorf(__fadd_rn(p.vy, __fmul_rn(fi, p.ey)));
+    const float qz = floorf(__fadd_rn(p.vz, __fmul_rn(fi, p.ez)));
     const bool in_range = qx >= kVoxelIndexMin && qx <= kVoxelIndexMax &&
                           qy >= kVoxelIndexMin && qy <= kVoxelIndexMax &&
                           qz >= kVoxelIndexMin && qz <= kVoxelIndexMax;

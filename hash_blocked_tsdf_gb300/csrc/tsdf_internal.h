@@ -119,12 +119,11 @@ cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords,
 // With the reprojection occlusion test every kind runs the per-sample kernel.
 cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
                           cudaStream_t stream);
-// Count the float32 x (all 2^32 bit patterns) for which the walk's use of the
-// fixed-divisor quotient differs from its use of the IEEE quotient x / y
-// (role 0: floored voxel index and range decision; role 1: min(1, x / y) for
-// x >= -y); result added to *mismatches.
-cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int role,
-                                        unsigned long long* mismatches, cudaStream_t stream);
+// Count the float32 x >= -y (all 2^32 bit patterns tried) for which
+// min(1, x / y) with the fixed-divisor quotient differs from the IEEE one;
+// result added to *mismatches.
+cudaError_t launch_verify_fixed_divisor(float y, float inv_y, unsigned long long* mismatches,
+                                        cudaStream_t stream);
 cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 // Marching tetrahedra over blocks [0, n_blocks) (coords[idx] = coordinate of
 // pool index idx); triangles past `capacity` are counted, not written.

@@ -57,30 +57,19 @@ __global__ void __launch_bounds__(kThreads) export_coords_kernel(VolumeView vol,
     unpack_block(e.key, coords + 3 * (size_t)e.idx);
 }
 
-// Every float32 bit pattern x: does the walk's use of x / y come out the same
-// with div_fixed as with IEEE division?  role 0 (y = voxel size): the floored
-// quotient and whether it lies in the packable voxel-index range; role 1
-// (y = truncation): min(1, x / y) for every x >= -y (no other x reaches that
-// division), compared as numbers.
+// Every float32 bit pattern x >= -y: does min(1, x / y) come out the same
+// with div_fixed as with IEEE division (y the truncation distance)?
 __global__ void __launch_bounds__(kThreads) verify_fixed_divisor_kernel(
-    float y, float r, int role, unsigned long long* mismatches)
+    float y, float r, unsigned long long* mismatches)
 {
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     uint32_t bad = 0;
     for (uint64_t b = (uint64_t)blockIdx.x * kThreads + threadIdx.x; b < (1ull << 32);
          b += stride) {
         const float x = __uint_as_float((uint32_t)b);
-        const float fast = role == 0 ? div_voxel<true>(x, y, r) : div_trunc<true>(x, y, r);
+        const float fast = div_trunc<true>(x, y, r);
         const float ieee = __fdiv_rn(x, y);
-        bool same;
-        if (role == 0) {
-            const float a = floorf(fast), c = floorf(ieee);
-            const bool ina = a >= kVoxelIndexMin && a <= kVoxelIndexMax;
-            const bool inc = c >= kVoxelIndexMin && c <= kVoxelIndexMax;
-            same = ina == inc && (!ina || a == c);
-        } else {
-            same = !(x >= -y) || fminf(1.0f, fast) == fminf(1.0f, ieee);
-        }
+        const bool same = !(x >= -y) || fminf(1.0f, fast) == fminf(1.0f, ieee);
         bad += same ? 0u : 1u;
     }
     bad = __reduce_add_sync(0xFFFFFFFFu, bad);
@@ -89,14 +78,14 @@ __global__ void __launch_bounds__(kThreads) verify_fixed_divisor_kernel(
 
 }  // namespace
 
-cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int role,
-                                        unsigned long long* mismatches, cudaStream_t stream)
+cudaError_t launch_verify_fixed_divisor(float y, float inv_y, unsigned long long* mismatches,
+                                        cudaStream_t stream)
 {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
-    verify_fixed_divisor_kernel<<<(unsigned)(sms * 16), kThreads, 0, stream>>>(y, inv_y, role,
+    verify_fixed_divisor_kernel<<<(unsigned)(sms * 16), kThreads, 0, stream>>>(y, inv_y,
                                                                               mismatches);
     return cudaGetLastError();
 }

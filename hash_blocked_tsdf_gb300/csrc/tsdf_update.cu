@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
-        valid = back_project(cam, u, v, depth, p);
+        valid = back_project(cam, vol.div, u, v, depth, p);
         if (valid && !kReproject) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);
@@ -173,7 +173,7 @@ constexpr int kRowWords = 8 * kCellWords + 4;         // + 4 words to spread the
 constexpr int kRowMaxProbe = 32;
 constexpr uint32_t kNoRow = 0xFFFFFFFFu;
 // Per-pixel fields in shared memory, [field][64].
-enum PixField { kPxValid = 0, kPxD, kPxPx, kPxPy, kPxPz, kPxDx, kPxDy, kPxDz, kPxR, kPxG, kPxB,
+enum PixField { kPxValid = 0, kPxD, kPxVx, kPxVy, kPxVz, kPxEx, kPxEy, kPxEz, kPxR, kPxG, kPxB,
                 kPxFields };
 // Shared layout in 32-bit words (offsets keep the 64-bit block keys 8-byte
 // aligned and the sums 16-byte aligned).
@@ -247,7 +247,7 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
         float c[3] = {0.0f, 0.0f, 0.0f};
         if (u < fb.width && v < fb.height) {
             const size_t pix = (size_t)v * fb.width + u;
-            valid = back_project(cam, u, v, __ldg(fb.frame[f].depth + pix), p);
+            valid = back_project(cam, vol.div, u, v, __ldg(fb.frame[f].depth + pix), p);
             if (valid) {
                 const float* rgb = fb.frame[f].rgb;
                 c[0] = __ldg(rgb + 3 * pix);
@@ -257,12 +257,12 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
         }
         s_pix[kPxValid * kRowPix + t] = valid ? 1u : 0u;
         s_pixf[kPxD * kRowPix + t] = p.d;
-        s_pixf[kPxPx * kRowPix + t] = p.px;
-        s_pixf[kPxPy * kRowPix + t] = p.py;
-        s_pixf[kPxPz * kRowPix + t] = p.pz;
-        s_pixf[kPxDx * kRowPix + t] = p.dx;
-        s_pixf[kPxDy * kRowPix + t] = p.dy;
-        s_pixf[kPxDz * kRowPix + t] = p.dz;
+        s_pixf[kPxVx * kRowPix + t] = p.vx;
+        s_pixf[kPxVy * kRowPix + t] = p.vy;
+        s_pixf[kPxVz * kRowPix + t] = p.vz;
+        s_pixf[kPxEx * kRowPix + t] = p.ex;
+        s_pixf[kPxEy * kRowPix + t] = p.ey;
+        s_pixf[kPxEz * kRowPix + t] = p.ez;
         s_pixf[kPxR * kRowPix + t] = c[0];
         s_pixf[kPxG * kRowPix + t] = c[1];
         s_pixf[kPxB * kRowPix + t] = c[2];
@@ -284,12 +284,12 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
     const bool valid = s_pix[kPxValid * kRowPix + q] != 0;
     RayPoint p;
     p.d = s_pixf[kPxD * kRowPix + q];
-    p.px = s_pixf[kPxPx * kRowPix + q];
-    p.py = s_pixf[kPxPy * kRowPix + q];
-    p.pz = s_pixf[kPxPz * kRowPix + q];
-    p.dx = s_pixf[kPxDx * kRowPix + q];
-    p.dy = s_pixf[kPxDy * kRowPix + q];
-    p.dz = s_pixf[kPxDz * kRowPix + q];
+    p.vx = s_pixf[kPxVx * kRowPix + q];
+    p.vy = s_pixf[kPxVy * kRowPix + q];
+    p.vz = s_pixf[kPxVz * kRowPix + q];
+    p.ex = s_pixf[kPxEx * kRowPix + q];
+    p.ey = s_pixf[kPxEy * kRowPix + q];
+    p.ez = s_pixf[kPxEz * kRowPix + q];
     const uint32_t bit = 1u << (q & 31);
     const int half_word = q >> 5;
     unsigned long long last = kEmptyKey;

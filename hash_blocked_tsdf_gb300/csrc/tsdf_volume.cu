@@ -46,7 +46,7 @@ struct tsdf_volume {
     int occlusion = TSDF_OCCLUSION_RAY;
     int layout = TSDF_LAYOUT_INTERLEAVED;
     DivisorPair div = {};
-    bool fast_div = false;          // the fixed-divisor division was verified for both divisors
+    bool fast_div = false;          // the fixed-divisor division by trunc was verified
 
     Entry* table = nullptr;
     uint32_t* dense_list = nullptr;  // [kDenseListCapacity] adaptive update's dense tiles
@@ -257,22 +257,19 @@ int one_frame(tsdf_volume* v, const float* depth, const float* rgb, int width, i
                          as_stream(stream));
 }
 
-// Check, for every float32 dividend, that the walk makes the same decisions
-// and values with the fixed-divisor division as with IEEE division, for both
-// of the volume's divisors.
+// Check, for every float32 dividend, that the walk's truncated distances come
+// out the same with the fixed-divisor division as with IEEE division.
 int verify_divisors(tsdf_volume* v)
 {
     unsigned long long* bad = &v->state->counters.reserved[0];
-    TSDF_CUDA(cudaMemsetAsync(bad, 0, 2 * sizeof(unsigned long long), 0), "cudaMemsetAsync");
-    TSDF_CUDA(launch_verify_fixed_divisor(v->div.voxel, v->div.inv_voxel, 0, bad, 0),
+    TSDF_CUDA(cudaMemsetAsync(bad, 0, sizeof(unsigned long long), 0), "cudaMemsetAsync");
+    TSDF_CUDA(launch_verify_fixed_divisor(v->div.trunc, v->div.inv_trunc, bad, 0),
               "verify kernel");
-    TSDF_CUDA(launch_verify_fixed_divisor(v->div.trunc, v->div.inv_trunc, 1, bad + 1, 0),
-              "verify kernel");
-    unsigned long long h[2] = {1, 1};
-    TSDF_CUDA(cudaMemcpyAsync(h, bad, sizeof(h), cudaMemcpyDeviceToHost, 0), "cudaMemcpyAsync");
-    TSDF_CUDA(cudaMemsetAsync(bad, 0, 2 * sizeof(unsigned long long), 0), "cudaMemsetAsync");
+    unsigned long long h = 1;
+    TSDF_CUDA(cudaMemcpyAsync(&h, bad, sizeof(h), cudaMemcpyDeviceToHost, 0), "cudaMemcpyAsync");
+    TSDF_CUDA(cudaMemsetAsync(bad, 0, sizeof(unsigned long long), 0), "cudaMemsetAsync");
     TSDF_CUDA(cudaStreamSynchronize(0), "cudaStreamSynchronize");
-    v->fast_div = h[0] == 0 && h[1] == 0;
+    v->fast_div = h == 0;
     return TSDF_OK;
 }
 

@@ -99,10 +99,11 @@ typedef struct tsdf_info {
     float trunc;                /* metres */
     int32_t band_samples;       /* samples per point, 2k + 1 */
     int32_t device;             /* CUDA device ordinal that owns the memory */
-    int32_t fixed_divisor_fast_path;  /* 1: divisions by voxel_size and trunc use a
+    int32_t fixed_divisor_fast_path;  /* 1: the per-sample division by trunc uses a
                                           reciprocal-and-correction sequence that was
-                                          checked at create to equal IEEE division for
-                                          every float32 dividend; 0: IEEE division */
+                                          checked at create to give the same truncated
+                                          distance as IEEE division for every float32
+                                          dividend; 0: IEEE division */
     int32_t max_frames_per_launch;    /* frames a batch call packs into one launch */
     int32_t pool_layout;              /* TSDF_LAYOUT_INTERLEAVED or TSDF_LAYOUT_PLANAR */
 } tsdf_info;
