@@ -676,6 +676,8 @@ def run_ours(args):
     if args.occlusion == "reproject":
         upd_kernel = "update_kernel (reprojection test)"
     mode = args.update_kernel if args.occlusion == "ray" else "reproject"
+    if args.layout == "planar":
+        mode += "_planar"
     prof_upd = _profile_record(f"update_{mode}_room_walk_1280x720.md",
                                ["tsdf_update.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     prof_alloc = _profile_record("allocate_kernel_room_walk_1280x720.md"
