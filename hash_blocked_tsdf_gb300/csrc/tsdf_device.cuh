@@ -420,18 +420,18 @@ __device__ __forceinline__ void warp_add_samples(const VolumeView& vol, float4* 
 }
 
 
-// Where to pre-reduce (adaptive mode).  A 16 x 16 pixel tile is dense when
-// at least half of its valid pixels (finite depth > 0) see a voxel edge at
-// least w pixels wide (voxel * fx >= w * depth): there samples crowd into few
-// voxels and summing them on chip pays; below, they rarely share a voxel and
-// direct additions are cheaper.  Measured on GB300 the crossing lies near 5
-// pixels for launches of several frames (the frames' samples of a voxel
-// meet in L2 as well) and near 10 for a single frame.  The kernels that add
-// samples one by one (the per-sample update kernel and the fused integrate
-// kernel) apply this rule to their 16 x 16 tiles and list the dense ones for
-// the pre-reducing kernel, so every tile is integrated exactly once.
-// Launches below kAdaptiveMinPixels pixels add every sample directly (there
-// launch latency dominates).
+// Where to pre-reduce in shared memory (adaptive mode).  A 16 x 16 pixel
+// tile is dense when at least half of its valid pixels (finite depth > 0) see
+// a voxel edge at least w pixels wide (voxel * fx >= w * depth): there
+// samples crowd into few voxels.  The widths are where the shared-memory
+// pre-reduction overtook five direct reductions per sample on GB300: near 5
+// pixels for launches of several frames (the frames' samples of a voxel meet
+// in L2 as well) and near 10 for a single frame; against the warp-merged
+// per-sample kernel it no longer wins anywhere measured, which is why the
+// mode is not the default.  The per-sample kernel applies this rule to its
+// 16 x 16 tiles and lists the dense ones for the pre-reducing kernel, so
+// every tile is integrated exactly once.  Launches below kAdaptiveMinPixels
+// pixels add every sample directly (there launch latency dominates).
 constexpr uint32_t kAdaptiveMinPixels = 1u << 18;
 
 __device__ __forceinline__ float dense_width(int n_frames) { return n_frames >= 4 ? 5.0f : 10.0f; }

@@ -105,10 +105,6 @@ struct FrameBatch {
 
 cudaError_t launch_allocate(const VolumeView& vol, const FrameBatch& fb, bool instrument,
                             cudaStream_t stream);
-// The pre-reducing update of the dense tiles listed in vol.dense_list (by
-// the per-sample update or the fused integrate kernel of the same batch).
-cudaError_t launch_update_listed(const VolumeView& vol, const FrameBatch& fb,
-                                 cudaStream_t stream);
 // Allocate and update in one kernel (bands of at most 9 samples, the ray
 // occlusion test).
 cudaError_t launch_integrate_fused(const VolumeView& vol, const FrameBatch& fb, bool instrument,

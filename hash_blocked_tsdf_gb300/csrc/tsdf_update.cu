@@ -1,13 +1,16 @@
 // Update kernels ("What Irregularity Costs", design section, integration:
 // the regular stage; accumulation: sums, not running means).
 //
-// By default (adaptive) both kernels run on every batch and split the frame
-// by 16 x 16 pixel tiles: a tile whose pixels are small against the voxels
-// (the density rule in tsdf_device.cuh: at least half of them see a voxel
-// edge 5 or more pixels wide, 10 for launches of fewer than 4 frames) has its
+// By default (TSDF_UPDATE_PER_SAMPLE) update_kernel alone adds every
+// sample, merging a warp's samples of the same voxel first.  In the
+// adaptive mode both kernels run on every batch and split the frame by
+// 16 x 16 pixel tiles: a tile whose pixels are small against the voxels (the
+// density rule in tsdf_device.cuh: at least half of them see a voxel edge 5
+// or more pixels wide, 10 for launches of fewer than 4 frames) has its
 // samples crowd into few voxels; update_kernel lists it and the persistent
-// update_rows_kernel pre-reduces it; update_kernel adds every other tile's
-// samples itself.
+// update_rows_kernel pre-reduces it in shared memory; update_kernel adds
+// every other tile's samples itself.  In the pre-reduced mode
+// update_rows_kernel takes every tile.
 //
 // update_kernel (per sample): every thread walks one pixel's band, looks
 // up each passing sample's block (one lookup per new key, almost always a
@@ -484,18 +487,6 @@ cudaError_t launch_rows(const VolumeView& vol, const FrameBatch& fb, unsigned gr
     }
     update_rows_kernel<kFast, kAlways><<<grid, kRowThreads, kRowSmemBytes, stream>>>(vol, fb);
     return cudaGetLastError();
-}
-
-cudaError_t launch_update_listed(const VolumeView& vol, const FrameBatch& fb,
-                                 cudaStream_t stream)
-{
-    int dev = 0, sms = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(sms > 0 ? sms : 1) * kRowBlocksPerSM;
-    return vol.fast_div ? launch_rows<true, false>(vol, fb, grid, stream)
-                        : launch_rows<false, false>(vol, fb, grid, stream);
 }
 
 cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,

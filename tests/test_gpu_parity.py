@@ -537,9 +537,9 @@ def test_room_walk_full_size_sampled(torch_cuda, oracle_mod):
                                          (0.004, 0.016)])
 def test_fixed_divisor_fast_path_verified(torch_cuda, voxel, trunc):
     """At create the library checks, over all 2^32 float32 dividends, that the
-    reciprocal-and-correction division gives the walk the same floored voxel
-    indices and the same tsdf values as IEEE division; for the workloads'
-    divisors that check must pass (the parity tests then run on that path)."""
+    reciprocal-and-correction division by the truncation distance gives the
+    walk the same tsdf values as IEEE division; for the workloads' divisors
+    that check must pass (the parity tests then run on that path)."""
     from hash_blocked_tsdf_gb300 import TsdfVolume
     vol = TsdfVolume(64, voxel, trunc)
     assert vol.info["fixed_divisor_fast_path"] == 1
