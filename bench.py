@@ -45,7 +45,7 @@ WORKLOADS = {
     "vga": ("vga_sphere_plane", {}),
     "tiny": ("tiny_sphere_plane", {}),
     # the orbit seen through 4 cm voxels: nearly every pixel sees a voxel edge
-    # 5+ pixels wide, the regime the adaptive update pre-reduces
+    # 5+ pixels wide, so many samples share a voxel (the dense regime)
     "orbit_coarse": ("orbit_trajectory", {"n_frames": 100, "voxel_size": 0.04, "trunc": 0.16,
                                           "pool_capacity": 1 << 16}),
 }

@@ -297,7 +297,7 @@ int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uin
 /* Set blocks from host arrays (restoring a saved volume, or loading a known
  * field): for each of the n block coordinates (int32 [n][3], all distinct),
  * ensure the block exists through the allocate kernel's insert path, then
- * overwrite its five arrays with tsdf, weight, r, g, b (float32 [n][512]
+ * overwrite its five sums with tsdf, weight, r, g, b (float32 [n][512]
  * each, voxel j = lx + 8 ly + 64 lz, the layout tsdf_export_blocks
  * returns).  Blocks that find the pool full are counted (pool_exhausted) and
  * left unwritten; coordinates outside [-2^20, 2^20 - 1] are counted as out of
