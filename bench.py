@@ -685,7 +685,7 @@ def run_ours(args):
                                  "allocate_kernel_reproject_room_walk_1280x720.md",
                                  ["tsdf_alloc.cu", "tsdf_device.cuh", "tsdf_internal.h"])
     same_shape = (args.workload == "room_walk" and frames.width == 1280 and frames.height == 720
-                  and group == 8)
+                  and group == vol.info["max_frames_per_launch"])
     roofline = {
         "bound": "hbm", "kernel": upd_kernel, "achieved": achieved, "peak": hbm_peak,
         "unit": "GB/s", "frac": achieved / hbm_peak,

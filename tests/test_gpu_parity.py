@@ -177,7 +177,7 @@ def test_adaptive_dense_frame(torch_cuda, oracle_mod, kernel):
 
 
 def test_fused_room_walk_batch(torch_cuda, oracle_mod):
-    # allocate and update in one kernel, on two 8-frame launches of the room
+    # allocate and update in one kernel, on the first 16 frames of the room
     # walk: exact blocks and weights, no wait for a published index gave up
     frames = scenes.room_random_walk(n_frames=300, frames=(0, 16))
     vol = _gpu_volume(torch_cuda, frames)

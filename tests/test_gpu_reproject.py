@@ -139,7 +139,7 @@ def test_the_two_tests_differ_at_depth_edges(torch_cuda, oracle_mod):
 
 
 def test_room_walk_batch_reprojected(torch_cuda, oracle_mod):
-    # two 8-frame launches of the 1280 x 720 room walk
+    # the first 16 frames of the 1280 x 720 room walk in one launch
     frames = scenes.room_random_walk(n_frames=300, frames=(0, 16))
     _run(torch_cuda, oracle_mod, frames, strict=False)
 
@@ -154,7 +154,7 @@ def test_invalid_occlusion_mode_rejected(torch_cuda):
 
 @pytest.mark.slow
 def test_room_walk_full_size_sampled_reprojected(torch_cuda, oracle_mod):
-    """The 300-frame 1280x720 room walk in 8-frame batch launches under the
+    """The 300-frame 1280x720 room walk in batch launches under the
     reprojection test.  Exact: block set (frame-parallel oracle), counters.
     Sampled: 96 blocks' sums."""
     torch = torch_cuda
