@@ -689,7 +689,8 @@ def run_ours(args):
     roofline = {
         "bound": "hbm", "kernel": upd_kernel, "achieved": achieved, "peak": hbm_peak,
         "unit": "GB/s", "frac": achieved / hbm_peak,
-        "traffic": (prof_upd.get("traffic_bytes_per_launch") if same_shape else None),
+        "traffic": (_per_launch(prof_upd, "traffic_bytes_per_launch", n / ng)
+                    if same_shape else None),
         "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS)",
         "bytes_per_launch_alg": bytes_per_launch, "avg_launch_ms": upd_ms_avg,
         "units": "per frame: 16 B per valid point + 40 B per distinct voxel of the frame",
@@ -722,25 +723,25 @@ def run_ours(args):
     sm_mhz = (clk or {}).get("sm_mhz") or 2070.0
     sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     if same_shape and prof_alloc.get("warp_instructions_per_launch"):
-        ipl = prof_alloc["warp_instructions_per_launch"]
+        ipl = _per_launch(prof_alloc, "warp_instructions_per_launch", n / ng)
         peak_issue = sms * 4 * sm_mhz * 1e6
         ach = ipl / (alloc_ms_avg / 1000.0)
         alloc_roof = {"bound": "alu", "kernel": "allocate_kernel", "unit": "warp instructions/s",
                       "achieved": ach, "peak": peak_issue, "frac": ach / peak_issue,
                       "warp_instructions_per_launch": ipl,
                       "peak_source": f"{sms} SMs x 4 issue slots x sampled {sm_mhz:.0f} MHz",
-                      "traffic": prof_alloc.get("traffic_bytes_per_launch")}
+                      "traffic": _per_launch(prof_alloc, "traffic_bytes_per_launch", n / ng)}
     # its memory terms, for the record (far from binding): HBM bytes it must
     # read (4 B of depth per pixel of the launch) and the L2 atomic sectors
     # ncu counted (compare-and-swaps and pool-counter adds) against the
     # measured compare-and-swap rate
-    px_launch = frames.width * frames.height * group
+    px_launch = frames.width * frames.height * n / ng
     alloc_mem = {"hbm_bytes_per_launch_alg": 4.0 * px_launch,
                  "frac_hbm": 4.0 * px_launch / (alloc_ms_avg / 1000.0) / 1e9 / hbm_peak,
                  "cas_peak_ops_per_s": cas_peaks["hbm_4GB"]["ops_per_s"],
                  "cas_peak_ops_per_s_l2": cas_peaks["l2_32MB"]["ops_per_s"]}
     if same_shape and prof_alloc.get("l2_atomic_sectors_per_launch"):
-        at = prof_alloc["l2_atomic_sectors_per_launch"]
+        at = _per_launch(prof_alloc, "l2_atomic_sectors_per_launch", n / ng)
         alloc_mem["l2_atomic_sectors_per_launch"] = at
         alloc_mem["frac_l2_atomics"] = at / (alloc_ms_avg / 1000.0) / cas_peaks["l2_32MB"]["ops_per_s"]
 
@@ -997,10 +998,19 @@ def _profile_record(name: str, sources) -> dict:
         return {}
     out = {}
     for k in ("traffic_bytes_per_launch", "warp_instructions_per_launch",
-              "l2_atomic_sectors_per_launch"):
+              "l2_atomic_sectors_per_launch", "frames_per_captured_launch"):
         if k in rec:
             out[k] = float(rec[k])
     return out
+
+
+def _per_launch(rec: dict, key: str, frames_per_launch: float):
+    """A captured per-launch figure scaled to the timed launches' average
+    frame count (the last group of a trajectory is shorter), in proportion
+    to the frames processed."""
+    if key not in rec:
+        return None
+    return rec[key] * frames_per_launch / rec.get("frames_per_captured_launch", frames_per_launch)
 
 
 def census_distinct_voxels(torch, vol, frames, d_dev, c_dev, groups) -> dict:
