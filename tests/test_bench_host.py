@@ -99,3 +99,13 @@ def test_parity_gate_rejects_a_sum_outside_the_bound(oracle_mod):
         g["tsdf"][tuple(i)] += 1e-3
     out = _gate(oracle_mod, shift)
     assert out["sums_worst_error_over_bound"] > 1.0 and not out["pass"]
+
+
+def test_captured_figures_scale_to_the_timed_launches():
+    # a 32-frame capture stands for launches that average 30 frames
+    rec = {"traffic_bytes_per_launch": 3200.0, "frames_per_captured_launch": 32.0}
+    assert bench._per_launch(rec, "traffic_bytes_per_launch", 30.0) == pytest.approx(3000.0)
+    assert bench._per_launch(rec, "warp_instructions_per_launch", 30.0) is None
+    # a record without the captured frame count is taken as it stands
+    assert bench._per_launch({"traffic_bytes_per_launch": 5.0}, "traffic_bytes_per_launch",
+                             8.0) == 5.0
