@@ -107,3 +107,41 @@ def test_product_path_never_touches_the_oracle(lib):
             if f.endswith((".cu", ".cuh", ".h", ".c", ".py")):
                 assert "oracle_" not in text and "liboracle" not in text, f"{f} calls the oracle"
     assert not hasattr(lib, "oracle_integrate")
+
+
+def _header_struct_fields(name):
+    """Field names of `typedef struct <name> { ... } <name>;` in the header."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    body = re.search(r"typedef struct " + name + r" \{(.*?)\} " + name + ";", text, re.S).group(1)
+    fields = []
+    for decl in body.split(";"):
+        m = re.search(r"(\w+)\s*(\[[^\]]*\])?\s*$", decl.strip())
+        if m:
+            fields.append(m.group(1))
+    return fields
+
+
+@pytest.mark.parametrize("name", ["tsdf_info", "tsdf_pool_view", "tsdf_stats"])
+def test_binding_structs_follow_the_header(name):
+    # the ctypes mirrors must list the header's fields in the header's order
+    from hash_blocked_tsdf_gb300 import binding
+    mirror = [f for f, _ in getattr(binding, name)._fields_]
+    assert mirror == _header_struct_fields(name)
+
+
+def test_binding_constants_follow_the_header():
+    from hash_blocked_tsdf_gb300 import binding
+    defs = dict(re.findall(r"#define (TSDF_[A-Z_]+) \(?(-?\d+)", open(HEADER).read()))
+    pairs = {
+        "TSDF_UPDATE_ADAPTIVE": binding.UPDATE_KERNELS["adaptive"],
+        "TSDF_UPDATE_PER_SAMPLE": binding.UPDATE_KERNELS["per_sample"],
+        "TSDF_UPDATE_PRE_REDUCED": binding.UPDATE_KERNELS["pre_reduced"],
+        "TSDF_UPDATE_FUSED": binding.UPDATE_KERNELS["fused"],
+        "TSDF_OCCLUSION_RAY": binding.OCCLUSION_TESTS["ray"],
+        "TSDF_OCCLUSION_REPROJECT": binding.OCCLUSION_TESTS["reproject"],
+        "TSDF_LAYOUT_INTERLEAVED": binding.POOL_LAYOUTS["interleaved"],
+        "TSDF_LAYOUT_PLANAR": binding.POOL_LAYOUTS["planar"],
+        "TSDF_PROBE_HIST_BINS": binding.PROBE_HIST_BINS,
+    }
+    for k, v in pairs.items():
+        assert int(defs[k]) == v, k
