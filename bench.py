@@ -514,7 +514,8 @@ def run_reference(args):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * dt / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": dict(workload_config(frames, args), frames_per_step=per_step),
+        "config": dict(workload_config(frames, args), frames_per_step=per_step,
+                       l2="not applicable: the oracle runs on the host CPU"),
         "cpu_baseline": {"value": value, "unit": "points/s", "cores": 1, "kind": "oracle",
                          "sample": sample, "cpu": platform.machine()},
         "e2e": {"value": value, "unit": "points/s", "h2d_bytes_per_step": 0,
