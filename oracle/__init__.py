@@ -64,6 +64,9 @@ def load(mutant: int = 0):
         "oracle_create": ([ctypes.c_float, ctypes.c_float, ctypes.c_longlong], ctypes.c_void_p),
         "oracle_destroy": ([ctypes.c_void_p], None),
         "oracle_keep_only": ([ctypes.c_void_p, i32p, ctypes.c_longlong], ctypes.c_int),
+        "oracle_keep_partition": ([ctypes.c_void_p, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+        "oracle_walk": ([ctypes.c_void_p, f32p, f32p, ctypes.c_int, ctypes.c_int, ctypes.c_float,
+                         i32p, i32p], ctypes.c_int),
         "oracle_integrate": ([ctypes.c_void_p, f32p, f32p, ctypes.c_int, ctypes.c_int, f32p, f32p],
                              ctypes.c_int),
         "oracle_set_occlusion": ([ctypes.c_void_p, ctypes.c_int], ctypes.c_int),
@@ -127,6 +130,27 @@ class OracleVolume:
         c = np.ascontiguousarray(np.asarray(coords, dtype=np.int32).reshape(-1, 3))
         if self._lib.oracle_keep_only(self._h, _ptr(c, ctypes.c_int32), c.shape[0]) != 0:
             raise RuntimeError("keep_only must be called before the first integrate")
+
+    def keep_partition(self, parts: int, part: int) -> None:
+        """Keep sums only for blocks with (bx + by + bz) mod parts == part; the
+        ``parts`` partitions are disjoint and cover every block."""
+        if self._lib.oracle_keep_partition(self._h, int(parts), int(part)) != 0:
+            raise RuntimeError("keep_partition must be called before the first integrate, "
+                               "with 0 <= part < parts")
+
+    def walk(self, K, pose, u: int, v: int, d: float):
+        """The band walk of pixel (u, v) at depth d under the ray-depth test:
+        (voxel indices int32 [S, 3], status int32 [S]: 0 pass, 1 occluded,
+        2 out of range); empty arrays for an invalid depth."""
+        K = np.ascontiguousarray(K, dtype=np.float32).reshape(4)
+        pose = np.ascontiguousarray(pose, dtype=np.float32).reshape(16)
+        S = 2 * int(round(self.trunc / self.voxel_size)) + 3
+        ix = np.zeros((S, 3), np.int32)
+        st = np.zeros(S, np.int32)
+        n = self._lib.oracle_walk(self._h, _ptr(K, ctypes.c_float), _ptr(pose, ctypes.c_float),
+                                  int(u), int(v), float(d), _ptr(ix, ctypes.c_int32),
+                                  _ptr(st, ctypes.c_int32))
+        return ix[:n], st[:n]
 
     def set_occlusion(self, mode: str) -> None:
         """Occlusion test of later integrations: "ray" (the ray pixel's depth,

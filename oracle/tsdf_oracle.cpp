@@ -297,12 +297,24 @@ bool walk_pixel(const Camera& cam, float voxel, float trunc, int band_half,
     // left to right)
     WalkRay r;
     r.d = d;
+#if ORACLE_MUTANT == 26
+    r.vx = ((cam.R[0][0] * px + cam.R[0][1] * py) + cam.R[0][2] * pz) / voxel + cam.t[0];  // planted:
+    r.vy = ((cam.R[1][0] * px + cam.R[1][1] * py) + cam.R[1][2] * pz) / voxel + cam.t[1];  // t not in
+    r.vz = ((cam.R[2][0] * px + cam.R[2][1] * py) + cam.R[2][2] * pz) / voxel + cam.t[2];  // voxels
+#else
     r.vx = (((cam.R[0][0] * px + cam.R[0][1] * py) + cam.R[0][2] * pz) + cam.t[0]) / voxel;
     r.vy = (((cam.R[1][0] * px + cam.R[1][1] * py) + cam.R[1][2] * pz) + cam.t[1]) / voxel;
     r.vz = (((cam.R[2][0] * px + cam.R[2][1] * py) + cam.R[2][2] * pz) + cam.t[2]) / voxel;
+#endif
+#if ORACLE_MUTANT == 25
+    r.ex = (cam.R[0][0] * dx + cam.R[1][0] * dy) + cam.R[2][0] * dz;   // planted: R^T dir
+    r.ey = (cam.R[0][1] * dx + cam.R[1][1] * dy) + cam.R[2][1] * dz;
+    r.ez = (cam.R[0][2] * dx + cam.R[1][2] * dy) + cam.R[2][2] * dz;
+#else
     r.ex = (cam.R[0][0] * dx + cam.R[0][1] * dy) + cam.R[0][2] * dz;
     r.ey = (cam.R[1][0] * dx + cam.R[1][1] * dy) + cam.R[1][2] * dz;
     r.ez = (cam.R[2][0] * dx + cam.R[2][1] * dy) + cam.R[2][2] * dz;
+#endif
     r.pz = pz;
     r.dz = dz;
 #if ORACLE_MUTANT == 13
@@ -327,6 +339,8 @@ struct Volume {
 
     bool keep_all = true;    // false: sums are kept only for blocks in `keep`
     std::unordered_set<BlockCoord, BlockCoordHash> keep;
+    int keep_parts = 0;      // > 0: sums are kept only for blocks of partition keep_part
+    int keep_part = 0;
 
     // every allocated block; the sums pointer is null when not kept
     std::unordered_map<BlockCoord, std::unique_ptr<BlockSums>, BlockCoordHash> blocks;
@@ -341,6 +355,16 @@ struct Volume {
     unsigned long long dropped_blocks = 0;        // distinct keys refused for lack of pool
     unsigned long long bad_local_index = 0;       // self-check: local index outside [0, 512)
 };
+
+/* Partition of a block for keep_partition: (bx + by + bz) mod parts, taken
+ * non-negative.  It only selects which blocks' sums are kept. */
+bool in_partition(const Volume& v, const BlockCoord& b)
+{
+    if (v.keep_parts <= 0) return false;
+    const long long s = (long long)b.x + (long long)b.y + (long long)b.z;
+    const long long m = ((s % v.keep_parts) + v.keep_parts) % v.keep_parts;
+    return m == v.keep_part;
+}
 
 BlockCoord block_of(const Sample& s)
 {
@@ -406,6 +430,45 @@ int oracle_keep_only(void* h, const int32_t* coords, long long n)
     return 0;
 }
 
+/* The band walk of one pixel (u, v) with depth d, as the integrator walks
+ * it under the ray-depth test: for band sample i = 0 .. 2k, its voxel index
+ * (ix_out[3 i .. 3 i + 2], left unset when out of range) and status
+ * (status_out[i]: 0 passes, 1 occluded, 2 out of range).  Returns the number
+ * of samples, or 0 for an invalid depth.  For checking the walk on its own;
+ * it changes nothing in the volume. */
+int oracle_walk(void* h, const float K[4], const float pose[16], int u, int v, float d,
+                int32_t* ix_out, int32_t* status_out)
+{
+    Volume* vol = static_cast<Volume*>(h);
+    const Camera cam = make_camera(K, pose);
+    int n = 0;
+    walk_pixel(cam, vol->voxel, vol->trunc, vol->band_half, u, v, d,
+               [&](SampleStatus st, const Sample& s) {
+        status_out[n] = (int32_t)st;
+        if (st != SAMPLE_OUT_OF_RANGE) {
+            ix_out[3 * n] = s.ix;
+            ix_out[3 * n + 1] = s.iy;
+            ix_out[3 * n + 2] = s.iz;
+        }
+        ++n;
+    });
+    return n;
+}
+
+/* Keep sums only for the blocks whose (bx + by + bz) mod parts equals part
+ * (taken non-negative): `parts` calls with part = 0 .. parts - 1 split the
+ * volume into disjoint pieces that together hold every block.  The block set
+ * and all counters are still tracked for every block. */
+int oracle_keep_partition(void* h, int parts, int part)
+{
+    Volume* v = static_cast<Volume*>(h);
+    if (!v->blocks.empty() || parts < 1 || part < 0 || part >= parts) return -1;
+    v->keep_all = false;
+    v->keep_parts = parts;
+    v->keep_part = part;
+    return 0;
+}
+
 /* Integrate one frame: depth float32 [H][W] (metres, 0 = invalid),
  * rgb float32 [H][W][3], K = {fx, fy, cx, cy}, pose = row-major 4x4
  * camera-to-world. */
@@ -444,7 +507,7 @@ int oracle_integrate(void* h, const float* depth, const float* rgb, int W, int H
                     return;
                 }
                 std::unique_ptr<BlockSums> sums;
-                if (v->keep_all || v->keep.count(b)) {
+                if (v->keep_all || v->keep.count(b) || in_partition(*v, b)) {
                     sums.reset(new BlockSums);
                     std::memset(sums.get(), 0, sizeof(BlockSums));
                 }
@@ -644,8 +707,16 @@ uint64_t oracle_hash_slot(uint64_t key, uint64_t table_size)
     z = z ^ (z >> 30);
     z = z * 0xBF58476D1CE4E5B9ull;        // modulo 2^64
     z = z ^ (z >> 27);
+#if ORACLE_MUTANT == 24
+    z = z * 0xBF58476D1CE4E5B9ull;        // planted: the first multiplier used twice
+#else
     z = z * 0x94D049BB133111EBull;
+#endif
+#if ORACLE_MUTANT == 23
+    z = z ^ (z >> 32);                    // planted: last shift 32 instead of 31
+#else
     z = z ^ (z >> 31);
+#endif
     return z % table_size;                // table_size is a power of two
 }
 

@@ -3,6 +3,8 @@ path): a dense-grid brute-force integrator written with numpy, and analytic
 surface-crossing extraction for closed-form scenes."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 
 F32 = np.float32
@@ -141,3 +143,22 @@ def zero_crossings(mean, lo, voxel, axis, direction):
         idx[ax] = r
     pts = np.stack(idx, axis=1) + np.asarray(lo)[None, :] + 0.5
     return pts * voxel
+
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+SPLITMIX64_GAMMA = 0x9E3779B97F4A7C15
+
+
+def splitmix64_vectors():
+    """(input, output) pairs of the SplitMix64 output mix from its published
+    output sequence (tests/golden/splitmix64_seed1234567.txt): output k of
+    seed s is the mix of the state s + k * gamma (mod 2^64)."""
+    out = []
+    with open(os.path.join(GOLDEN, "splitmix64_seed1234567.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            seed, k, value = (int(v) for v in line.split())
+            out.append(((seed + k * SPLITMIX64_GAMMA) % (1 << 64), value))
+    return out

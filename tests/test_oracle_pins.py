@@ -291,8 +291,126 @@ def pin_invariants(oracle_mod, mutant=0):
     return fails
 
 
+# ----------------------------------------------------------------------------
+# The walk against a float64 evaluation in another operation order
+# ----------------------------------------------------------------------------
+
+def _walk_float64(depth, K, pose, voxel, trunc, pixels):
+    """Band samples of the given pixels evaluated in float64, in the
+    camera-then-world order of the plain reading of the walk: sample
+    i = 0 .. 2k at p + (i voxel - trunc) dir in camera coordinates, moved to
+    the world with [R | t], divided by the voxel edge and floored; the
+    occlusion test at the voxel centre, z_c = (R^T (centre - t))_z,
+    sdf = d - z_c, pass iff z_c > 0 and sdf >= -trunc.  Returns the voxels
+    [n, S, 3], pass flags [n, S], each coordinate's distance (in voxels)
+    from the nearest voxel boundary [n, S, 3], and the distance (in voxels)
+    of the test's quantities from their thresholds [n, S]."""
+    fx, fy, cx, cy = (float(x) for x in K)
+    R = pose[:3, :3].astype(np.float64)
+    t = pose[:3, 3].astype(np.float64)
+    v = float(np.float32(voxel))
+    tau = float(np.float32(trunc))
+    k = int(round(tau / v))
+    u = pixels[:, 0].astype(np.float64)
+    vv = pixels[:, 1].astype(np.float64)
+    d = depth[pixels[:, 1], pixels[:, 0]].astype(np.float64)
+    ray = np.stack([(u - cx) / fx, (vv - cy) / fy, np.ones_like(u)], axis=1)
+    p = ray * d[:, None]
+    dirn = ray / np.linalg.norm(ray, axis=1, keepdims=True)
+    off = np.arange(2 * k + 1, dtype=np.float64) * v - tau
+    cam = p[:, None, :] + off[None, :, None] * dirn[:, None, :]
+    world = cam @ R.T + t
+    q = world / v
+    vox = np.floor(q)
+    edge = np.abs(q - np.round(q))
+    centre = (vox + 0.5) * v
+    zc = (centre - t) @ R[:, 2]
+    sdf = d[:, None] - zc
+    passes = (zc > 0) & (sdf >= -tau)
+    test_margin = np.minimum(np.abs(sdf + tau), np.abs(zc)) / v
+    return vox.astype(np.int64), passes, edge, test_margin
+
+
+def _walk_frames():
+    """(name, depth, K, pose, voxel, trunc, pixel step) cases: the worked
+    examples, the sphere frames, and subsamples of the noisy 640x480 frame
+    and of a room-walk frame (a general rotation)."""
+    cases = []
+    for name, depth, pose in (("worked identity", WE_IDENTITY_DEPTH, WE_IDENTITY_POSE),
+                              ("worked rotated", WE_ROT_DEPTH, WE_ROT_POSE)):
+        cases.append((name, depth, WE_K, pose, VOXEL, TRUNC, 0))
+    for frames, step in ((scenes.tiny_sphere_plane(), 1), (oblique_sphere_frames(), 1),
+                         (scenes.vga_sphere_plane(), 7),
+                         (scenes.room_random_walk(n_frames=300, frames=(0, 1)), 41)):
+        cases.append((frames.name, frames.depth[0], frames.K, frames.poses[0],
+                      frames.voxel_size, frames.trunc, step))
+    return cases
+
+
+def pin_walk_float64(oracle_mod, mutant=0):
+    """Every band sample of the oracle against the float64 evaluation above.
+    Per axis, where the float64 coordinate lies more than 1e-4 voxel from a
+    voxel boundary, the oracle's voxel index must equal its floor; where all
+    three do and the occlusion test's quantities are 1e-4 voxel clear of
+    their thresholds, the oracle must take the same decision; every pixel
+    must have 2k + 1 samples.  The oracle evaluates the walk in voxel units
+    with float32 operations in another order, so this does not share its
+    arithmetic; float32 rounding moves a sample by far less than 1e-4 voxel
+    at these coordinates.  (Coordinates on a boundary, such as the zero x of
+    a ray along the optical axis, are skipped on that axis.)"""
+    fails = []
+    margin = 1e-4
+    for name, depth, K, pose, voxel, trunc, step in _walk_frames():
+        vv, uu = np.nonzero(np.isfinite(depth) & (depth > 0))
+        pix = np.stack([uu, vv], axis=1)
+        if step:
+            pix = pix[::step]
+        vox64, pass64, edge, tmargin = _walk_float64(depth, K, pose, voxel, trunc, pix)
+        o = oracle_mod.OracleVolume(voxel, trunc, mutant=mutant)
+        S = vox64.shape[1]
+        clear = edge > margin
+        axes = whole = decided = 0
+        bad = []
+        for n, (u, v) in enumerate(pix):
+            ix, st = o.walk(K, pose, int(u), int(v), float(depth[v, u]))
+            if ix.shape[0] != S:
+                bad.append(f"pixel ({u}, {v}): {ix.shape[0]} samples, not {S}")
+                continue
+            for i in range(S):
+                if st[i] == 2:
+                    bad.append(f"pixel ({u}, {v}) sample {i}: out of range")
+                    continue
+                for a in range(3):
+                    if clear[n, i, a]:
+                        axes += 1
+                        if ix[i, a] != vox64[n, i, a]:
+                            bad.append(f"pixel ({u}, {v}) sample {i} axis {a}: voxel "
+                                       f"{ix[i, a]} != {vox64[n, i, a]}")
+                if clear[n, i].all():
+                    whole += 1
+                    if tmargin[n, i] > margin:
+                        decided += 1
+                        if (st[i] == 0) != bool(pass64[n, i]):
+                            bad.append(f"pixel ({u}, {v}) sample {i}: test {st[i]} != "
+                                       f"{'pass' if pass64[n, i] else 'occluded'}")
+            if len(bad) > 5:
+                break
+        o.close()
+        total = pix.shape[0] * S
+        if bad:
+            fails.append(f"{name}: " + "; ".join(bad[:3]))
+        elif axes < total:
+            fails.append(f"{name}: only {axes} coordinates of {total} samples clear of "
+                         f"voxel boundaries")
+        elif step and (whole < 0.8 * total or decided < 0.8 * total):
+            fails.append(f"{name}: only {whole} / {decided} of {total} samples compared "
+                         f"whole / decided")
+    return fails
+
+
 # cheapest first: the planted-mistake test stops at the first pin that fails
-ALL_PINS = [pin_worked_identity, pin_worked_rotated, pin_invariants, pin_sphere, pin_dense]
+ALL_PINS = [pin_worked_identity, pin_worked_rotated, pin_invariants, pin_walk_float64,
+            pin_sphere, pin_dense]
 
 
 @pytest.mark.parametrize("pin", ALL_PINS, ids=lambda p: p.__name__)
@@ -315,6 +433,8 @@ PLANTED = {
     12: "allocate pass ignores the occlusion test",
     13: "band one voxel too wide",
     14: "ray direction not normalised",
+    25: "ray direction moved to the world by R^T instead of R",
+    26: "camera position added after the division by the voxel edge",
 }
 
 
@@ -403,3 +523,33 @@ def test_keep_only_restricts_sums_not_the_block_set(oracle_mod):
     rows = np.arange(0, ef["coords"].shape[0], 97)
     for k in ("tsdf", "weight", "r", "g", "b", "tsdf_abs"):
         assert np.array_equal(ep[k], ef[k][rows])
+
+
+def test_keep_partition_splits_the_volume_into_disjoint_parts(oracle_mod):
+    """keep_partition(parts, part) keeps the sums of the blocks with
+    (bx + by + bz) mod parts == part: the parts are disjoint, together they
+    are the whole volume, and each part's sums equal the unrestricted run's
+    (the filter only selects blocks; the arithmetic is the same)."""
+    frames = scenes.tiny_sphere_plane()
+    full = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
+    full.integrate_frames(frames)
+    ef = full.export()
+    parts = 3
+    seen = []
+    for p in range(parts):
+        o = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
+        o.keep_partition(parts, p)
+        o.integrate_frames(frames)
+        e = o.export()
+        assert o.block_count() == full.block_count()
+        assert o.counters() == full.counters()
+        assert np.all(np.mod(e["coords"].astype(np.int64).sum(axis=1), parts) == p)
+        rows = np.nonzero(np.mod(ef["coords"].astype(np.int64).sum(axis=1), parts) == p)[0]
+        assert np.array_equal(e["coords"], ef["coords"][rows])
+        for k in ("tsdf", "weight", "r", "g", "b", "tsdf_abs"):
+            assert np.array_equal(e[k], ef[k][rows])
+        seen.append(e["coords"])
+    assert sum(s.shape[0] for s in seen) == ef["coords"].shape[0]
+    assert min(s.shape[0] for s in seen) > 0
+    with pytest.raises(RuntimeError):
+        oracle_mod.OracleVolume(frames.voxel_size, frames.trunc).keep_partition(3, 3)

@@ -176,3 +176,36 @@ def test_clustered_coords_form_one_long_chain(oracle_mod):
     assert np.array_equal(occ, np.arange(1000, 1000 + want))
     # mean displacement is about half the run length
     assert disp / distinct > want / 2 - w
+
+
+def test_hash_known_answers_from_the_published_splitmix64_sequence(oracle_mod):
+    """The slot hash is the SplitMix64 output mix: on the states that give
+    the generator's published outputs it must return those outputs (here
+    to 63 bits, the largest power-of-two table the call accepts, and masked
+    to the table sizes of the workloads)."""
+    import helpers
+    vectors = helpers.splitmix64_vectors()
+    assert len(vectors) == 5
+    for state, value in vectors:
+        assert oracle_mod.hash_slot(state, 1 << 63) == value % (1 << 63)
+        for T in (1 << 14, 1 << 16, 1 << 18, 1 << 21):
+            assert oracle_mod.hash_slot(state, T) == value % T
+
+
+@pytest.mark.parametrize("mutant,what", [(23, "last xor-shift by 32 instead of 31"),
+                                         (24, "first multiplier used for the second")])
+def test_hash_mistakes_pass_the_spread_pins_but_not_the_known_answers(oracle_mod, mutant, what):
+    """A wrong shift or constant still spreads keys well (the structural
+    pins cannot see it); the published outputs reject it."""
+    import os
+
+    import helpers
+    try:
+        vectors = helpers.splitmix64_vectors()
+        wrong = [s for s, v in vectors
+                 if oracle_mod.hash_slot(s, 1 << 63, mutant=mutant) != v % (1 << 63)]
+        assert wrong, f"the known-answer pin misses the planted mistake: {what}"
+    finally:
+        path = oracle_mod.library_path(mutant)
+        if os.path.exists(path):
+            os.remove(path)
