@@ -104,6 +104,30 @@ def test_parity_ragged_sizes(torch_cuda, oracle_mod, wh, kernel):
     _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
 
 
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_parity_long_band_single_frame(torch_cuda, oracle_mod, kernel):
+    """Voxel 5 mm, truncation 5 cm: 21 samples per ray under the ray-depth
+    test.  Bands longer than 9 samples take the allocate kernel's step-by-step
+    insert path, the pre-reducing kernel's three-way band split with 7
+    samples per part, and (fused mode) the two-kernel fallback."""
+    f = scenes.tiny_sphere_plane()
+    frames = scenes.Frames("long_band_160x120", f.depth, f.rgb, f.poses, f.K, 0.005, 0.05,
+                           1 << 15, 0, 0)
+    rep = _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
+    assert rep["blocks"] > 1000
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_parity_long_band_orbit_batch(torch_cuda, oracle_mod, kernel):
+    """Eight orbit frames in one launch through 2 cm voxels with a 20 cm
+    truncation (21 samples per ray): near tiles see voxel edges 5+ pixels
+    wide, so the adaptive mode sends them to the pre-reducing kernel with the
+    long band."""
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 8), voxel_size=0.02, trunc=0.2,
+                                     pool_capacity=1 << 16)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=False, kernel=kernel)
+
+
 def _flat_frame(name, W, H, f, depth_m, pose, voxel, trunc, pool, rgb_scale=1.0, rgb_shift=0.0,
                 seed=0):
     """One frame of a surface at constant camera depth, colours uniform."""
@@ -405,6 +429,31 @@ def _check_table_structure(oracle_mod, vol, expected_coords):
     return disp / max(n, 1)
 
 
+@pytest.mark.parametrize("T", [1 << 16, 1 << 21])
+def test_home_slot_known_answers_from_the_published_splitmix64_sequence(torch_cuda, T):
+    """The kernels' slot hash against SplitMix64's published outputs: the
+    generator states with bit 63 clear are valid packed keys, so their
+    block coordinates are inserted one at a time into an empty table; each
+    key must land in the slot given by the published output, masked to the
+    table (and the stored key must be the state: the packing agrees)."""
+    import helpers
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    torch = torch_cuda
+    planted = [(k, v) for k, v in helpers.splitmix64_vectors() if k >> 63 == 0]
+    assert len(planted) == 3
+    for key, value in planted:
+        coord = np.array([[(key >> (21 * a) & 0x1FFFFF) - (1 << 20) for a in range(3)]],
+                         dtype=np.int32)
+        vol = TsdfVolume(64, 0.01, 0.04, T)
+        vol.allocate_blocks(torch.from_numpy(coord).cuda())
+        torch.cuda.synchronize()
+        keys, idx = vol.export_table()
+        occ = np.nonzero(keys != np.uint64(0xFFFFFFFFFFFFFFFF))[0]
+        assert occ.tolist() == [value % T], (hex(key), occ, value % T)
+        assert int(keys[occ[0]]) == key and int(idx[occ[0]]) == 0
+        vol.close()
+
+
 def test_table_structure_matches_sequential_linear_probing(torch_cuda, oracle_mod):
     torch = torch_cuda
     frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 4))
@@ -487,50 +536,38 @@ def test_load_factor_sweep(torch_cuda, oracle_mod):
 
 
 @pytest.mark.slow
-def test_room_walk_full_size_sampled(torch_cuda, oracle_mod):
+def test_room_walk_full_volume(torch_cuda, oracle_mod):
     """The 300-frame 1280x720 room walk (pool 2^20, table 2^21) in the batch
-    call the benchmark times.  Exact: block set (against a frame-parallel
-    oracle), counters.  Sampled: 96 blocks' sums, chosen from the oracle's own
-    first and last frames."""
+    call the benchmark times, compared with the oracle's whole volume
+    (computed in parallel over frame chunks and block partitions): the exact
+    block set, every weight of every block, the counters, and every TSDF
+    and colour sum within max(1e-5 |x|, 1e-6), or the float32 summation
+    bound where a voxel's terms cancel (the test prints how many voxels
+    needed it, and by how much they exceeded the stated bound)."""
     torch = torch_cuda
-    n = 300
-    frames = scenes.room_random_walk(n_frames=n)
+    frames = scenes.room_random_walk(n_frames=300)
     vol = _gpu_volume(torch, frames)
     _integrate_gpu(torch, frames, vol)
     st = vol.stats()
-    B = vol.block_count()
-    g = vol.export_blocks(fields=("coords",))
-    # sample blocks from the oracle's view of frames 0 and n-1
-    rng = np.random.Generator(np.random.PCG64(2024))
-    keep = []
-    for f in (0, n - 1):
-        o1 = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
-        o1.integrate(frames.depth[f], frames.rgb[f], frames.K, frames.poses[f])
-        c1 = o1.coords()
-        keep.append(c1[rng.choice(c1.shape[0], size=48, replace=False)])
-    keep = np.unique(np.concatenate(keep), axis=0)
+    g = vol.export_blocks()
+    vol.close()
+    torch.cuda.empty_cache()
+    ref, counters = parity.full_volume_oracle(frames)
     del frames
-    import os
-    workers = max(2, min(16, (os.cpu_count() or 2)))
-    coords, counters, merged = parity.parallel_oracle("room_random_walk", {"n_frames": n}, n,
-                                                      keep, workers)
-    assert B == coords.shape[0], (B, coords.shape[0])
-    gc = g["coords"][parity.sort_by_coords(g["coords"])]
-    assert np.array_equal(gc, coords)
     assert st["pool_exhausted"] == 0 and st["probe_overflow"] == 0
     assert st["valid_points"] == counters["valid_points"]
     assert st["voxel_updates"] == counters["accumulated"] == counters["passing_samples"]
+    assert st["missed_contributions"] == counters["missed_contributions"] == 0
     assert st["out_of_range_samples"] == counters["out_of_range_samples"]
-    # sampled sums
-    lut = {tuple(int(v) for v in c): i for i, c in enumerate(g["coords"])}
-    for key, ref in merged.items():
-        i = lut[key]
-        one = vol.export_blocks(first=i, count=1)
-        parity.compare_sums({k: one[k] for k in ("tsdf", "weight", "r", "g", "b")},
-                            {k: ref[k][None, :] for k in ref}, strict=False)
-    print(f"room walk: {B} blocks, {st['voxel_updates']} voxel updates, "
-          f"{len(merged)} sampled blocks match")
-    vol.close()
+    rep = parity.compare_volume(g, ref, strict=False)
+    assert rep["blocks"] == st["blocks_allocated"]
+    assert np.all(g["weight"].sum(axis=1) > 0)
+    print(f"room walk full volume: {rep['blocks']} blocks, {rep['blocks'] * 512} voxels, "
+          f"{st['voxel_updates']} voxel updates; "
+          + "; ".join(f"{k}: max error {rep[k]['max_err']:.3g}, "
+                      f"{rep[k]['voxels_over_base']} voxels over max(1e-5|x|, 1e-6) "
+                      f"(worst {rep[k]['max_err_over_base']:.3g}x)"
+                      for k in ("tsdf", "r", "g", "b")))
 
 
 @pytest.mark.parametrize("voxel,trunc", [(0.02, 0.08), (0.01, 0.04), (0.005, 0.02),
