@@ -65,7 +65,9 @@ def _gate(oracle_mod, mutate=None):
     if mutate:
         mutate(g)
     stats = {"valid_points": c["valid_points"], "voxel_updates": c["accumulated"],
-             "missed_contributions": c["missed_contributions"]}
+             "missed_contributions": c["missed_contributions"],
+             "out_of_range_samples": c["out_of_range_samples"], "pool_exhausted": 0,
+             "probe_overflow": 0}
     fake_torch = types.SimpleNamespace(cuda=types.SimpleNamespace(synchronize=lambda: None))
     return bench.parity_gate(fake_torch, _FakeVolume(g, stats), frames, frames.depth,
                              frames.rgb, frames.n_frames, o)
@@ -99,6 +101,18 @@ def test_parity_gate_rejects_a_sum_outside_the_bound(oracle_mod):
         g["tsdf"][tuple(i)] += 1e-3
     out = _gate(oracle_mod, shift)
     assert out["sums_worst_error_over_bound"] > 1.0 and not out["pass"]
+    assert out["sums"]["tsdf"]["voxels_over_stated_bound"] == 1
+    assert out["sums"]["r"]["voxels_over_stated_bound"] == 0
+
+
+def test_a_failed_gate_withholds_the_headline(oracle_mod):
+    line = {"value": 5.0, "e2e": {"value": 4.0, "unit": "points/s"}}
+    bench.apply_gate(line, {"pass": True})
+    assert line["value"] == 5.0 and line["gated"] is True and "withheld" not in line
+    line = {"value": 5.0, "e2e": {"value": 4.0, "unit": "points/s"}}
+    bench.apply_gate(line, _gate(oracle_mod, lambda g: g["weight"].__setitem__((0, 0), 7.0)))
+    assert line["value"] is None and line["e2e"]["value"] is None and line["gated"] is False
+    assert line["withheld"]["value"] == 5.0 and line["withheld"]["e2e_value"] == 4.0
 
 
 def test_captured_figures_scale_to_the_timed_launches():
