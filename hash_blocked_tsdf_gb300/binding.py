@@ -397,13 +397,16 @@ UPDATE_ADAPTIVE = 0
 UPDATE_PER_SAMPLE = 1
 UPDATE_PRE_REDUCED = 2
 UPDATE_FUSED = 3
+UPDATE_AUTO = 4
 UPDATE_KERNELS = {"adaptive": UPDATE_ADAPTIVE, "per_sample": UPDATE_PER_SAMPLE,
-                  "pre_reduced": UPDATE_PRE_REDUCED, "fused": UPDATE_FUSED}
+                  "pre_reduced": UPDATE_PRE_REDUCED, "fused": UPDATE_FUSED,
+                  "auto": UPDATE_AUTO}
 
 
 def tsdf_set_update_kernel(h, kind) -> None:
-    """Select how updates reach the pool: "per_sample" (default: each warp
-    merges its lanes' samples of one voxel, then reduces into the pool),
+    """Select how updates reach the pool: "auto" (default: "per_sample", with
+    integrate launches under 2^19 pixels run as "fused"), "per_sample" (each
+    warp merges its lanes' samples of one voxel, then reduces into the pool),
     "adaptive" (tiles whose samples crowd into voxels pre-reduce in shared
     memory), "pre_reduced" (every tile does), or "fused" (integrate calls run
     allocate and update as one kernel); or the header's integer constants."""

@@ -148,4 +148,8 @@ struct tsdf_volume;
 namespace tsdf {
 VolumeView volume_view(const tsdf_volume* vol);
 int record_error(int code, const char* message);   // sets tsdf_last_error, returns code
+// Device address of the no-allocation export's scratch array on the current
+// device (looked up at volume creation; tsdf_noalloc.cu).
+int resolve_noalloc_scratch(int32_t** out);
+int32_t* noalloc_scratch_of(const tsdf_volume* vol);
 }  // namespace tsdf

@@ -13,13 +13,17 @@
 // The scratch is a file-scope __device__ array of kNoAllocMaxBlocks block
 // coordinates (768 KB); every GPU that loads the library holds one copy until
 // the process exits.  Host code may not hand the array's name to a kernel
-// (on the host it names a stand-in, not device memory), so the device address
-// is looked up with cudaGetSymbolAddress on the first call on each device
-// (with that device current) and cached.  All calls share the one array, and
-// it keeps the previous call's contents: each call clears the part it uses,
-// and two calls whose work overlaps on the GPU race on it.
-#include <mutex>
-
+// (on the host it names a stand-in, not device memory), so its device address
+// is looked up with cudaGetSymbolAddress when a volume is created, with the
+// volume's device current, and kept in the volume.  Looking it up there also
+// loads the module that holds the array and its export kernel (CUDA loads
+// modules and kernels lazily, on first use), so the array's memory is set
+// aside by tsdf_create, which allocates anyway, and never by the export
+// call.  A volume created after a
+// cudaDeviceReset looks the address up again in the new context.  All calls
+// share the one array, and it keeps the previous call's contents: each call
+// clears the part it uses, and two calls whose work overlaps on the GPU race
+// on it.
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -27,13 +31,8 @@ namespace {
 
 constexpr uint32_t kNoAllocMaxBlocks = TSDF_NOALLOC_MAX_BLOCKS;
 constexpr int kThreads = 256;
-constexpr int kMaxDevices = 64;
 
 __device__ __align__(256) int32_t g_coord_scratch[3 * kNoAllocMaxBlocks];
-
-// Device address of g_coord_scratch per device, filled on first use.
-std::mutex g_scratch_mutex;
-int32_t* g_scratch_ptr[kMaxDevices] = {};
 
 // coords[idx - first] = coordinate of the block whose table entry holds pool
 // index idx, for idx in [first, first + count).
@@ -49,25 +48,23 @@ __global__ void __launch_bounds__(kThreads) export_coords_range_kernel(VolumeVie
     unpack_block(e.key, coords + 3 * (size_t)(e.idx - first));
 }
 
-int scratch_for_current_device(int32_t** out)
+}  // namespace
+
+int resolve_noalloc_scratch(int32_t** out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return record_error(TSDF_ERR_CUDA, cudaGetErrorString(e));
-    if (dev < 0 || dev >= kMaxDevices) return record_error(TSDF_ERR_ARG, "device ordinal >= 64");
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_coord_scratch);
-        if (e != cudaSuccess || !p)
-            return record_error(TSDF_ERR_CUDA, "cudaGetSymbolAddress(g_coord_scratch) failed");
-        g_scratch_ptr[dev] = static_cast<int32_t*>(p);
-    }
-    *out = g_scratch_ptr[dev];
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_coord_scratch);
+    if (e != cudaSuccess || !p)
+        return record_error(TSDF_ERR_CUDA, "cudaGetSymbolAddress(g_coord_scratch) failed");
+    // load the export kernel as well (kernels too are loaded on first use)
+    cudaFuncAttributes attr;
+    e = cudaFuncGetAttributes(&attr, export_coords_range_kernel);
+    if (e != cudaSuccess)
+        return record_error(TSDF_ERR_CUDA, "cudaFuncGetAttributes(export kernel) failed");
+    *out = static_cast<int32_t*>(p);
     return TSDF_OK;
 }
 
-}  // namespace
 }  // namespace tsdf
 
 using namespace tsdf;
@@ -80,13 +77,13 @@ extern "C" int tsdf_export_block_coords_noalloc(tsdf_volume* vol, void* stream, 
         return record_error(TSDF_ERR_ARG,
                             "count exceeds the no-allocation export limit of 65536 blocks");
     uint32_t n = 0;
-    int rc = tsdf_block_count(vol, stream, &n);
+    int rc = tsdf_block_count(vol, stream, &n);     // (checks the current device too)
     if (rc) return rc;
     if ((uint64_t)first + count > n)
         return record_error(TSDF_ERR_ARG, "first + count exceeds the number of allocated blocks");
     if (count == 0) return TSDF_OK;
-    int32_t* scratch = nullptr;
-    if ((rc = scratch_for_current_device(&scratch))) return rc;
+    int32_t* scratch = noalloc_scratch_of(vol);
+    if (!scratch) return record_error(TSDF_ERR_CUDA, "the volume has no scratch address");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const VolumeView view = volume_view(vol);
     const size_t bytes = (size_t)count * 3 * sizeof(int32_t);

@@ -18,6 +18,12 @@ namespace {
 
 // Blocks per chunk when export splits the interleaved voxel records into
 // planes (16,384 blocks: a 128 MB scratch buffer).
+// In the default update mode, integrate launches of fewer pixels than this
+// (frames x width x height) run the fused kernel: measured on GB300, one
+// fused launch took 0.039 / 0.046 / 0.077 ms against 0.054 / 0.061 / 0.079 ms
+// for allocate + update at 160x120 / 320x240 / 640x480, and 0.205 against
+// 0.194 ms at 1280x960, where the two kernels fill the GPU.
+constexpr uint64_t kAutoFusedPixels = 1ull << 19;
 constexpr uint32_t kExportChunkBlocks = 1u << 14;
 
 // Device-resident mutable state: the pool's bump counter and the counters.
@@ -42,7 +48,7 @@ struct tsdf_volume {
     float trunc = 0.0f;
     int band_half = 0;
     bool instrument = false;
-    int update_kind = TSDF_UPDATE_PER_SAMPLE;
+    int update_kind = TSDF_UPDATE_AUTO;
     int occlusion = TSDF_OCCLUSION_RAY;
     int layout = TSDF_LAYOUT_INTERLEAVED;
     DivisorPair div = {};
@@ -54,6 +60,8 @@ struct tsdf_volume {
                                     // pool_capacity * 512 blue sums
     DeviceState* state = nullptr;
     int32_t* coords = nullptr;      // [pool_capacity][3], allocated on first export
+    int32_t* noalloc_scratch = nullptr;  // device address of the no-allocation export's
+                                         // scratch array, looked up at create
     float* export_scratch = nullptr;  // [kExportChunkBlocks][512][4], allocated on first export
 
     // host-batch staging: two buffers of (depth, rgb) frames
@@ -143,9 +151,20 @@ int check_size(int width, int height)
     return TSDF_OK;
 }
 
+// Every call that touches the volume's device memory runs with the volume's
+// device current; a call from another device would hand that device's
+// kernels pointers into the wrong GPU's memory.
 int check_volume(const tsdf_volume* v)
 {
     if (!v) return fail(TSDF_ERR_ARG, "volume is null");
+    int dev = -1;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev != v->device)
+        return fail(TSDF_ERR_ARG, "the current CUDA device is " + std::to_string(dev) +
+                                      " but the volume lives on device " +
+                                      std::to_string(v->device) +
+                                      ": call cudaSetDevice with the volume's device first");
     return TSDF_OK;
 }
 
@@ -213,19 +232,25 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
             fb.frame[f].rgb = rgb ? rgb + 3 * (first + f) * px : nullptr;
             fb.frame[f].cam = cams[first + f];
         }
-        if (do_allocate && do_update && v->update_kind == TSDF_UPDATE_FUSED &&
-            v->occlusion == TSDF_OCCLUSION_RAY && 2 * v->band_half + 1 <= 9) {
+        // one fused kernel instead of allocate + update: always in the fused
+        // mode, and in the default mode for launches too small to fill the
+        // GPU, where the two kernels' latencies add up
+        const bool small = (uint64_t)px * (uint64_t)fb.n < kAutoFusedPixels;
+        const bool fuse = v->update_kind == TSDF_UPDATE_FUSED ||
+                          (v->update_kind == TSDF_UPDATE_AUTO && small);
+        if (do_allocate && do_update && fuse && v->occlusion == TSDF_OCCLUSION_RAY &&
+            2 * v->band_half + 1 <= 9) {
             TSDF_CUDA(launch_integrate_fused(vol, fb, v->instrument, stream), "fused kernel");
             continue;
         }
         if (do_allocate)
             TSDF_CUDA(launch_allocate(vol, fb, v->instrument, stream), "allocate kernel");
-        if (do_update)
-            TSDF_CUDA(launch_update(vol, fb,
-                                    v->update_kind == TSDF_UPDATE_FUSED ? TSDF_UPDATE_PER_SAMPLE
-                                                                        : v->update_kind,
-                                    stream),
-                      "update kernel");
+        if (do_update) {
+            const int kind = (v->update_kind == TSDF_UPDATE_FUSED ||
+                              v->update_kind == TSDF_UPDATE_AUTO) ? TSDF_UPDATE_PER_SAMPLE
+                                                                  : v->update_kind;
+            TSDF_CUDA(launch_update(vol, fb, kind, stream), "update kernel");
+        }
     }
     return TSDF_OK;
 }
@@ -277,6 +302,7 @@ int verify_divisors(tsdf_volume* v)
 
 namespace tsdf {
 VolumeView volume_view(const tsdf_volume* vol) { return view_of(vol); }
+int32_t* noalloc_scratch_of(const tsdf_volume* vol) { return vol->noalloc_scratch; }
 int record_error(int code, const char* message) { return fail(code, message); }
 }  // namespace tsdf
 
@@ -334,6 +360,9 @@ int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_
         return rc;
     }
     int rc = verify_divisors(v);
+    // the no-allocation export's scratch address, looked up now so that the
+    // module holding the array is loaded here and not in that call
+    if (!rc) rc = resolve_noalloc_scratch(&v->noalloc_scratch);
     if (rc) {
         release(v);
         return rc;
@@ -350,8 +379,15 @@ int tsdf_create(uint32_t pool_capacity, float voxel_size, float trunc, tsdf_volu
 int tsdf_destroy(tsdf_volume* vol)
 {
     if (!vol) return fail(TSDF_ERR_ARG, "volume is null");
-    cudaError_t e = cudaDeviceSynchronize();
+    // free on the volume's own device, then restore the caller's; the copy
+    // stream of the host-batch call is the only stream the volume owns
+    const int dev = vol->device;
+    int prev = -1;
+    cudaError_t e = cudaGetDevice(&prev);
+    if (e == cudaSuccess && prev != dev) e = cudaSetDevice(dev);
+    if (e == cudaSuccess && vol->copy_stream) e = cudaStreamSynchronize(vol->copy_stream);
     release(vol);
+    if (prev >= 0 && prev != dev) cudaSetDevice(prev);
     if (e != cudaSuccess) return cuda_fail(e, "tsdf_destroy");
     return TSDF_OK;
 }
@@ -702,10 +738,11 @@ int tsdf_set_update_kernel(tsdf_volume* vol, int kind)
     int rc = check_volume(vol);
     if (rc) return rc;
     if (kind != TSDF_UPDATE_ADAPTIVE && kind != TSDF_UPDATE_PER_SAMPLE &&
-        kind != TSDF_UPDATE_PRE_REDUCED && kind != TSDF_UPDATE_FUSED)
+        kind != TSDF_UPDATE_PRE_REDUCED && kind != TSDF_UPDATE_FUSED &&
+        kind != TSDF_UPDATE_AUTO)
         return fail(TSDF_ERR_ARG, "update mode must be TSDF_UPDATE_ADAPTIVE, "
-                                  "TSDF_UPDATE_PER_SAMPLE, TSDF_UPDATE_PRE_REDUCED or "
-                                  "TSDF_UPDATE_FUSED");
+                                  "TSDF_UPDATE_PER_SAMPLE, TSDF_UPDATE_PRE_REDUCED, "
+                                  "TSDF_UPDATE_FUSED or TSDF_UPDATE_AUTO");
     vol->update_kind = kind;
     return TSDF_OK;
 }

@@ -52,7 +52,10 @@
  * Ownership and synchronisation
  *   - A tsdf_volume owns its device memory (table, pool, counters), allocated
  *     at create and released at destroy, on the device that was current at
- *     create.  Call every function with that device current.
+ *     create.  Call every function with that device current: a call that
+ *     touches the volume's memory from another current device returns
+ *     TSDF_ERR_ARG and enqueues nothing (tsdf_destroy switches to the
+ *     volume's device by itself).
  *   - Device pointers passed in (depth, rgb, coords) are borrowed: they must
  *     stay valid until the work enqueued on `stream` has finished.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
@@ -144,7 +147,12 @@ typedef struct tsdf_stats {
 
 /* Create a volume of `pool_capacity` blocks, voxel edge `voxel_size` metres,
  * truncation `trunc` metres, with the default table size: the smallest power
- * of two strictly greater than 2 * pool_capacity.  Requires
+ * of two strictly greater than 2 * pool_capacity ("What Irregularity Costs",
+ * design section, data structure: blocks of 8^3 voxels, a flat pool of five
+ * float sums per voxel, an open-addressed linear-probing table of 16-byte
+ * entries sized to the next power of two above twice the pool capacity, so
+ * that an occupied table is at most half full; "above" is read as strictly
+ * above).  Requires
  * 1 <= pool_capacity <= TSDF_MAX_POOL_CAPACITY, finite voxel_size > 0 and
  * trunc > 0, and 2 * round(trunc / voxel_size) + 1 <= TSDF_MAX_BAND_SAMPLES.
  * Zeroes the pool and empties the table (synchronously).  *out receives the
@@ -153,29 +161,45 @@ int tsdf_create(uint32_t pool_capacity, float voxel_size, float trunc, tsdf_volu
 
 /* As tsdf_create with an explicit table size: table_capacity must be a power
  * of two with 2 * pool_capacity <= table_capacity <= TSDF_MAX_TABLE_CAPACITY,
- * or 0 for the default. */
+ * or 0 for the default (design section, data structure: any such table keeps
+ * the load at or below one half; the load-factor sweep of the expressiveness
+ * section varies the occupancy with the table fixed). */
 int tsdf_create_ex(uint32_t pool_capacity, uint32_t table_capacity, float voxel_size,
                    float trunc, tsdf_volume** out);
 
-/* Release the volume's device memory (synchronises the device first). */
+/* (design section, layout shared by the arms: the volume's memory is
+ * allocated once and handed to the kernels as pointers; this releases it.)
+ * Release the volume's device memory, on the volume's device (the caller's
+ * current device is restored).  It waits for the volume's own copy stream
+ * (tsdf_integrate_batch_host); cudaFree itself waits for work already
+ * enqueued on the device.  No other call may use the volume afterwards. */
 int tsdf_destroy(tsdf_volume* vol);
 
+/* The volume's parameters (design section, data structure: pool and table
+ * capacities; integration: the band's sample count). */
 int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out);
 
-/* Zero-copy access to the pool arrays (for read-out kernels of the caller). */
+/* Zero-copy access to the pool arrays, for read-out kernels of the caller
+ * (design section, accumulation: the arrays hold sums, and a reader forms the
+ * mean sum / weight itself). */
 int tsdf_get_pool(const tsdf_volume* vol, tsdf_pool_view* out);
 
 /* Empty the volume on `stream`: zero the used prefix of the pool (the first
  * min(blocks_allocated, pool_capacity) blocks' records and blue sums), empty the
- * table and zero every counter. */
+ * table and zero every counter.  This is the fresh volume each timed allocate
+ * starts from (measurement section: allocate is timed from an empty table;
+ * design section, data structure: an empty slot holds the all-ones key). */
 int tsdf_reset(tsdf_volume* vol, void* stream);
 
-/* Integrate one frame: tsdf_allocate followed by tsdf_update on `stream`. */
+/* Integrate one frame: tsdf_allocate followed by tsdf_update on `stream`
+ * (design section, integration: two kernels over the same points). */
 int tsdf_integrate(tsdf_volume* vol, const float* depth, const float* rgb, int width,
                    int height, const float K[4], const float pose[16], void* stream);
 
-/* The allocate kernel alone: make sure every block touched by a passing
- * sample of this frame exists in the table (keys are de-duplicated within a
+/* The allocate kernel alone (design section, integration: the irregular
+ * stage; the insert publishes a whole packed key with one compare-exchange):
+ * make sure every block touched by a passing sample of this frame exists in
+ * the table (keys are de-duplicated within a
  * warp before probing; a new key is claimed with one 64-bit compare-and-swap
  * and receives the next pool index).  Probing is unbounded up to the table
  * size; an insert that finds no slot counts probe_overflow, a key that finds
@@ -184,14 +208,18 @@ int tsdf_integrate(tsdf_volume* vol, const float* depth, const float* rgb, int w
 int tsdf_allocate(tsdf_volume* vol, const float* depth, int width, int height,
                   const float K[4], const float pose[16], void* stream);
 
-/* The update kernel alone: add (tsdf, 1, r, g, b) of every passing sample
- * into its voxel.  A sample whose block is absent or FAILED counts
+/* The update kernel alone (design section, integration: the regular stage,
+ * a lookup that almost always hits at the first probe and atomic additions
+ * into the five sums; accumulation: sums, not running means): add
+ * (tsdf, 1, r, g, b) of every passing sample into its voxel.  A sample whose block is absent or FAILED counts
  * missed_contributions.  Call it after tsdf_allocate of the same frame (on
  * the same stream) for the full integrate semantics. */
 int tsdf_update(tsdf_volume* vol, const float* depth, const float* rgb, int width,
                 int height, const float K[4], const float pose[16], void* stream);
 
-/* Integrate n_frames frames.  depth: device float32 [n_frames][height][width];
+/* Integrate n_frames frames (design section, integration, applied to each
+ * frame in turn; sums commute, accumulation).  depth: device float32
+ * [n_frames][height][width];
  * rgb: device float32 [n_frames][height][width][3]; K: host float[4] shared by
  * all frames; poses: host float[n_frames][16].  Frames are taken in groups of
  * up to max_frames_per_launch (tsdf_info): one allocate launch over the group,
@@ -208,13 +236,17 @@ int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, con
 /* The two stages of tsdf_integrate_batch separately, each over all n_frames
  * frames in launches of up to max_frames_per_launch frames: every allocate
  * launch of tsdf_allocate_batch, then (when called next on the same stream)
- * every update launch of tsdf_update_batch.  For timing the stages. */
+ * every update launch of tsdf_update_batch.  For timing the stages
+ * (measurement section: stages timed on their own; results section: the
+ * allocate stage's share of integrate). */
 int tsdf_allocate_batch(tsdf_volume* vol, int n_frames, const float* depth, int width,
                         int height, const float K[4], const float* poses, void* stream);
 int tsdf_update_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
                       int width, int height, const float K[4], const float* poses, void* stream);
 
-/* As tsdf_integrate_batch, but depth and rgb are HOST arrays.  Each group of
+/* As tsdf_integrate_batch, but depth and rgb are HOST arrays (design
+ * section, extraction: host transfers are kept apart from kernel time; this
+ * call overlaps them with the kernels instead).  Each group of
  * frames is copied into a double-buffered device staging area owned by the
  * volume on a separate copy stream, overlapping the copy of group g + 1 with
  * the kernels of group g.  For the copies to be asynchronous the host arrays must be
@@ -229,14 +261,21 @@ int tsdf_integrate_batch_host(tsdf_volume* vol, int n_frames, const float* depth
 
 /* Insert explicit block coordinates (device int32 [n][3]) through the same
  * de-duplicate / probe / compare-and-swap / pool-index path as the allocate
- * kernel.  Coordinates outside the key range count out_of_range_samples. */
+ * kernel (design section, integration: the insert; expressiveness section:
+ * the load-factor table, whose occupancies and clustered probe chains this
+ * reaches without a scene).  Coordinates outside the key range count out_of_range_samples. */
 int tsdf_allocate_blocks(tsdf_volume* vol, const int32_t* coords, uint32_t n, void* stream);
 
-/* Synchronise `stream` and return min(blocks_allocated, pool_capacity). */
+/* Synchronise `stream` and return min(blocks_allocated, pool_capacity): the
+ * number of allocated blocks, which the correctness section checks exactly
+ * against the reference (design section, occlusion: applying the test in
+ * both passes keeps this count consistent). */
 int tsdf_block_count(tsdf_volume* vol, void* stream, uint32_t* out);
 
 /* Copy pool blocks [first, first + count) to the host, after synchronising
- * `stream`: coords int32 [count][3] (block coordinates, recovered from the
+ * `stream` (design section, accumulation: the sums are read out and the mean
+ * is formed only then; extraction: the device-to-host copy is a separate
+ * step, not part of integrate): coords int32 [count][3] (block coordinates, recovered from the
  * table) and the five sums as separate arrays float32 [count][512] each.  Any
  * output pointer may be NULL to skip it.  first + count must not exceed
  * tsdf_block_count.  The first call that asks for tsdf, weight, r or g
@@ -258,11 +297,13 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
  * compiled into the library (TSDF_NOALLOC_MAX_BLOCKS blocks, 768 KB, held by
  * every GPU that loads the library until exit), so count must not exceed
  * TSDF_NOALLOC_MAX_BLOCKS (else TSDF_ERR_ARG, nothing done); first + count
- * must not exceed tsdf_block_count.  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) and should come before any
- * stream capture begins.  Every call shares the array: calls whose work
- * overlaps on the GPU (other streams, other threads) race.  Synchronises
- * `stream`. */
+ * must not exceed tsdf_block_count.  tsdf_create looks up the array's device
+ * address (cudaGetSymbolAddress) with the volume's device current and loads
+ * the export kernel, so that this call only uses them; a volume does not
+ * survive cudaDeviceReset (create a new one afterwards).  Every call shares
+ * the array and it keeps the last call's contents (each call clears the part
+ * it uses): calls whose work overlaps on the GPU (other streams, other
+ * threads) race.  Synchronises `stream`. */
 #define TSDF_NOALLOC_MAX_BLOCKS 65536u
 int tsdf_export_block_coords_noalloc(tsdf_volume* vol, void* stream, uint32_t first,
                                      uint32_t count, int32_t* coords);
@@ -295,7 +336,8 @@ int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uin
                            uint64_t* n_out);
 
 /* Set blocks from host arrays (restoring a saved volume, or loading a known
- * field): for each of the n block coordinates (int32 [n][3], all distinct),
+ * field; design section, accumulation: a volume's whole state is its block
+ * set and the five sums of each voxel): for each of the n block coordinates (int32 [n][3], all distinct),
  * ensure the block exists through the allocate kernel's insert path, then
  * overwrite its five sums with tsdf, weight, r, g, b (float32 [n][512]
  * each, voxel j = lx + 8 ly + 64 lz, the layout tsdf_export_blocks
@@ -309,21 +351,26 @@ int tsdf_import_blocks(tsdf_volume* vol, void* stream, uint32_t n, const int32_t
                        const float* tsdf, const float* weight, const float* r, const float* g,
                        const float* b);
 
-/* Copy the raw hash table to the host after synchronising `stream`: keys
+/* Copy the raw hash table to the host after synchronising `stream` (design
+ * section, data structure: the 16-byte entries with their packed keys and
+ * pool indices; for checking the table's structure and probe chains): keys
  * uint64 [table_capacity] (TSDF_EMPTY_KEY for an empty slot) and indices
  * uint32 [table_capacity].  `capacity` must equal the table capacity. Either
  * output may be NULL. */
 int tsdf_export_table(tsdf_volume* vol, void* stream, uint32_t capacity, uint64_t* keys,
                       uint32_t* indices);
 
-/* Synchronise `stream` and read the counters. */
+/* Synchronise `stream` and read the counters (correctness section: no point
+ * dropped and pool exhaustion reported; expressiveness section: dropped
+ * blocks counted rather than lost, probe depth). */
 int tsdf_get_stats(tsdf_volume* vol, void* stream, tsdf_stats* out);
 
-/* Zero the counters (not the pool counter, the table or the pool). */
+/* Zero the counters (not the pool counter, the table or the pool), as
+ * tsdf_get_stats reads them. */
 int tsdf_clear_stats(tsdf_volume* vol, void* stream);
 
 /* Turn probe instrumentation (probe_* statistics) on or off for later
- * launches.  It costs a shared-memory histogram per block of threads; keep it
+ * launches (expressiveness section: probe depth under load).  It costs a shared-memory histogram per block of threads; keep it
  * off when timing. */
 int tsdf_set_instrumentation(tsdf_volume* vol, int on);
 
@@ -332,7 +379,13 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
  * Irregularity Costs", design section, integration: the update adds tsdf, 1
  * and the pixel colour into the five sums for every passing sample); they
  * differ in how the additions reach memory:
- *   TSDF_UPDATE_PER_SAMPLE (the default): each thread walks one pixel's band
+ *   TSDF_UPDATE_AUTO (the default): TSDF_UPDATE_PER_SAMPLE, except that
+ *     calls which both allocate and update (tsdf_integrate and its batch
+ *     forms) run TSDF_UPDATE_FUSED's single kernel for launches of fewer than
+ *     2^19 pixels (frames x width x height), where the two kernels would not
+ *     fill the GPU and their latencies add up (same conditions as the fused
+ *     mode: ray-depth test, bands of at most 9 samples).
+ *   TSDF_UPDATE_PER_SAMPLE: each thread walks one pixel's band
  *     (16 x 16 pixel tiles, 8 x 4 per warp); at every band step the warp sums
  *     in registers the samples of its lanes that fall in the same voxel, and
  *     one lane adds them with two reductions (a 4-wide one into the voxel's
@@ -364,6 +417,7 @@ int tsdf_set_instrumentation(tsdf_volume* vol, int on);
 #define TSDF_UPDATE_PER_SAMPLE 1
 #define TSDF_UPDATE_PRE_REDUCED 2
 #define TSDF_UPDATE_FUSED 3
+#define TSDF_UPDATE_AUTO 4
 int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 
 /* The occlusion test of later allocate and update launches.  The design
@@ -404,7 +458,9 @@ int tsdf_set_occlusion(tsdf_volume* vol, int mode);
 #define TSDF_LAYOUT_PLANAR 1
 int tsdf_set_pool_layout(tsdf_volume* vol, int layout);
 
-/* Message of the last failure on the calling thread ("" if none). */
+/* Message of the last failure on the calling thread ("" if none); every
+ * call of this C ABI (design section, layout shared by the arms: a C ABI
+ * handing pointers across) reports failures by code and message. */
 const char* tsdf_last_error(void);
 
 #ifdef __cplusplus

@@ -137,6 +137,7 @@ def test_binding_constants_follow_the_header():
         "TSDF_UPDATE_PER_SAMPLE": binding.UPDATE_KERNELS["per_sample"],
         "TSDF_UPDATE_PRE_REDUCED": binding.UPDATE_KERNELS["pre_reduced"],
         "TSDF_UPDATE_FUSED": binding.UPDATE_KERNELS["fused"],
+        "TSDF_UPDATE_AUTO": binding.UPDATE_KERNELS["auto"],
         "TSDF_OCCLUSION_RAY": binding.OCCLUSION_TESTS["ray"],
         "TSDF_OCCLUSION_REPROJECT": binding.OCCLUSION_TESTS["reproject"],
         "TSDF_LAYOUT_INTERLEAVED": binding.POOL_LAYOUTS["interleaved"],

@@ -5,10 +5,12 @@ memory belongs to a caching allocator that has reserved nearly all of it, or
 they live under a fixed device-memory budget, or they run on threads that
 must not stall in cudaMalloc.  tsdf_export_block_coords_noalloc serves them
 from a scratch array compiled into the library.  This test calls it through
-the C ABI and checks that it returns exactly what the ordinary export
-(tsdf_export_blocks, which allocates its own buffer) returns, on two calls in
-a row and after a call on a different range (the scratch array is shared and
-keeps the last call's contents).  Block coordinates are integers, so the
+the C ABI on a fresh volume, first (before the ordinary export has run) and
+then again with the device's free memory unchanged across the call, and
+checks that it returns exactly what the ordinary export (tsdf_export_blocks,
+which allocates its own buffer) returns, on two calls in a row and after a
+call on a different range (the scratch array is shared and keeps the last
+call's contents).  Block coordinates are integers, so the
 comparison is exact.
 """
 import ctypes
@@ -34,7 +36,6 @@ def test_noalloc_coordinate_export_matches_the_allocating_export():
                   torch.from_numpy(frames.rgb[0]).cuda(), frames.K, frames.poses[0])
     n = vol.block_count()
     assert 0 < n <= binding.NOALLOC_MAX_BLOCKS
-    expected = vol.export_blocks(fields=("coords",))["coords"]
     stream = torch.cuda.current_stream().cuda_stream
 
     def call(first, count):
@@ -44,7 +45,20 @@ def test_noalloc_coordinate_export_matches_the_allocating_export():
         assert rc == 0, lib.tsdf_last_error()
         return out
 
-    np.testing.assert_array_equal(call(0, n), expected)
+    # on a fresh volume, before the allocating export has ever run: the first
+    # call, then a second one across which the device's free memory must not
+    # move (the allocating export would take a coordinate buffer here)
+    first_call = call(0, n)
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    second_call = call(0, n)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before, (free_before, free_after)
+    np.testing.assert_array_equal(first_call, second_call)
+
+    expected = vol.export_blocks(fields=("coords",))["coords"]
+    np.testing.assert_array_equal(first_call, expected)
     np.testing.assert_array_equal(call(0, n), expected)
     np.testing.assert_array_equal(call(17, 100), expected[17:117])
     np.testing.assert_array_equal(call(0, n), expected)
