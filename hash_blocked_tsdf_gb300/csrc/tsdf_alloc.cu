@@ -125,13 +125,17 @@ __device__ __forceinline__ bool allocate_visible(const VolumeView& vol, const Ca
 // b % n: the batch's frames are interleaved chunk by chunk.
 //
 // With kShort (bands of at most kShortBand samples) a thread first walks its
-// whole band and keeps the distinct block keys of its passing samples in a
-// small register list; the warp then runs one insert round per list entry
-// (usually two or three) instead of one per band sample.  Longer bands insert
-// step by step.  A sample whose block is the one its thread listed last is
-// not tested: whatever the test says, the list stays the same.  With
-// kReproject the occlusion test is the reprojection of the voxel centre
-// (reprojected_visible), as in the update it pairs with.
+// whole band and marks, in a bit mask, each band step whose sample passes
+// the occlusion test and lies in another block than the last passing sample
+// (a sample in the block of the last passing one is not tested: it cannot
+// add a block).  The samples of a ray move monotonically along each axis,
+// so a block once left never comes back and the marked steps are exactly
+// the first passing samples of the ray's distinct blocks.  The warp then
+// runs one insert round per marked step (usually two or three): each lane
+// recomputes the voxel of its next marked step (the same float operations,
+// hence the same voxel) and offers its block.  Longer bands insert step by
+// step.  With kReproject the occlusion test is the reprojection of the voxel
+// centre (reprojected_visible), as in the update it pairs with.
 template <bool kInstrument, bool kFast, bool kShort, bool kReproject>
 __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                                                            const __grid_constant__ FrameBatch fb)
@@ -152,43 +156,49 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
         const int u = pix - v * fb.width;
         valid = back_project(cam, vol.div, u, v, __ldg(depth + pix), p);
     }
-    const int steps = 2 * vol.band_half + 1;
-    unsigned long long last = kEmptyKey;
+    const int half = vol.band_half;
+    const int steps = 2 * half + 1;
     uint32_t out_of_range = 0;
     if (kShort) {
-        unsigned long long keys[kShortBand];
-        int n_keys = 0;
+        uint32_t starts = 0;                // band steps that start a new block
+        int lbx = 0, lby = 0, lbz = 0;      // block of the last passing sample
+        bool any = false;
 #pragma unroll
         for (int j = 0; j < kShortBand; ++j) {
-            keys[j] = kEmptyKey;
             if (valid && j < steps) {
                 VoxelSample s;
-                if (!band_voxel<kFast>(cam, vol.div, p, j - vol.band_half, s)) {
+                if (!band_voxel<kFast>(cam, vol.div, p, j - half, s)) {
                     ++out_of_range;
                 } else {
-                    const unsigned long long key = block_key(s.ix, s.iy, s.iz);
-                    // a sample of the block listed last cannot change the
-                    // list, so its occlusion test is skipped
-                    if (key != last && allocate_visible<kFast, kReproject>(
-                                           vol, cam, p, depth, fb.width, fb.height, s)) {
-                        // newest key first; static indices only
-#pragma unroll
-                        for (int m = kShortBand - 1; m > 0; --m) keys[m] = keys[m - 1];
-                        keys[0] = key;
-                        ++n_keys;
-                        last = key;
+                    const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
+                    if ((!any || bx != lbx || by != lby || bz != lbz) &&
+                        allocate_visible<kFast, kReproject>(vol, cam, p, depth, fb.width,
+                                                            fb.height, s)) {
+                        starts |= 1u << j;
+                        lbx = bx;
+                        lby = by;
+                        lbz = bz;
+                        any = true;
                     }
                 }
             }
         }
-        const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)n_keys);
+        const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)__popc(starts));
         for (int r = 0; r < rounds; ++r) {
-            warp_insert_step<kInstrument>(vol, r < n_keys, keys[0], &st);
-#pragma unroll
-            for (int m = 0; m < kShortBand - 1; ++m) keys[m] = keys[m + 1];
+            unsigned long long key = kEmptyKey;
+            const bool offer = starts != 0u;
+            if (offer) {
+                const int j = __ffs(starts) - 1;
+                starts &= starts - 1u;
+                VoxelSample s;
+                band_voxel<kFast>(cam, vol.div, p, j - half, s);
+                key = block_key(s.ix, s.iy, s.iz);
+            }
+            warp_insert_step<kInstrument>(vol, offer, key, &st);
         }
     } else {
-        for (int i = -vol.band_half; i <= vol.band_half; ++i) {
+        unsigned long long last = kEmptyKey;
+        for (int i = -half; i <= half; ++i) {
             unsigned long long key = kEmptyKey;
             if (valid) {
                 VoxelSample s;
@@ -302,58 +312,60 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
             cb = __ldg(rgb + 3 * pix + 2);
         }
     }
-    const int steps = 2 * vol.band_half + 1;
-    // distinct keys, newest first, each with the mask of its band steps; and
-    // per step the sample's voxel in its block, its tsdf and (after the
-    // insert rounds) its block's pool index
-    unsigned long long keys[kShortBand];
-    uint32_t masks[kShortBand];
+    const int half = vol.band_half;
+    const int steps = 2 * half + 1;
+    // per band step: the sample's voxel in its block, its tsdf and (after the
+    // insert rounds) its block's pool index; `passed` marks the steps whose
+    // sample passed, `starts` those that begin a new block (the samples of a
+    // ray move monotonically along each axis, so a block's passing samples
+    // are the passing steps from its start to the next start)
     int lv[kShortBand];
     float tv[kShortBand];
     uint32_t sidx[kShortBand];
-    int n_keys = 0;
-    unsigned long long last = kEmptyKey;
+    uint32_t passed = 0, starts = 0;
+    int lbx = 0, lby = 0, lbz = 0;
     uint32_t out_of_range = 0;
 #pragma unroll
     for (int j = 0; j < kShortBand; ++j) {
-        keys[j] = kEmptyKey;
-        masks[j] = 0;
         lv[j] = 0;
         tv[j] = 0.0f;
         sidx[j] = kIndexFailed;
         if (valid && j < steps) {
             VoxelSample s;
-            const int status = band_sample<kFast>(cam, vol.div, p, j - vol.band_half, s);
+            const int status = band_sample<kFast>(cam, vol.div, p, j - half, s);
             if (status == kSamplePass) {
                 lv[j] = local_voxel(s.ix, s.iy, s.iz);
                 tv[j] = s.tsdf;
-                const unsigned long long key = block_key(s.ix, s.iy, s.iz);
-                if (key != last) {          // static indices only
-#pragma unroll
-                    for (int m = kShortBand - 1; m > 0; --m) {
-                        keys[m] = keys[m - 1];
-                        masks[m] = masks[m - 1];
-                    }
-                    keys[0] = key;
-                    masks[0] = 1u << j;
-                    ++n_keys;
-                    last = key;
-                } else {
-                    masks[0] |= 1u << j;
+                const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
+                if (passed == 0u || bx != lbx || by != lby || bz != lbz) {
+                    starts |= 1u << j;
+                    lbx = bx;
+                    lby = by;
+                    lbz = bz;
                 }
+                passed |= 1u << j;
             } else if (status == kSampleOutOfRange) {
                 ++out_of_range;
             }
         }
     }
-    uint32_t passed = 0;                    // band steps whose sample passed
-#pragma unroll
-    for (int m = 0; m < kShortBand; ++m) passed |= masks[m];
     uint32_t updates = 0, timeouts = 0;
-    const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)n_keys);
+    const int rounds = (int)__reduce_max_sync(0xFFFFFFFFu, (unsigned)__popc(starts));
+    uint32_t rest = starts;
     for (int r = 0; r < rounds; ++r) {
-        const bool offered = r < n_keys;
-        const InsertResult ins = warp_insert_step<kInstrument>(vol, offered, keys[0], &st);
+        const bool offered = rest != 0u;
+        unsigned long long key = kEmptyKey;
+        uint32_t mine = 0;                  // this key's passing steps
+        if (offered) {
+            const int j = __ffs(rest) - 1;
+            rest &= rest - 1u;
+            const uint32_t from = 1u << j;
+            mine = passed & (rest ? (rest & (0u - rest)) - from : 0u - from);
+            VoxelSample s;
+            band_voxel<kFast>(cam, vol.div, p, j - half, s);
+            key = block_key(s.ix, s.iy, s.iz);
+        }
+        const InsertResult ins = warp_insert_step<kInstrument>(vol, offered, key, &st);
         __syncwarp();                       // this warp's winners have published
         if (offered) {
             uint32_t idx = kIndexFailed;
@@ -363,12 +375,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
             }
 #pragma unroll
             for (int j = 0; j < kShortBand; ++j)
-                if (masks[0] & (1u << j)) sidx[j] = idx;
-        }
-#pragma unroll
-        for (int m = 0; m < kShortBand - 1; ++m) {
-            keys[m] = keys[m + 1];
-            masks[m] = masks[m + 1];
+                if (mine & (1u << j)) sidx[j] = idx;
         }
     }
     // the update, one band step at a time for the whole warp

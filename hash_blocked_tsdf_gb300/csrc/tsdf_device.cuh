@@ -58,6 +58,18 @@ __device__ __forceinline__ bool back_project(const Camera& c, const DivisorPair&
     p.ex = __fadd_rn(__fadd_rn(__fmul_rn(c.r00, dx), __fmul_rn(c.r01, dy)), __fmul_rn(c.r02, dz));
     p.ey = __fadd_rn(__fadd_rn(__fmul_rn(c.r10, dx), __fmul_rn(c.r11, dy)), __fmul_rn(c.r12, dz));
     p.ez = __fadd_rn(__fadd_rn(__fmul_rn(c.r20, dx), __fmul_rn(c.r21, dy)), __fmul_rn(c.r22, dz));
+    // If any of p' and e is not finite (absurd depths or poses), every band
+    // sample has a non-finite coordinate on some axis (a non-finite p'
+    // component stays non-finite after adding a step; a non-finite e
+    // component gives 0 * inf = NaN at the middle step and +-inf or NaN at
+    // the others), so every sample is out of range.  The ray is replaced by
+    // one whose samples all lie at +inf in x, which band_voxel's integer
+    // range check rejects like the non-finite originals.
+    if (!(isfinite(p.vx) && isfinite(p.vy) && isfinite(p.vz) && isfinite(p.ex) &&
+          isfinite(p.ey) && isfinite(p.ez))) {
+        p.vx = INFINITY;
+        p.vy = p.vz = p.ex = p.ey = p.ez = 0.0f;
+    }
     return true;
 }
 
@@ -95,8 +107,8 @@ __device__ __forceinline__ float div_trunc(float x, float y, float r)
 }
 
 // Voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1].
-constexpr float kVoxelIndexMin = -8388608.0f;
-constexpr float kVoxelIndexMax = 8388607.0f;
+constexpr unsigned kVoxelIndexBias = 1u << 23;
+constexpr unsigned kVoxelIndexSpan = 1u << 24;
 
 // Camera-frame depth of the centre of voxel (ix, iy, iz):
 // z_c = (R^T (centre - t))_z = r02 * cx + r12 * cy + r22 * cz, with the
@@ -120,23 +132,21 @@ __device__ __forceinline__ float truncated_sdf(const DivisorPair& dv, float d, f
 
 // The voxel of band sample `i` (offset i voxels along the unit ray, i in
 // -k..k): the floor of p' + i e, and whether it lies in the packable range.
-// Out-of-range indices are clamped before the integer conversion and never
-// used.
+// The floor and the conversion to an integer are one round-toward-minus-
+// infinity conversion, which saturates values beyond the int32 range, so the
+// range test is an integer comparison; back_project guarantees finite p' and
+// e (or a ray whose every sample is rejected), so no coordinate is NaN.
 template <bool kFast>
 __device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
                                            const RayPoint& p, int i, VoxelSample& s)
 {
     const float fi = (float)i;
-    const float qx = floorf(__fadd_rn(p.vx, __fmul_rn(fi, p.ex)));
-    const float qy = floorf(__fadd_rn(p.vy, __fmul_rn(fi, p.ey)));
-    const float qz = floorf(__fadd_rn(p.vz, __fmul_rn(fi, p.ez)));
-    const bool in_range = qx >= kVoxelIndexMin && qx <= kVoxelIndexMax &&
-                          qy >= kVoxelIndexMin && qy <= kVoxelIndexMax &&
-                          qz >= kVoxelIndexMin && qz <= kVoxelIndexMax;
-    s.ix = (int)fminf(fmaxf(qx, kVoxelIndexMin), kVoxelIndexMax);
-    s.iy = (int)fminf(fmaxf(qy, kVoxelIndexMin), kVoxelIndexMax);
-    s.iz = (int)fminf(fmaxf(qz, kVoxelIndexMin), kVoxelIndexMax);
-    return in_range;
+    s.ix = __float2int_rd(__fadd_rn(p.vx, __fmul_rn(fi, p.ex)));
+    s.iy = __float2int_rd(__fadd_rn(p.vy, __fmul_rn(fi, p.ey)));
+    s.iz = __float2int_rd(__fadd_rn(p.vz, __fmul_rn(fi, p.ez)));
+    return ((unsigned)s.ix + kVoxelIndexBias < kVoxelIndexSpan) &
+           ((unsigned)s.iy + kVoxelIndexBias < kVoxelIndexSpan) &
+           ((unsigned)s.iz + kVoxelIndexBias < kVoxelIndexSpan);
 }
 
 // The occlusion test of the sample in voxel s against its own ray's depth:

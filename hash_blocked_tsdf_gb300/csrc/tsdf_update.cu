@@ -108,7 +108,8 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
         }
     }
     uint32_t updates = 0, missed = 0;
-    unsigned long long last = kEmptyKey;
+    int lbx = 0, lby = 0, lbz = 0;          // block of the last lookup
+    bool looked_up = false;
     uint32_t idx = kIndexFailed;
     // every lane runs every band step (the warp merges each step's samples)
     for (int i = -vol.band_half; i <= vol.band_half; ++i) {
@@ -132,10 +133,13 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                 status = band_sample<kFast>(cam, vol.div, p, i, s);
             }
             if (status == kSamplePass) {
-                const unsigned long long key = block_key(s.ix, s.iy, s.iz);
-                if (key != last) {
-                    idx = lookup(vol.table, vol.table_mask, key);
-                    last = key;
+                const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
+                if (!looked_up || bx != lbx || by != lby || bz != lbz) {
+                    idx = lookup(vol.table, vol.table_mask, pack_block(bx, by, bz));
+                    lbx = bx;
+                    lby = by;
+                    lbz = bz;
+                    looked_up = true;
                 }
                 if (idx < vol.pool_capacity) {
                     // (pool indices are below 2^23, so e fits in 32 bits)
