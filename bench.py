@@ -70,10 +70,17 @@ def parse_args():
     ap.add_argument("--sweep", action="store_true",
                     help="run the measurement matrix (one JSON line per cell) instead of the "
                          "headline workload")
+    ap.add_argument("--probe-report", action="store_true",
+                    help="print the probe-depth histogram at table occupancy 0.1 .. 0.5 "
+                         "(untimed) instead of the headline workload")
     ap.add_argument("--pool", type=int, default=0,
                     help="override the workload's pool capacity in blocks (small profiling runs)")
-    ap.add_argument("--update-kernel", choices=["adaptive", "per_sample", "pre_reduced", "fused"],
-                    default="per_sample", help="how the library's update reaches the pool")
+    ap.add_argument("--update-kernel",
+                    choices=["auto", "adaptive", "per_sample", "pre_reduced", "fused"],
+                    default="auto",
+                    help="how the library's update reaches the pool (auto, the library's "
+                         "default, times like per_sample here: the stages are timed as "
+                         "separate calls)")
     ap.add_argument("--layout", choices=["interleaved", "planar"], default="interleaved",
                     help="pool layout: tsdf, weight, r, g interleaved per voxel (default) or "
                          "five separate arrays")
@@ -440,14 +447,14 @@ def run_sweep(args):
         vol = TsdfVolume(fr.pool_capacity, fr.voxel_size, fr.trunc, fr.table_capacity)
         clocks = ClockSampler(dev)
         clocks.start()
-        times = {"allocate": [], "update": [], "fused": []}
+        times = {"allocate": [], "update": [], "fused": [], "auto": []}
         for r in range(reps + 3):
-            for mode in ("per_sample", "fused"):
+            for mode in ("per_sample", "fused", "auto"):
                 vol.set_update_kernel(mode)
                 vol.reset()
                 ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
                 ev[0].record(stream)
-                if mode == "fused":
+                if mode in ("fused", "auto"):
                     vol.integrate_batch(d, c, fr.K, fr.poses)
                     ev[1].record(stream)
                 else:
@@ -457,8 +464,8 @@ def run_sweep(args):
                 ev[2].record(stream)
                 torch.cuda.synchronize()
                 if r >= 3:
-                    if mode == "fused":
-                        times["fused"].append(ev[0].elapsed_time(ev[1]))
+                    if mode in ("fused", "auto"):
+                        times[mode].append(ev[0].elapsed_time(ev[1]))
                     else:
                         times["allocate"].append(ev[0].elapsed_time(ev[1]))
                         times["update"].append(ev[1].elapsed_time(ev[2]))
@@ -481,7 +488,70 @@ def run_sweep(args):
             "fused_ms": _percentiles(times["fused"]),
             "points_per_s": pts / (float(np.median(total)) / 1e3),
             "points_per_s_fused": pts / (float(np.median(times["fused"])) / 1e3),
+            "points_per_s_integrate_default": pts / (float(np.median(times["auto"])) / 1e3),
+            "integrate_default_ms": _percentiles(times["auto"]),
             "clocks": clk}), flush=True)
+    for rec in probe_depth_report(torch):
+        print(json.dumps({"sweep": "probe_depth", **rec}), flush=True)
+
+
+def probe_depth_report(torch, targets=(0.1, 0.2, 0.3, 0.4, 0.5), n_frames: int = 100):
+    """Probe depth against table occupancy (the load-factor configuration:
+    the orbit scene into fixed tables).  For each target occupancy the orbit
+    is integrated frame by frame into a fixed table (2^17 slots below 0.25,
+    2^16 above) until the block count reaches it; 0.5, beyond what the
+    orbit allocates in 2^16 slots, is reached by topping the table up with
+    blocks far from the scene through the same insert path.  Then every
+    stored key is looked up again through the insert path with the probe
+    instrumentation on: each probe is a successful search, and its length is
+    the key's displacement + 1.  Reports the probe-length histogram, mean and
+    maximum beside Knuth's expected successful-search cost for random keys,
+    (1 + 1 / (1 - alpha)) / 2 (TAOCP vol. 3, 6.4), and the counters that
+    show nothing was dropped.  Untimed."""
+    from hash_blocked_tsdf_gb300 import TsdfVolume, scenes
+    frames = scenes.orbit_trajectory(n_frames=n_frames)
+    d = torch.from_numpy(frames.depth).cuda()
+    c = torch.from_numpy(frames.rgb).cuda()
+    out = []
+    for target in targets:
+        T = 1 << 17 if target < 0.25 else 1 << 16
+        vol = TsdfVolume(T // 2, frames.voxel_size, frames.trunc, T)
+        f = 0
+        while f < frames.n_frames and vol.block_count() < target * T:
+            vol.integrate(d[f], c[f], frames.K, frames.poses[f])
+            f += 1
+        B = vol.block_count()
+        topped = 0
+        if B < target * T:
+            want = int(round(target * T)) - B
+            g = np.stack(np.meshgrid(np.arange(1000, 1064), np.arange(0, 64),
+                                     np.arange(0, 64), indexing="ij"), -1).reshape(-1, 3)[:want]
+            vol.allocate_blocks(torch.from_numpy(np.ascontiguousarray(g, np.int32)).cuda())
+            topped = int(g.shape[0])
+            B = vol.block_count()
+        st_build = vol.stats()
+        coords = vol.export_blocks(fields=("coords",))["coords"]
+        vol.clear_stats()
+        vol.set_instrumentation(True)
+        vol.allocate_blocks(torch.from_numpy(np.ascontiguousarray(coords)).cuda())
+        torch.cuda.synchronize()
+        st = vol.stats()
+        vol.close()
+        alpha = B / T
+        hist = [int(x) for x in st["probe_hist"]]
+        while len(hist) > 1 and hist[-1] == 0:
+            hist.pop()
+        out.append({
+            "target_occupancy": target, "table_capacity": T, "frames_integrated": f,
+            "blocks_from_far_topping": topped, "blocks": B, "occupancy": alpha,
+            "probes": st["probe_inserts"], "probe_mean": st["probe_steps"] / max(1, st["probe_inserts"]),
+            "probe_max": st["probe_max"],
+            "knuth_successful_search_mean": 0.5 * (1.0 + 1.0 / (1.0 - alpha)),
+            "probe_hist_len1_up": hist,
+            "pool_exhausted": st_build["pool_exhausted"], "probe_overflow": st_build["probe_overflow"],
+            "blocks_added_by_the_lookup_pass": st["blocks_allocated"] - B,
+        })
+    return out
 
 
 def _percentiles(xs) -> dict:
@@ -712,12 +782,15 @@ def run_ours(args):
     bytes_per_launch = (16.0 * points_per_step + 40.0 * u_frames) / ng
     achieved = bytes_per_launch / (upd_ms_avg / 1000.0) / 1e9
     # the kernels the update stage launches in the selected mode
-    upd_kernel = {"per_sample": "update_kernel", "pre_reduced": "update_rows_kernel",
+    upd_kernel = {"per_sample": "update_kernel", "auto": "update_kernel",
+                  "pre_reduced": "update_rows_kernel",
                   "adaptive": "update_kernel+update_rows_kernel",
                   "fused": "integrate_fused_kernel"}[args.update_kernel]
     if args.occlusion == "reproject":
         upd_kernel = "update_kernel (reprojection test)"
     mode = args.update_kernel if args.occlusion == "ray" else "reproject"
+    if mode == "auto":
+        mode = "per_sample"         # the stage calls run the per-sample update
     if args.layout == "planar":
         mode += "_planar"
     prof_upd = _profile_record(f"update_{mode}_room_walk_1280x720.md",
@@ -738,14 +811,32 @@ def run_ours(args):
         "units": "per frame: 16 B per valid point + 40 B per distinct voxel of the frame",
     }
     adds_alg = 5.0 * u_frames / ng
+    red_peak_l2 = max(v["adds_per_s"] for v in red_peaks["l2_32MB"].values())
+    add_rate = adds_alg / (upd_ms_avg / 1000.0)
     red_roof = {
         "bound": "l2_red", "kernel": upd_kernel, "unit": "float adds/s",
-        "achieved": adds_alg / (upd_ms_avg / 1000.0), "peak": red_peak,
-        "frac": adds_alg / (upd_ms_avg / 1000.0) / red_peak,
+        "achieved": add_rate, "peak": red_peak, "frac": add_rate / red_peak,
+        "peak_l2_resident": red_peak_l2, "frac_l2_resident": add_rate / red_peak_l2,
         "algorithmic_adds_per_launch": adds_alg,
         "issued_adds_per_launch": 5.0 * updates_per_step / ng,
-        "peak_source": "measured live: best red.global.add pattern, 4 GB footprint",
+        "peak_source": "measured live: best red.global.add pattern, 4 GB footprint "
+                       "(peak_l2_resident: best pattern, 32 MB footprint)",
         "probe": red_peaks,
+    }
+    # the binding resource: L2 reduction requests.  Sectors the kernel sends
+    # (ncu, per launch, while the source matches the capture) per second of
+    # the live launch time, against the measured rate of scattered 4-wide
+    # reductions into L2-resident lines (one sector each)
+    req_peak = red_peaks["l2_32MB"]["v4_scattered"]["ops_per_s"]
+    sectors = (_per_launch(prof_upd, "l2_red_sectors_per_launch", n / ng)
+               if same_shape else None)
+    red_requests = {
+        "bound": "l2_red_requests", "kernel": upd_kernel, "unit": "sectors/s",
+        "peak": req_peak,
+        "peak_source": "measured live: scattered red.global.add.v4.f32, 32 MB footprint",
+        "sectors_per_launch": sectors,
+        "achieved": None if sectors is None else sectors / (upd_ms_avg / 1000.0),
+        "frac": None if sectors is None else sectors / (upd_ms_avg / 1000.0) / req_peak,
     }
     t_hbm = bytes_per_launch / (hbm_peak * 1e9)
     t_red = adds_alg / red_peak
@@ -821,6 +912,7 @@ def run_ours(args):
                                               for a, b in groups)),
         "roofline": roofline,
         "roofline_l2_red": red_roof,
+        "roofline_l2_red_requests": red_requests,
         "roofline_update_combined": combined,
         "roofline_update_launch_union": union,
         "roofline_allocate": alloc_roof,
@@ -1046,7 +1138,8 @@ def _profile_record(name: str, sources) -> dict:
         return {}
     out = {}
     for k in ("traffic_bytes_per_launch", "warp_instructions_per_launch",
-              "l2_atomic_sectors_per_launch", "frames_per_captured_launch"):
+              "l2_atomic_sectors_per_launch", "l2_red_sectors_per_launch",
+              "frames_per_captured_launch"):
         if k in rec:
             out[k] = float(rec[k])
     return out
@@ -1132,6 +1225,13 @@ def main():
     args = parse_args()
     if args.sweep:
         run_sweep(args)
+        return
+    if args.probe_report:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        for rec in probe_depth_report(torch):
+            print(json.dumps({"probe_depth": rec}), flush=True)
         return
     if args.impl == "reference":
         run_reference(args)

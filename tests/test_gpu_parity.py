@@ -72,7 +72,7 @@ def test_smoke_entry(torch_cuda):
     __graft_entry__.smoke()
 
 
-KERNELS = ["adaptive", "pre_reduced", "per_sample", "fused"]
+KERNELS = ["adaptive", "pre_reduced", "per_sample", "fused", "auto"]
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
@@ -485,8 +485,10 @@ def test_adversarial_clustered_keys(torch_cuda, oracle_mod):
     mean_disp = _check_table_structure(oracle_mod, vol, coords)
     assert mean_disp > want / 2 - T // 64
     assert st["probe_inserts"] > 0 and st["probe_max"] > 1000
+    hist = list(st["probe_hist"])
     print("adversarial: mean displacement", mean_disp, "probe max", st["probe_max"],
-          "mean probe", st["probe_steps"] / st["probe_inserts"])
+          "mean probe", st["probe_steps"] / st["probe_inserts"], "probes", st["probe_inserts"],
+          "histogram (lengths 1..31, 32+)", hist)
     vol.close()
 
 
