@@ -163,17 +163,26 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
         uint32_t starts = 0;                // band steps that start a new block
         int lbx = 0, lby = 0, lbz = 0;      // block of the last passing sample
         bool any = false;
+        // band steps whose ray-depth test provably passes are not tested
+        SurePass sure = {-INFINITY, false};
+        if (!kReproject && valid) sure = sure_pass(cam, vol.div, p, half);
+        const float fhalf = (float)half;
 #pragma unroll
         for (int j = 0; j < kShortBand; ++j) {
             if (valid && j < steps) {
                 VoxelSample s;
-                if (!band_voxel<kFast>(cam, vol.div, p, j - half, s)) {
+                // the step j - half as a float: exact, with no integer
+                // conversion per step
+                const float fi = __fsub_rn((float)j, fhalf);
+                if (!band_voxel_f<kFast>(p, fi, s)) {
                     ++out_of_range;
                 } else {
                     const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
+                    const bool proven = !kReproject && sure.near &&
+                                        fmaxf(fi, 0.0f) <= sure.i_max;
                     if ((!any || bx != lbx || by != lby || bz != lbz) &&
-                        allocate_visible<kFast, kReproject>(vol, cam, p, depth, fb.width,
-                                                            fb.height, s)) {
+                        (proven || allocate_visible<kFast, kReproject>(vol, cam, p, depth,
+                                                                       fb.width, fb.height, s))) {
                         starts |= 1u << j;
                         lbx = bx;
                         lby = by;
@@ -314,6 +323,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     }
     const int half = vol.band_half;
     const int steps = 2 * half + 1;
+    const float fhalf = (float)half;
     // per band step: the sample's voxel in its block, its tsdf and (after the
     // insert rounds) its block's pool index; `passed` marks the steps whose
     // sample passed, `starts` those that begin a new block (the samples of a
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
         sidx[j] = kIndexFailed;
         if (valid && j < steps) {
             VoxelSample s;
-            const int status = band_sample<kFast>(cam, vol.div, p, j - half, s);
+            const int status = band_sample<kFast>(cam, vol.div, p, __fsub_rn((float)j, fhalf), s);
             if (status == kSamplePass) {
                 lv[j] = local_voxel(s.ix, s.iy, s.iz);
                 tv[j] = s.tsdf;

@@ -137,16 +137,58 @@ __device__ __forceinline__ float truncated_sdf(const DivisorPair& dv, float d, f
 // range test is an integer comparison; back_project guarantees finite p' and
 // e (or a ray whose every sample is rejected), so no coordinate is NaN.
 template <bool kFast>
-__device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
-                                           const RayPoint& p, int i, VoxelSample& s)
+__device__ __forceinline__ bool band_voxel_f(const RayPoint& p, float fi, VoxelSample& s)
 {
-    const float fi = (float)i;
     s.ix = __float2int_rd(__fadd_rn(p.vx, __fmul_rn(fi, p.ex)));
     s.iy = __float2int_rd(__fadd_rn(p.vy, __fmul_rn(fi, p.ey)));
     s.iz = __float2int_rd(__fadd_rn(p.vz, __fmul_rn(fi, p.ez)));
     return ((unsigned)s.ix + kVoxelIndexBias < kVoxelIndexSpan) &
            ((unsigned)s.iy + kVoxelIndexBias < kVoxelIndexSpan) &
            ((unsigned)s.iz + kVoxelIndexBias < kVoxelIndexSpan);
+}
+
+// The same with the step as an int (i converts exactly: |i| <= 127).
+template <bool kFast>
+__device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
+                                           const RayPoint& p, int i, VoxelSample& s)
+{
+    return band_voxel_f<kFast>(p, (float)i, s);
+}
+
+// Which band steps of a ray provably pass the ray-depth occlusion test,
+// before it is evaluated (the allocate kernel skips it there).  In exact
+// arithmetic, with R a rotation, sample i of the ray lies at camera depth
+// d + i voxel dz (dz <= 1 the ray's z direction), and the centre of its voxel
+// lies within half a voxel diagonal, (sqrt(3) / 2) voxel, of it; so the
+// centre's depth is at most d + (max(i, 0) + sqrt(3) / 2) voxel and at least
+// d - (k + sqrt(3) / 2) voxel.  The test (centre depth > 0 and
+// d - centre depth >= -trunc) therefore passes when
+//     max(i, 0) + sqrt(3) / 2 + e <= trunc / voxel   and
+//     d / voxel > k + sqrt(3) / 2 + e,
+// where e bounds, in voxels, every rounding of the float32 walk and test:
+// each of the ~20 operations from the pose to the centre's depth errs by at
+// most 2^-24 of its operands, whose magnitudes are at most
+// m = |p'|_1 + 2k + 2 (the ray in voxel units) plus the camera position
+// |t|_1 / voxel, so e = (64 * 2^-24 + 4 * defect) (m + |t|_1 / voxel), with
+// defect = max |R^T R - I| covering a pose that is not exactly a rotation
+// (above 1e-3 no band step is proven).  Returns the largest provably passing
+// max(i, 0) (in voxels; -inf when none) and whether the near side holds.
+struct SurePass {
+    float i_max;
+    bool near;
+};
+
+__device__ __forceinline__ SurePass sure_pass(const Camera& c, const DivisorPair& dv,
+                                              const RayPoint& p, int half)
+{
+    const float m = fabsf(p.vx) + fabsf(p.vy) + fabsf(p.vz) + (float)(2 * half + 2);
+    const float e = c.sure_err * (m + c.sure_tmag);
+    SurePass r;
+    r.i_max = c.sure_tau - e;
+    // d / voxel through the reciprocal (relative error 2^-23 at most), with
+    // margin for it
+    r.near = __fmul_rn(p.d, dv.inv_voxel) * 0.999999f > (float)half + c.sure_near + e;
+    return r;
 }
 
 // The occlusion test of the sample in voxel s against its own ray's depth:
@@ -166,13 +208,21 @@ __device__ __forceinline__ bool ray_visible(const Camera& c, const DivisorPair& 
 // quantity is computed and the status is selected at the end.
 template <bool kFast>
 __device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
-                                           const RayPoint& p, int i, VoxelSample& s)
+                                           const RayPoint& p, float fi, VoxelSample& s)
 {
-    const bool in_range = band_voxel<kFast>(c, dv, p, i, s);
+    const bool in_range = band_voxel_f<kFast>(p, fi, s);
     float zc;
     const bool visible = ray_visible(c, dv, p, s, zc);
     s.tsdf = truncated_sdf<kFast>(dv, p.d, zc);
     return !in_range ? kSampleOutOfRange : (visible ? kSamplePass : kSampleOccluded);
+}
+
+// The same with the step as an int (converted exactly: |i| <= 127).
+template <bool kFast>
+__device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
+                                           const RayPoint& p, int i, VoxelSample& s)
+{
+    return band_sample<kFast>(c, dv, p, (float)i, s);
 }
 
 // The occlusion test by reprojection (selected per volume; the alternative

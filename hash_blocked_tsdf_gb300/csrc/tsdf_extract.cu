@@ -19,12 +19,14 @@
 //     (E(o,a), E(o,b), E(o,c)); two inside i1, i2 and two outside o1, o2:
 //     (E(i1,o1), E(i1,o2), E(i2,o2)) and (E(i1,o1), E(i2,o2), E(i2,o1)).
 //
-// One block of 256 threads per allocated block: the block's 512 means go to
-// shared memory, its seven upper neighbours (+x, +y, +z and their
-// combinations) are looked up in the table once, and each thread marches two
-// cells, reading corners that fall in a neighbour from the pool.  Threads
-// count their triangles first; a warp takes one range of the output with one
-// atomic and each thread writes its triangles there.
+// One block of 256 threads per allocated block: its seven upper neighbours
+// (+x, +y, +z and their combinations) are looked up in the table once; the
+// block's 512 means and the 217 lattice points its cells take from those
+// neighbours go to shared memory (9 x 9 x 9, NaN where unobserved); each
+// thread classifies two cells by the sign mask of their corners and counts
+// their triangles from it; a warp takes one range of the output with one
+// atomic, and each thread writes the triangles of its crossed cells there,
+// skipping tetrahedra the surface does not cross.
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -162,21 +164,50 @@ __device__ __forceinline__ Tet make_tet(const float f[8], int tet)
     return T;
 }
 
+// The block's lattice with its upper neighbours' first layer: 9 x 9 x 9
+// points, x fastest (index lx + 9 ly + 81 lz); a point's value is the mean
+// tsdf / weight, and NaN marks an unobserved point.
+constexpr int kLat = 9;
+constexpr int kLatPoints = kLat * kLat * kLat;          // 729
+constexpr int kHaloPoints = kLatPoints - kBlockVoxels;  // 217
+
+// Bit mask (bit k = corner k, k = 0..7) of the cube corners of tetrahedron
+// `tet` (tet_corner's sets).
+__device__ __forceinline__ uint32_t tet_corner_mask(int tet)
+{
+    return (1u << tet_corner(tet, 0)) | (1u << tet_corner(tet, 1)) | (1u << tet_corner(tet, 2)) |
+           (1u << tet_corner(tet, 3));
+}
+
+// Triangles of a fully observed cell whose inside corners are `mask` (bit k =
+// corner k < 0): per tetrahedron, one when one or three of its corners are
+// inside, two when two are.
+__device__ __forceinline__ int cell_triangles(uint32_t mask)
+{
+    int n = 0;
+#pragma unroll
+    for (int tet = 0; tet < 6; ++tet) {
+        const int k = __popc(mask & tet_corner_mask(tet));
+        n += k == 2 ? 2 : (k == 1 || k == 3) ? 1 : 0;
+    }
+    return n;
+}
+
+// Lattice index of corner k of the cell at (lx, ly, lz).
+__device__ __forceinline__ int corner_point(int base, int k)
+{
+    return base + (k & 1) + ((k >> 1) & 1) * kLat + ((k >> 2) & 1) * kLat * kLat;
+}
+
 __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const int32_t* coords,
                                                           float* out, uint64_t capacity,
                                                           unsigned long long* count)
 {
-    __shared__ float s_mean[kBlockVoxels];
-    __shared__ uint8_t s_seen[kBlockVoxels];
-    __shared__ uint32_t s_nb[8];                 // pool index of block + (d & 1, d >> 1 & 1, d >> 2 & 1)
+    __shared__ float s_lat[kLatPoints];
+    __shared__ uint32_t s_nb[8];        // pool index of block + (d & 1, d >> 1 & 1, d >> 2 & 1)
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
     const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
-    for (int j = t; j < kBlockVoxels; j += kThreads) {
-        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + j);
-        s_seen[j] = tw.y > 0.0f ? 1 : 0;
-        s_mean[j] = tw.y > 0.0f ? __fdiv_rn(tw.x, tw.y) : 0.0f;
-    }
     if (t < 8) {
         uint32_t idx = kIndexFailed;
         if (t == 0) {
@@ -189,58 +220,63 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
         }
         s_nb[t] = idx;
     }
+    // the block's own 512 means
+    for (int j = t; j < kBlockVoxels; j += kThreads) {
+        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + j);
+        s_lat[(j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat] =
+            tw.y > 0.0f ? __fdiv_rn(tw.x, tw.y) : __int_as_float(0x7FFFFFFF);
+    }
+    __syncthreads();
+    // the upper neighbours' first layers: +x face, +y face, +z face (64 points
+    // each), the three edges (8 each) and the corner
+    if (t < kHaloPoints) {
+        int d, lx, ly, lz;                  // neighbour, and the lattice point (0..8)
+        if (t < 64) {
+            d = 1; lx = 8; ly = t & 7; lz = t >> 3;
+        } else if (t < 128) {
+            d = 2; lx = (t - 64) & 7; ly = 8; lz = (t - 64) >> 3;
+        } else if (t < 192) {
+            d = 4; lx = (t - 128) & 7; ly = (t - 128) >> 3; lz = 8;
+        } else if (t < 200) {
+            d = 3; lx = 8; ly = 8; lz = t - 192;
+        } else if (t < 208) {
+            d = 5; lx = 8; ly = t - 200; lz = 8;
+        } else if (t < 216) {
+            d = 6; lx = t - 208; ly = 8; lz = 8;
+        } else {
+            d = 7; lx = 8; ly = 8; lz = 8;
+        }
+        float v = __int_as_float(0x7FFFFFFF);
+        const uint32_t nb = s_nb[d];
+        if (nb < vol.pool_capacity) {
+            const int jj = (lx & 7) | ((ly & 7) << 3) | ((lz & 7) << 6);
+            const float2 tw = tsdf_and_weight(vol, (size_t)nb * kBlockVoxels + jj);
+            if (tw.y > 0.0f) v = __fdiv_rn(tw.x, tw.y);
+        }
+        s_lat[lx + ly * kLat + lz * kLat * kLat] = v;
+    }
     __syncthreads();
 
-    // the two cells of this thread: corner values, observed or not; ok[c]
-    // marks a cell that is fully observed and crosses the surface
+    // the two cells of this thread: the sign mask of their corners; a cell is
+    // used when all 8 corners are observed and the surface crosses it
     const float voxel = vol.div.voxel;
-    float f[2][8];
-    bool ok[2];
+    uint32_t mask[2];
+    int base[2];
     int n_tris = 0;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int j = t + c * kThreads;
-        const int l[3] = {j & 7, (j >> 3) & 7, j >> 6};
-        ok[c] = true;
+        base[c] = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
+        uint32_t m = 0;
+        bool seen = true;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            int q[3], d = 0;
-#pragma unroll
-            for (int ax = 0; ax < 3; ++ax) {
-                q[ax] = l[ax] + ((k >> ax) & 1);
-                if (q[ax] == kBlockEdge) {
-                    q[ax] = 0;
-                    d |= 1 << ax;
-                }
-            }
-            const int jj = q[0] | (q[1] << 3) | (q[2] << 6);
-            float v = 0.0f;
-            bool seen;
-            if (d == 0) {
-                seen = s_seen[jj] != 0;
-                v = s_mean[jj];
-            } else {
-                const uint32_t nb = s_nb[d];
-                seen = false;
-                if (nb < vol.pool_capacity) {
-                    const float2 tw = tsdf_and_weight(vol, (size_t)nb * kBlockVoxels + jj);
-                    seen = tw.y > 0.0f;
-                    if (seen) v = __fdiv_rn(tw.x, tw.y);
-                }
-            }
-            ok[c] = ok[c] && seen;
-            f[c][k] = v;
+            const float v = s_lat[corner_point(base[c], k)];
+            seen = seen && !isnan(v);
+            m |= (v < 0.0f ? 1u : 0u) << k;
         }
-        // a cell whose corners are all inside or all outside holds no surface
-        int n_neg = 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) n_neg += f[c][k] < 0.0f ? 1 : 0;
-        ok[c] = ok[c] && n_neg != 0 && n_neg != 8;
-        if (ok[c]) {
-#pragma unroll 1
-            for (int tet = 0; tet < 6; ++tet)
-                n_tris += mask_triangles(inside_mask(make_tet(f[c], tet)));
-        }
+        mask[c] = (seen && m != 0u && m != 0xFFu) ? m : 0u;
+        if (mask[c]) n_tris += cell_triangles(mask[c]);
     }
 
     // one output range per warp
@@ -251,22 +287,25 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
         const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
         if ((int)lane >= d) incl += y;
     }
-    unsigned long long base = 0;
-    if (lane == 31 && incl) base = atomicAdd(count, (unsigned long long)incl);
-    base = __shfl_sync(0xFFFFFFFFu, base, 31);
-    uint64_t next = base + incl - (uint32_t)n_tris;
+    unsigned long long first = 0;
+    if (lane == 31 && incl) first = atomicAdd(count, (unsigned long long)incl);
+    first = __shfl_sync(0xFFFFFFFFu, first, 31);
+    uint64_t next = first + incl - (uint32_t)n_tris;
 #pragma unroll 1
     for (int c = 0; c < 2; ++c) {
-        if (!ok[c]) continue;
+        if (!mask[c]) continue;
         const int j = t + c * kThreads;
         const int cell[3] = {bc[0] * kBlockEdge + (j & 7), bc[1] * kBlockEdge + ((j >> 3) & 7),
                              bc[2] * kBlockEdge + (j >> 6)};
         float fc[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) fc[k] = c == 0 ? f[0][k] : f[1][k];
+        for (int k = 0; k < 8; ++k) fc[k] = s_lat[corner_point(base[c], k)];
 #pragma unroll 1
-        for (int tet = 0; tet < 6; ++tet)
+        for (int tet = 0; tet < 6; ++tet) {
+            const int k = __popc(mask[c] & tet_corner_mask(tet));
+            if (k == 0 || k == 4) continue;     // no surface in this tetrahedron
             next = emit_tet(make_tet(fc, tet), cell, voxel, out, capacity, next);
+        }
     }
 }
 

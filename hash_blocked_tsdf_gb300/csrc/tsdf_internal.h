@@ -45,6 +45,14 @@ struct Camera {
     float fx, fy, cx, cy;
     float r00, r01, r02, r10, r11, r12, r20, r21, r22;   // R, row-major
     float tx, ty, tz;                                   // t
+    // Bounds with which the allocate kernel proves, before testing, that a
+    // band sample passes the ray-depth occlusion test (sure_pass in
+    // tsdf_device.cuh; computed on the host from the pose, the voxel edge
+    // and the truncation, each rounded towards the safe side):
+    float sure_tau;     // trunc / voxel - (sqrt(3) / 2) |R column 2| - 1e-3; -inf: never
+    float sure_near;    // (sqrt(3) / 2) |R column 2| + 1e-2
+    float sure_err;     // 64 * 2^-24 + 4 * max |R^T R - I|: rounding per voxel of magnitude
+    float sure_tmag;    // (|tx| + |ty| + |tz|) / voxel
 };
 
 // The two divisors of the walk with their float reciprocals.

@@ -111,8 +111,10 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     int lbx = 0, lby = 0, lbz = 0;          // block of the last lookup
     bool looked_up = false;
     uint32_t idx = kIndexFailed;
-    // every lane runs every band step (the warp merges each step's samples)
-    for (int i = -vol.band_half; i <= vol.band_half; ++i) {
+    // every lane runs every band step (the warp merges each step's samples);
+    // the step also counts as a float, exactly, to spare a conversion per step
+    float fi = -(float)vol.band_half;
+    for (int i = -vol.band_half; i <= vol.band_half; ++i, fi = __fadd_rn(fi, 1.0f)) {
         VoxelSample s;
         s.tsdf = 0.0f;
         bool add = false;
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                     cb = __ldg(rgb + 3 * q + 2);
                 }
             } else {
-                status = band_sample<kFast>(cam, vol.div, p, i, s);
+                status = band_sample<kFast>(cam, vol.div, p, fi, s);
             }
             if (status == kSamplePass) {
                 const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdio>
 #include <cstring>
+#include <limits>
 #include <new>
 #include <string>
 #include <vector>
@@ -143,6 +144,39 @@ int make_camera(const float* K, const float* pose, Camera* c)
     return TSDF_OK;
 }
 
+// The bounds of Camera::sure_* for a volume of voxel edge `voxel` and
+// truncation `trunc`.  Where the pose is far from a rotation (an entry of
+// R^T R - I above 1e-3) the proof is not attempted (sure_tau = -inf).
+void sure_pass_bounds(float voxel, float trunc, Camera* c)
+{
+    const double R[3][3] = {{c->r00, c->r01, c->r02}, {c->r10, c->r11, c->r12},
+                            {c->r20, c->r21, c->r22}};
+    double defect = 0.0;
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 3; ++j) {
+            double g = 0.0;
+            for (int k = 0; k < 3; ++k) g += R[k][i] * R[k][j];
+            defect = std::max(defect, std::fabs(g - (i == j ? 1.0 : 0.0)));
+        }
+    const double s3n2 = 0.5 * std::sqrt(3.0) *
+                        std::sqrt(R[0][2] * R[0][2] + R[1][2] * R[1][2] + R[2][2] * R[2][2]);
+    const double tau = (double)trunc / (double)voxel - s3n2 - 1e-3;
+    const double tmag = (std::fabs((double)c->tx) + std::fabs((double)c->ty) +
+                         std::fabs((double)c->tz)) / (double)voxel;
+    const float inf = std::numeric_limits<float>::infinity();
+    if (!(defect <= 1e-3) || !std::isfinite(tmag)) {
+        c->sure_tau = -inf;
+        c->sure_near = inf;
+        c->sure_err = inf;
+        c->sure_tmag = inf;
+        return;
+    }
+    c->sure_tau = std::nextafter((float)tau, -inf);
+    c->sure_near = std::nextafter((float)(s3n2 + 1e-2), inf);
+    c->sure_err = std::nextafter((float)(64.0 * 0x1p-24 + 4.0 * defect), inf);
+    c->sure_tmag = std::nextafter((float)tmag, inf);
+}
+
 int check_size(int width, int height)
 {
     if (width <= 0 || height <= 0) return fail(TSDF_ERR_ARG, "width and height must be positive");
@@ -268,6 +302,7 @@ int check_batch(tsdf_volume* v, int n_frames, const float* depth, const float* r
     cams->resize((size_t)n_frames);
     for (int f = 0; f < n_frames; ++f)
         if ((rc = make_camera(K, poses + 16 * (size_t)f, &(*cams)[f]))) return rc;
+    for (int f = 0; f < n_frames; ++f) sure_pass_bounds(v->voxel, v->trunc, &(*cams)[f]);
     return TSDF_OK;
 }
 

@@ -139,6 +139,45 @@ def _flat_frame(name, W, H, f, depth_m, pose, voxel, trunc, pool, rgb_scale=1.0,
                          0, seed)
 
 
+# The allocate kernel skips the ray-depth occlusion test on band steps it
+# proves pass (a margin argument on the voxel-centre depth, tsdf_device.cuh
+# sure_pass).  These cases sit at the proof's edges; the block set must stay
+# exactly the oracle's.
+
+@pytest.mark.parametrize("ratio", [3.6, 4.4])
+@pytest.mark.parametrize("kernel", ["per_sample", "auto"])
+def test_parity_truncation_not_a_multiple_of_the_voxel(torch_cuda, oracle_mod, ratio, kernel):
+    f = scenes.vga_sphere_plane()
+    frames = scenes.Frames(f"vga_trunc{ratio}", f.depth, f.rgb, f.poses, f.K, 0.01,
+                           float(np.float32(0.01 * ratio)), 1 << 16, 0, 0)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel=kernel)
+
+
+@pytest.mark.parametrize("scale", [1.00001, 1.05])
+def test_parity_pose_not_exactly_a_rotation(torch_cuda, oracle_mod, scale):
+    # 1.00001: R^T R - I ~ 2e-5, the proof allows for it; 1.05: far from a
+    # rotation, the proof is not attempted and every step is tested
+    from test_oracle_pins import oblique_sphere_frames
+    f = oblique_sphere_frames()
+    poses = f.poses.copy()
+    poses[:, :3, :3] *= np.float32(scale)
+    frames = scenes.Frames(f"oblique_scaled{scale}", f.depth, f.rgb, poses, f.K, f.voxel_size,
+                           f.trunc, f.pool_capacity, f.table_capacity, 0)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="per_sample")
+
+
+@pytest.mark.parametrize("depth_m", [0.03, 0.045, 0.0488, 0.05, 0.06])
+def test_parity_surface_at_the_near_limit(torch_cuda, oracle_mod, depth_m):
+    # voxel 1 cm, truncation 4 cm: the proof needs depth / voxel above about
+    # 4.9; nearer surfaces have band samples behind the camera
+    a = np.array([0.3, -0.2, 1.0]) / np.linalg.norm([0.3, -0.2, 1.0])
+    pose = scenes.look_at(-0.37 * a + np.array([0.011, -0.007, 0.003]),
+                          np.array([0.011, -0.007, 0.003]))
+    frames = _flat_frame(f"near_{depth_m}", 96, 64, 60.0, depth_m, pose, 0.01, 0.04, 4096,
+                         seed=11)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="per_sample")
+
+
 def test_pre_reduced_colours_outside_unit_range(torch_cuda, oracle_mod):
     # colours in [-50, 205): those pixels take the per-sample path; the sums
     # must still match the oracle exactly as before
