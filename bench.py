@@ -516,6 +516,7 @@ def probe_depth_report(torch, targets=(0.1, 0.2, 0.3, 0.4, 0.5), n_frames: int =
     for target in targets:
         T = 1 << 17 if target < 0.25 else 1 << 16
         vol = TsdfVolume(T // 2, frames.voxel_size, frames.trunc, T)
+        vol.set_update_kernel("per_sample")     # the allocate and update kernels
         f = 0
         while f < frames.n_frames and vol.block_count() < target * T:
             vol.integrate(d[f], c[f], frames.K, frames.poses[f])

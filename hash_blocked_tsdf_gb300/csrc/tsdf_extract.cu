@@ -23,10 +23,10 @@
 // (+x, +y, +z and their combinations) are looked up in the table once; the
 // block's 512 means and the 217 lattice points its cells take from those
 // neighbours go to shared memory (9 x 9 x 9, NaN where unobserved); each
-// thread classifies two cells by the sign mask of their corners and counts
-// their triangles from it; a warp takes one range of the output with one
-// atomic, and each thread writes the triangles of its crossed cells there,
-// skipping tetrahedra the surface does not cross.
+// thread classifies two cells by the sign mask of their corners; the
+// tetrahedra the surface crosses become one task list for the block (scans
+// of the task and triangle counts; one atomic takes the block's range of the
+// output), and all 256 threads emit the list's triangles.
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -45,15 +45,6 @@ __device__ __forceinline__ int tet_corner(int tet, int k)
     const int q = (tet & 1) ? hi : lo;
     const int c1 = 1 << p, c2 = c1 | (1 << q);
     return k == 0 ? 0 : k == 1 ? c1 : k == 2 ? c2 : 7;
-}
-
-// f[k] for a run-time k (0..7) without indexing a register array.
-__device__ __forceinline__ float pick8(const float f[8], int k)
-{
-    const float a = (k & 1) ? f[1] : f[0], b = (k & 1) ? f[3] : f[2];
-    const float c = (k & 1) ? f[5] : f[4], d = (k & 1) ? f[7] : f[6];
-    const float ab = (k & 2) ? b : a, cd = (k & 2) ? d : c;
-    return (k & 4) ? cd : ab;
 }
 
 __device__ __forceinline__ float lattice(int i, float voxel)
@@ -112,12 +103,6 @@ __device__ __forceinline__ int inside_mask(const Tet& T)
            (T.v[3] < 0.0f ? 8 : 0);
 }
 
-__device__ __forceinline__ int mask_triangles(int m)
-{
-    const int n = __popc(m);
-    return n == 2 ? 2 : (n == 1 || n == 3) ? 1 : 0;
-}
-
 // Writes the tetrahedron's triangles from index `next` on (those at or past
 // `capacity` are dropped); returns the index after them.
 __device__ __forceinline__ uint64_t emit_tet(const Tet& T, const int cell[3], float voxel,
@@ -153,17 +138,6 @@ __device__ __forceinline__ uint64_t emit_tet(const Tet& T, const int cell[3], fl
     return next;
 }
 
-__device__ __forceinline__ Tet make_tet(const float f[8], int tet)
-{
-    Tet T;
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        T.id[k] = tet_corner(tet, k);
-        T.v[k] = pick8(f, T.id[k]);
-    }
-    return T;
-}
-
 // The block's lattice with its upper neighbours' first layer: 9 x 9 x 9
 // points, x fastest (index lx + 9 ly + 81 lz); a point's value is the mean
 // tsdf / weight, and NaN marks an unobserved point.
@@ -179,20 +153,6 @@ __device__ __forceinline__ uint32_t tet_corner_mask(int tet)
            (1u << tet_corner(tet, 3));
 }
 
-// Triangles of a fully observed cell whose inside corners are `mask` (bit k =
-// corner k < 0): per tetrahedron, one when one or three of its corners are
-// inside, two when two are.
-__device__ __forceinline__ int cell_triangles(uint32_t mask)
-{
-    int n = 0;
-#pragma unroll
-    for (int tet = 0; tet < 6; ++tet) {
-        const int k = __popc(mask & tet_corner_mask(tet));
-        n += k == 2 ? 2 : (k == 1 || k == 3) ? 1 : 0;
-    }
-    return n;
-}
-
 // Lattice index of corner k of the cell at (lx, ly, lz).
 __device__ __forceinline__ int corner_point(int base, int k)
 {
@@ -205,6 +165,12 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
 {
     __shared__ float s_lat[kLatPoints];
     __shared__ uint32_t s_nb[8];        // pool index of block + (d & 1, d >> 1 & 1, d >> 2 & 1)
+    // crossed tetrahedra of the block: cell (9 bits) | tetrahedron (3) << 9 |
+    // first triangle within the block << 12
+    __shared__ uint32_t s_task[6 * kBlockVoxels];
+    __shared__ uint32_t s_warp_tasks[kThreads / 32], s_warp_tris[kThreads / 32];
+    __shared__ uint32_t s_total_tasks;
+    __shared__ unsigned long long s_first;
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
     const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
@@ -257,55 +223,103 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
     }
     __syncthreads();
 
-    // the two cells of this thread: the sign mask of their corners; a cell is
-    // used when all 8 corners are observed and the surface crosses it
-    const float voxel = vol.div.voxel;
-    uint32_t mask[2];
-    int base[2];
+    // the two cells of this thread: the sign mask of their corners (a cell
+    // counts when all 8 corners are observed and the surface crosses it), and
+    // the tetrahedra of each that the surface crosses
+    uint32_t tets = 0;                  // bits 0-5: cell 0's tetrahedra, 8-13: cell 1's
+    uint32_t masks = 0;                 // bits 0-7: cell 0's inside corners, 8-15: cell 1's
     int n_tris = 0;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int j = t + c * kThreads;
-        base[c] = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
+        const int base = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
         uint32_t m = 0;
         bool seen = true;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const float v = s_lat[corner_point(base[c], k)];
+            const float v = s_lat[corner_point(base, k)];
             seen = seen && !isnan(v);
             m |= (v < 0.0f ? 1u : 0u) << k;
         }
-        mask[c] = (seen && m != 0u && m != 0xFFu) ? m : 0u;
-        if (mask[c]) n_tris += cell_triangles(mask[c]);
+        if (seen && m != 0u && m != 0xFFu) {
+            masks |= m << (8 * c);
+#pragma unroll
+            for (int tet = 0; tet < 6; ++tet) {
+                const int k = __popc(m & tet_corner_mask(tet));
+                if (k != 0 && k != 4) {
+                    tets |= 1u << (8 * c + tet);
+                    n_tris += k == 2 ? 2 : 1;
+                }
+            }
+        }
     }
 
-    // one output range per warp
+    // the block's crossed tetrahedra become one task list (block-wide scans of
+    // the task and triangle counts), so every thread emits triangles, not
+    // only the few that hold surface cells
     const unsigned lane = lane_id();
-    uint32_t incl = (uint32_t)n_tris;
+    const int warp = t >> 5;
+    uint32_t n_tasks = (uint32_t)__popc(tets);
+    uint32_t task_incl = n_tasks, tri_incl = (uint32_t)n_tris;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-        if ((int)lane >= d) incl += y;
+        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, task_incl, d);
+        const uint32_t b2 = __shfl_up_sync(0xFFFFFFFFu, tri_incl, d);
+        if ((int)lane >= d) {
+            task_incl += a;
+            tri_incl += b2;
+        }
     }
-    unsigned long long first = 0;
-    if (lane == 31 && incl) first = atomicAdd(count, (unsigned long long)incl);
-    first = __shfl_sync(0xFFFFFFFFu, first, 31);
-    uint64_t next = first + incl - (uint32_t)n_tris;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-        if (!mask[c]) continue;
-        const int j = t + c * kThreads;
+    if (lane == 31) {
+        s_warp_tasks[warp] = task_incl;
+        s_warp_tris[warp] = tri_incl;
+    }
+    __syncthreads();
+    if (t == 0) {
+        uint32_t tasks = 0, tris = 0;
+        for (int w = 0; w < kThreads / 32; ++w) {
+            const uint32_t a = s_warp_tasks[w], b2 = s_warp_tris[w];
+            s_warp_tasks[w] = tasks;
+            s_warp_tris[w] = tris;
+            tasks += a;
+            tris += b2;
+        }
+        s_total_tasks = tasks;
+        s_first = tris ? atomicAdd(count, (unsigned long long)tris) : 0ull;
+    }
+    __syncthreads();
+    uint32_t task = s_warp_tasks[warp] + task_incl - n_tasks;
+    uint32_t tri = s_warp_tris[warp] + tri_incl - (uint32_t)n_tris;
+    while (tets) {
+        const int bit = __ffs(tets) - 1;
+        tets &= tets - 1u;
+        const int c = bit >> 3, tet = bit & 7;
+        s_task[task] = (uint32_t)(t + c * kThreads) | ((uint32_t)tet << 9) | (tri << 12);
+        ++task;
+        // (a crossed tetrahedron holds 1 or 2 triangles)
+        const uint32_t m = (masks >> (8 * c)) & 0xFFu;
+        tri += __popc(m & tet_corner_mask(tet)) == 2 ? 2u : 1u;
+    }
+    __syncthreads();
+
+    const float voxel = vol.div.voxel;
+    const unsigned long long first = s_first;
+    const uint32_t total = s_total_tasks;
+    for (uint32_t k = (uint32_t)t; k < total; k += kThreads) {
+        const uint32_t code = s_task[k];
+        const int j = (int)(code & 511u);
+        const int tet = (int)((code >> 9) & 7u);
+        const uint32_t at = code >> 12;
+        const int base = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
         const int cell[3] = {bc[0] * kBlockEdge + (j & 7), bc[1] * kBlockEdge + ((j >> 3) & 7),
                              bc[2] * kBlockEdge + (j >> 6)};
-        float fc[8];
+        Tet T;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) fc[k] = s_lat[corner_point(base[c], k)];
-#pragma unroll 1
-        for (int tet = 0; tet < 6; ++tet) {
-            const int k = __popc(mask[c] & tet_corner_mask(tet));
-            if (k == 0 || k == 4) continue;     // no surface in this tetrahedron
-            next = emit_tet(make_tet(fc, tet), cell, voxel, out, capacity, next);
+        for (int q = 0; q < 4; ++q) {
+            T.id[q] = tet_corner(tet, q);
+            T.v[q] = s_lat[corner_point(base, T.id[q])];
         }
+        emit_tet(T, cell, voxel, out, capacity, first + at);
     }
 }
 
