@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
             VoxelSample s;
             const int status = band_sample<kFast>(cam, vol.div, p, __fsub_rn((float)j, fhalf), s);
             if (status == kSamplePass) {
-                lv[j] = local_voxel(s.ix, s.iy, s.iz);
+                lv[j] = (int)voxel_slot(vol, s.ix & 7, s.iy & 7, s.iz & 7);
                 tv[j] = s.tsdf;
                 const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
                 if (passed == 0u || bx != lbx || by != lby || bz != lbz) {

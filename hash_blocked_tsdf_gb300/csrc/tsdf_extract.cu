@@ -19,9 +19,9 @@
 //     (E(o,a), E(o,b), E(o,c)); two inside i1, i2 and two outside o1, o2:
 //     (E(i1,o1), E(i1,o2), E(i2,o2)) and (E(i1,o1), E(i2,o2), E(i2,o1)).
 //
-// One block of 256 threads per allocated block: its seven upper neighbours
-// (+x, +y, +z and their combinations) are looked up in the table once; the
-// block's 512 means and the 217 lattice points its cells take from those
+// One block of 256 threads per allocated block.  A first pass looks up every
+// block's seven upper neighbours (+x, +y, +z and their combinations) in the
+// table, all in parallel; the block's 512 means and the 217 lattice points its cells take from those
 // neighbours go to shared memory (9 x 9 x 9, NaN where unobserved); each
 // thread classifies two cells by the sign mask of their corners; the
 // tetrahedra the surface crosses become one task list for the block (scans
@@ -159,12 +159,35 @@ __device__ __forceinline__ int corner_point(int base, int k)
     return base + (k & 1) + ((k >> 1) & 1) * kLat + ((k >> 2) & 1) * kLat * kLat;
 }
 
+// nb[8 b + d] = pool index of block b's neighbour (bx + (d & 1), by + (d >> 1
+// & 1), bz + (d >> 2 & 1)), kIndexFailed when absent (d = 0: b itself): all
+// lookups of all blocks in parallel, so no extraction block waits on one.
+__global__ void __launch_bounds__(kThreads) neighbour_kernel(VolumeView vol,
+                                                            const int32_t* coords,
+                                                            uint32_t n_blocks, uint32_t* nb)
+{
+    const uint32_t i = blockIdx.x * kThreads + threadIdx.x;
+    if (i >= 8u * n_blocks) return;
+    const uint32_t b = i >> 3;
+    const int d = (int)(i & 7u);
+    uint32_t idx = b;
+    if (d != 0) {
+        const int nx = coords[3 * b] + (d & 1), ny = coords[3 * b + 1] + ((d >> 1) & 1),
+                  nz = coords[3 * b + 2] + ((d >> 2) & 1);
+        const int hi = (1 << 20) - 1;
+        idx = kIndexFailed;
+        if (nx <= hi && ny <= hi && nz <= hi)
+            idx = lookup(vol.table, vol.table_mask, pack_block(nx, ny, nz));
+    }
+    nb[i] = idx;
+}
+
 __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const int32_t* coords,
-                                                          float* out, uint64_t capacity,
+                                                          const uint32_t* nb, float* out,
+                                                          uint64_t capacity,
                                                           unsigned long long* count)
 {
     __shared__ float s_lat[kLatPoints];
-    __shared__ uint32_t s_nb[8];        // pool index of block + (d & 1, d >> 1 & 1, d >> 2 & 1)
     // crossed tetrahedra of the block: cell (9 bits) | tetrahedron (3) << 9 |
     // first triangle within the block << 12
     __shared__ uint32_t s_task[6 * kBlockVoxels];
@@ -174,25 +197,12 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
     const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
-    if (t < 8) {
-        uint32_t idx = kIndexFailed;
-        if (t == 0) {
-            idx = b;
-        } else {
-            const int nx = bc[0] + (t & 1), ny = bc[1] + ((t >> 1) & 1), nz = bc[2] + ((t >> 2) & 1);
-            const int hi = (1 << 20) - 1;
-            if (nx <= hi && ny <= hi && nz <= hi)
-                idx = lookup(vol.table, vol.table_mask, pack_block(nx, ny, nz));
-        }
-        s_nb[t] = idx;
-    }
     // the block's own 512 means
     for (int j = t; j < kBlockVoxels; j += kThreads) {
-        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + j);
+        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + voxel_slot_of(vol, j));
         s_lat[(j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat] =
             tw.y > 0.0f ? __fdiv_rn(tw.x, tw.y) : __int_as_float(0x7FFFFFFF);
     }
-    __syncthreads();
     // the upper neighbours' first layers: +x face, +y face, +z face (64 points
     // each), the three edges (8 each) and the corner
     if (t < kHaloPoints) {
@@ -213,10 +223,10 @@ __global__ void __launch_bounds__(kThreads) extract_kernel(VolumeView vol, const
             d = 7; lx = 8; ly = 8; lz = 8;
         }
         float v = __int_as_float(0x7FFFFFFF);
-        const uint32_t nb = s_nb[d];
-        if (nb < vol.pool_capacity) {
+        const uint32_t n_idx = __ldg(nb + 8 * (size_t)b + d);
+        if (n_idx < vol.pool_capacity) {
             const int jj = (lx & 7) | ((ly & 7) << 3) | ((lz & 7) << 6);
-            const float2 tw = tsdf_and_weight(vol, (size_t)nb * kBlockVoxels + jj);
+            const float2 tw = tsdf_and_weight(vol, (size_t)n_idx * kBlockVoxels + voxel_slot_of(vol, jj));
             if (tw.y > 0.0f) v = __fdiv_rn(tw.x, tw.y);
         }
         s_lat[lx + ly * kLat + lz * kLat * kLat] = v;
@@ -343,7 +353,7 @@ __global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const 
     const uint32_t idx = s_idx;
     if (idx >= vol.pool_capacity) return;           // refused (pool full) or out of range
     for (int j = threadIdx.x; j < kBlockVoxels; j += kThreads) {
-        const size_t e = (size_t)idx * kBlockVoxels + j;
+        const size_t e = (size_t)idx * kBlockVoxels + voxel_slot_of(vol, j);
         float v[5];
 #pragma unroll
         for (int a = 0; a < 5; ++a) v[a] = src[((size_t)a * n + b) * kBlockVoxels + j];
@@ -360,11 +370,16 @@ __global__ void __launch_bounds__(kThreads) import_kernel(VolumeView vol, const 
 }  // namespace
 
 cudaError_t launch_extract(const VolumeView& vol, const int32_t* coords, uint32_t n_blocks,
-                           float* out, uint64_t capacity, unsigned long long* count,
-                           cudaStream_t stream)
+                           uint32_t* neighbours, float* out, uint64_t capacity,
+                           unsigned long long* count, cudaStream_t stream)
 {
     if (n_blocks == 0) return cudaSuccess;
-    extract_kernel<<<n_blocks, kThreads, 0, stream>>>(vol, coords, out, capacity, count);
+    neighbour_kernel<<<(8 * n_blocks + kThreads - 1) / kThreads, kThreads, 0, stream>>>(
+        vol, coords, n_blocks, neighbours);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    extract_kernel<<<n_blocks, kThreads, 0, stream>>>(vol, coords, neighbours, out, capacity,
+                                                      count);
     return cudaGetLastError();
 }
 

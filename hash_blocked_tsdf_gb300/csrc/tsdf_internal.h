@@ -136,8 +136,8 @@ cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 // Marching tetrahedra over blocks [0, n_blocks) (coords[idx] = coordinate of
 // pool index idx); triangles past `capacity` are counted, not written.
 cudaError_t launch_extract(const VolumeView& vol, const int32_t* coords, uint32_t n_blocks,
-                           float* out, uint64_t capacity, unsigned long long* count,
-                           cudaStream_t stream);
+                           uint32_t* neighbours, float* out, uint64_t capacity,
+                           unsigned long long* count, cudaStream_t stream);
 // Copy block i's five sums (src: [5][n][512], the order tsdf, weight, red,
 // green, blue) to the pool slot the table gives its coordinate (inserted
 // beforehand).

@@ -32,18 +32,23 @@ __global__ void __launch_bounds__(kThreads) zero_used_blocks_kernel(VolumeView v
     }
 }
 
-// Voxel records [first, first + n) of the pool split into four planes:
-// out[k * n + i] = component k (tsdf, weight, red, green) of record first + i.
+// Interleaved layout: voxels [first, first + n) of the pool, in the C ABI's
+// x-fastest numbering (first and n multiples of 512), split into five
+// planes: out[k * n + i] = sum k (tsdf, weight, red, green, blue) of voxel
+// first + i, read from the brick-ordered records and blue sums.
 __global__ void __launch_bounds__(kThreads) split_records_kernel(VolumeView vol, size_t first,
                                                                  size_t n, float* out)
 {
     const size_t stride = (size_t)gridDim.x * kThreads;
     for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
-        const float4 r = vol.voxel4[first + i];
+        const size_t v = first + i;
+        const size_t src = (v & ~(size_t)(kBlockVoxels - 1)) + voxel_slot_of(vol, (int)(v & 511));
+        const float4 r = vol.voxel4[src];
         out[i] = r.x;
         out[n + i] = r.y;
         out[2 * n + i] = r.z;
         out[3 * n + i] = r.w;
+        out[4 * n + i] = vol.blue[src];
     }
 }
 

@@ -30,8 +30,9 @@
 // with TSDF_UPDATE_PRE_REDUCED every tile, one per block), three threads per pixel, each walking one third
 // of the pixel's truncation band (a warp covers an 8 x 4 pixel patch).  The
 // block keeps a shared table of the voxel rows its samples fall in (a row is
-// the 8 voxels of a block that share ly and lz: 128 contiguous bytes of
-// voxel records and one 32-byte sector of the blue array), and for every
+// the 8 voxels of a block that share ly and lz: in the planar layout one
+// 32-byte sector of each array, in the interleaved one four 2 x 2 x 2
+// bricks' records), and for every
 // voxel of a row two 64-bit masks: which of
 // the tile's pixels put a sample in it, and which put a second one (a ray
 // puts at most two samples in a voxel: samples are one voxel edge apart and a
@@ -40,7 +41,7 @@
 // from the pixel depths and its own centre -- the walk's arithmetic, so the
 // same values -- sums them with the pixels' colours in pixel order, and adds
 // its five sums to the pool; the voxels of a row are flushed by adjacent
-// lanes, so each row reaches L2 as five sectors instead of two reductions per
+// lanes, so each row reaches L2 as a few sectors instead of two reductions per
 // sample.  Rows that find no slot in the shared table add their samples
 // directly.
 //
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                 }
                 if (idx < vol.pool_capacity) {
                     // (pool indices are below 2^23, so e fits in 32 bits)
-                    e = idx * (uint32_t)kBlockVoxels + (uint32_t)local_voxel(s.ix, s.iy, s.iz);
+                    e = idx * (uint32_t)kBlockVoxels + voxel_slot(vol, s.ix & 7, s.iy & 7, s.iz & 7);
                     add = true;
                     ++updates;
                 } else {
@@ -331,7 +332,7 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
             }
         }
         if (direct) {
-            const size_t e = (size_t)idx * kBlockVoxels + row * 8 + lx;
+            const size_t e = (size_t)idx * kBlockVoxels + voxel_slot(vol, lx, row & 7, row >> 3);
             add_to_voxel(vol, e, s.tsdf, 1.0f, s_pixf[kPxR * kRowPix + q],
                          s_pixf[kPxG * kRowPix + q], s_pixf[kPxB * kRowPix + q]);
         }
@@ -433,7 +434,7 @@ __device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& 
     // flush: each listed cell recomputes its samples' tsdf from the pixel
     // depths and its voxel centre (the walk's own arithmetic), sums them with
     // the colours in pixel order, and adds the five sums to the pool; cells of
-    // one row sit next to each other, so a row reaches L2 as five sectors
+    // one row sit next to each other, so a row reaches L2 as a few sectors
     const int n_cells = (int)sm[kOffCount + 1];
     for (int k = t; k < n_cells; k += kRowThreads) {
         const uint32_t code = s_cell_list[k];
@@ -467,7 +468,7 @@ __device__ __forceinline__ void flush_rows(const VolumeView& vol, const Camera& 
                 }
             }
         }
-        const size_t e = (size_t)(row_key >> 6) * kBlockVoxels + (size_t)row * 8 + lx;
+        const size_t e = (size_t)(row_key >> 6) * kBlockVoxels + voxel_slot(vol, lx, row & 7, row >> 3);
         add_to_voxel(vol, e, sum[0], sum[1], sum[2], sum[3], sum[4]);
     }
 }

@@ -17,8 +17,8 @@ using namespace tsdf;
 
 namespace {
 
-// Blocks per chunk when export splits the interleaved voxel records into
-// planes (16,384 blocks: a 128 MB scratch buffer).
+// Blocks per chunk when export splits the interleaved layout's voxel records
+// and blue sums into planes (16,384 blocks: a 160 MB scratch buffer).
 // In the default update mode, integrate launches of fewer pixels than this
 // (frames x width x height) run the fused kernel: measured on GB300, one
 // fused launch took 0.039 / 0.046 / 0.077 ms against 0.054 / 0.061 / 0.079 ms
@@ -61,9 +61,10 @@ struct tsdf_volume {
                                     // pool_capacity * 512 blue sums
     DeviceState* state = nullptr;
     int32_t* coords = nullptr;      // [pool_capacity][3], allocated on first export
+    uint32_t* neighbours = nullptr; // [pool_capacity][8], allocated on first extraction
     int32_t* noalloc_scratch = nullptr;  // device address of the no-allocation export's
                                          // scratch array, looked up at create
-    float* export_scratch = nullptr;  // [kExportChunkBlocks][512][4], allocated on first export
+    float* export_scratch = nullptr;  // [5][kExportChunkBlocks][512], allocated on first export
 
     // host-batch staging: two buffers of (depth, rgb) frames
     float* stage[2] = {nullptr, nullptr};
@@ -237,6 +238,7 @@ void release(tsdf_volume* v)
     if (v->export_scratch) cudaFree(v->export_scratch);
     if (v->state) cudaFree(v->state);
     if (v->coords) cudaFree(v->coords);
+    if (v->neighbours) cudaFree(v->neighbours);
     for (int b = 0; b < 2; ++b) {
         if (v->stage[b]) cudaFree(v->stage[b]);
         if (v->copied[b]) cudaEventDestroy(v->copied[b]);
@@ -599,33 +601,30 @@ int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t 
                   "cudaMemcpyAsync(coords)");
     }
     const VolumeView w = view_of(vol);
-    if (b)
-        TSDF_CUDA(cudaMemcpyAsync(b, w.blue + (size_t)first * kBlockVoxels,
-                                  (size_t)count * kBlockVoxels * sizeof(float),
-                                  cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(blue)");
-    float* dst[4] = {tsdf_out, weight, r, g};
+    float* dst[5] = {tsdf_out, weight, r, g, b};
     if (w.planar) {
-        for (int a = 0; a < 4; ++a) {
+        // five x-fastest arrays: copied out directly
+        for (int a = 0; a < 5; ++a) {
             if (!dst[a]) continue;
-            TSDF_CUDA(cudaMemcpyAsync(dst[a],
-                                      reinterpret_cast<float*>(w.voxel4) + a * w.plane +
-                                          (size_t)first * kBlockVoxels,
+            const float* src = a < 4 ? reinterpret_cast<float*>(w.voxel4) + a * w.plane : w.blue;
+            TSDF_CUDA(cudaMemcpyAsync(dst[a], src + (size_t)first * kBlockVoxels,
                                       (size_t)count * kBlockVoxels * sizeof(float),
                                       cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(sums)");
         }
-    } else if (tsdf_out || weight || r || g) {
-        // the interleaved records are split into planes on the device, a
-        // chunk of blocks at a time, and each plane is copied out whole
+    } else if (tsdf_out || weight || r || g || b) {
+        // the brick-ordered records and blue sums are split into x-fastest
+        // planes on the device, a chunk of blocks at a time, and each plane is
+        // copied out whole
         if (!vol->export_scratch)
             TSDF_CUDA(cudaMalloc(&vol->export_scratch,
-                                 (size_t)kExportChunkBlocks * kBlockVoxels * 4 * sizeof(float)),
+                                 (size_t)kExportChunkBlocks * kBlockVoxels * 5 * sizeof(float)),
                       "cudaMalloc(export scratch)");
         for (uint32_t c0 = 0; c0 < count; c0 += kExportChunkBlocks) {
             const uint32_t nb = count - c0 < kExportChunkBlocks ? count - c0 : kExportChunkBlocks;
             const size_t nv = (size_t)nb * kBlockVoxels;
             TSDF_CUDA(launch_split_records(w, ((size_t)first + c0) * kBlockVoxels, nv,
                                            vol->export_scratch, s), "split_records kernel");
-            for (int a = 0; a < 4; ++a) {
+            for (int a = 0; a < 5; ++a) {
                 if (!dst[a]) continue;
                 TSDF_CUDA(cudaMemcpyAsync(dst[a] + (size_t)c0 * kBlockVoxels,
                                           vol->export_scratch + (size_t)a * nv,
@@ -654,8 +653,11 @@ int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uin
     TSDF_CUDA(launch_export_coords(w, vol->coords, s), "export_coords kernel");
     TSDF_CUDA(cudaMemsetAsync(&vol->state->triangles, 0, sizeof(unsigned long long), s),
               "cudaMemsetAsync(triangles)");
-    TSDF_CUDA(launch_extract(w, vol->coords, n, triangles, capacity, &vol->state->triangles, s),
-              "extract kernel");
+    if (!vol->neighbours)
+        TSDF_CUDA(cudaMalloc(&vol->neighbours, (size_t)vol->pool_capacity * 8 * sizeof(uint32_t)),
+                  "cudaMalloc(neighbours)");
+    TSDF_CUDA(launch_extract(w, vol->coords, n, vol->neighbours, triangles, capacity,
+                             &vol->state->triangles, s), "extract kernel");
     unsigned long long total = 0;
     TSDF_CUDA(cudaMemcpyAsync(&total, &vol->state->triangles, sizeof(total),
                               cudaMemcpyDeviceToHost, s), "cudaMemcpyAsync(triangles)");

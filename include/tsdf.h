@@ -39,12 +39,16 @@
  *   - block coordinates must lie in [-2^20, 2^20 - 1] per axis (the 21-bit
  *     key fields); samples outside are counted (out_of_range_samples) and
  *     skipped.
- *   - pool layout: block b's voxel j = lx + 8 * ly + 64 * lz is record
- *     v = b * 512 + j.  By default its TSDF, weight, red and green sums are
- *     interleaved in one 16-byte record, floats 4v .. 4v + 3 of the record
- *     array, and its blue sum is element v of a separate blue array; the
- *     pages' five separate arrays are available as TSDF_LAYOUT_PLANAR
- *     (tsdf_set_pool_layout).  The record lets a sample's update reach four
+ *   - voxel numbering in a block, at every call of this ABI (export,
+ *     import, extraction): j = lx + 8 * ly + 64 * lz, x fastest.
+ *   - pool layout: voxel (lx, ly, lz) of block b is record v = b * 512 + s.
+ *     By default its TSDF, weight, red and green sums are interleaved in one
+ *     16-byte record, floats 4v .. 4v + 3 of the record array, and its blue
+ *     sum is element v of a separate blue array, with the block stored as
+ *     64 bricks of 2 x 2 x 2 voxels: s = 8 * (lx/2 + 4 (ly/2) + 16 (lz/2)) +
+ *     (lx%2) + 2 (ly%2) + 4 (lz%2) (a brick's records fill one 128-byte
+ *     line); the pages' five separate arrays, x fastest (s = j), are
+ *     available as TSDF_LAYOUT_PLANAR (tsdf_set_pool_layout).  The record lets a sample's update reach four
  *     of its five sums with one 4-wide reduction, and L2 executes reduction
  *     requests at about the same rate whether they carry one float or four.
  *     tsdf_export_blocks returns the five sums as separate arrays in both.
@@ -111,11 +115,12 @@ typedef struct tsdf_info {
     int32_t pool_layout;              /* TSDF_LAYOUT_INTERLEAVED or TSDF_LAYOUT_PLANAR */
 } tsdf_info;
 
-/* Device pointers to the pool's five sums.  Record v = b * 512 + j (block b,
- * voxel j) holds tsdf[stride * v], weight[stride * v], r[stride * v] and
- * g[stride * v], and b[v]: stride 4 in the interleaved layout (weight =
- * tsdf + 1, r = tsdf + 2, g = tsdf + 3), stride 1 in the planar one (five
- * separate arrays).  Each field spans pool_capacity * 512 voxels.  They stay valid until tsdf_destroy; reading them races with
+/* Device pointers to the pool's five sums.  Record v = b * 512 + s (block b,
+ * voxel at position s of the pool layout: the brick order above in the
+ * interleaved layout, s = j in the planar one) holds tsdf[stride * v],
+ * weight[stride * v], r[stride * v] and g[stride * v], and b[v]: stride 4 in
+ * the interleaved layout (weight = tsdf + 1, r = tsdf + 2, g = tsdf + 3),
+ * stride 1 in the planar one (five separate arrays).  Each field spans pool_capacity * 512 voxels.  They stay valid until tsdf_destroy; reading them races with
  * kernels still running. */
 typedef struct tsdf_pool_view {
     float* tsdf;
@@ -278,9 +283,10 @@ int tsdf_block_count(tsdf_volume* vol, void* stream, uint32_t* out);
  * step, not part of integrate): coords int32 [count][3] (block coordinates, recovered from the
  * table) and the five sums as separate arrays float32 [count][512] each.  Any
  * output pointer may be NULL to skip it.  first + count must not exceed
- * tsdf_block_count.  The first call that asks for tsdf, weight, r or g
- * allocates a 128 MB device scratch buffer (kept until tsdf_destroy) in
- * which the interleaved records are split, 16,384 blocks at a time.  Pool
+ * tsdf_block_count.  In the interleaved layout the first call that asks for
+ * a sum allocates a 160 MB device scratch buffer (kept until tsdf_destroy)
+ * in which the brick-ordered records are split into x-fastest arrays,
+ * 16,384 blocks at a time.  Pool
  * order is the order in which blocks won their pool index, which is not
  * deterministic: compare by coordinate. */
 int tsdf_export_blocks(tsdf_volume* vol, void* stream, uint32_t first, uint32_t count,
@@ -329,7 +335,11 @@ int tsdf_export_block_coords_noalloc(tsdf_volume* vol, void* stream, uint32_t fi
  * xyz), borrowed; the triangle order is unspecified.  *n_out receives the
  * total number of triangles, which may exceed `capacity`: then only
  * `capacity` of them are written (call again with a larger buffer).
- * `triangles` may be NULL with capacity 0 to count only.  Synchronises
+ * `triangles` may be NULL with capacity 0 to count only.  The first call
+ * allocates two device buffers kept until tsdf_destroy: the block
+ * coordinates (12 B per pool block, shared with tsdf_export_blocks) and the
+ * pool indices of each block's upper neighbours (32 B per pool block).
+ * Synchronises
  * `stream`.  TSDF_ERR_ARG for a null n_out, or a null buffer with
  * capacity > 0. */
 int tsdf_extract_triangles(tsdf_volume* vol, void* stream, float* triangles, uint64_t capacity,
@@ -442,10 +452,11 @@ int tsdf_set_update_kernel(tsdf_volume* vol, int kind);
 #define TSDF_OCCLUSION_REPROJECT 1
 int tsdf_set_occlusion(tsdf_volume* vol, int mode);
 
-/* How the pool stores the five sums of a voxel (record v = b * 512 + j):
+/* How the pool stores the five sums of a voxel (record v = b * 512 + s):
  *   TSDF_LAYOUT_INTERLEAVED (the default): TSDF, weight, red and green sums
- *     in one 16-byte record per voxel, blue in an array of its own; an
- *     update adds a sample with one 4-wide and one scalar reduction.
+ *     in one 16-byte record per voxel, blue in an array of its own, voxels
+ *     in 2 x 2 x 2 bricks (s as above); an update adds a sample with one
+ *     4-wide and one scalar reduction.
  *   TSDF_LAYOUT_PLANAR: five separate float arrays [pool_capacity][512]
  *     (the pages' own layout, "design section, data structure"); an update
  *     adds a sample with five scalar reductions, a row of 8 voxels being one

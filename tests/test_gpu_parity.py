@@ -298,8 +298,9 @@ def test_host_batch_matches_device_batch(torch_cuda, oracle_mod):
 @pytest.mark.parametrize("layout", ["interleaved", "planar"])
 def test_pool_view_matches_export(torch_cuda, layout):
     """The zero-copy pool view: tsdf, weight, r and g interleaved per voxel
-    (stride 4) or planar (stride 1), blue plain; the same numbers as the
-    export's separate arrays."""
+    (stride 4, voxels in 2 x 2 x 2 bricks) or planar (stride 1, x fastest),
+    blue plain in the same order; the same numbers as the export's separate
+    x-fastest arrays."""
     from hash_blocked_tsdf_gb300 import binding
     torch = torch_cuda
     frames = scenes.tiny_sphere_plane()
@@ -327,9 +328,18 @@ def test_pool_view_matches_export(torch_cuda, layout):
         rec = torch.as_tensor(_View(p["tsdf"], 4 * cap * 512), device="cuda").view(
             4, cap, 512).permute(1, 2, 0)
     blue = torch.as_tensor(_View(p["b"], cap * 512), device="cuda").view(cap, 512)
+    # position of x-fastest voxel j in the pool: 2 x 2 x 2 bricks in the
+    # interleaved layout (include/tsdf.h), x fastest in the planar one
+    j = np.arange(512)
+    lx, ly, lz = j & 7, (j >> 3) & 7, j >> 6
+    if layout == "interleaved":
+        pos = 8 * ((lx >> 1) + 4 * (ly >> 1) + 16 * (lz >> 1)) + (lx & 1) + 2 * (ly & 1) + 4 * (lz & 1)
+        assert np.array_equal(np.sort(pos), j)
+    else:
+        pos = j
     for k, key in enumerate(("tsdf", "weight", "r", "g")):
-        np.testing.assert_array_equal(rec[:n, :, k].cpu().numpy(), g[key])
-    np.testing.assert_array_equal(blue[:n].cpu().numpy(), g["b"])
+        np.testing.assert_array_equal(rec[:n, :, k].cpu().numpy()[:, pos], g[key])
+    np.testing.assert_array_equal(blue[:n].cpu().numpy()[:, pos], g["b"])
     assert float(rec[n:].abs().sum()) == 0.0 and float(blue[n:].abs().sum()) == 0.0
     # export of a sub-range (offset into the records)
     part = vol.export_blocks(first=n // 3, count=n // 2)
