@@ -103,10 +103,11 @@ struct FrameView {
 // blocks of threads are ordered region-major, frame-minor, so the frames'
 // work on the same part of the scene runs close together in time and their
 // reductions on a voxel meet in L2.  Measured on the room walk: 8, 16, 32 and
-// 64 frames per launch give 7.6, 8.2, 8.7 and 8.9 G points/s; 32 keeps the
-// launch parameters (2.8 KB) and the host-batch staging (2 x 32 frames)
-// moderate.
-constexpr int kMaxBatch = 32;
+// 64 frames per launch gave 7.6, 8.2, 8.7 and 8.9 G points/s with the first
+// kernels, and 64 against 32 saves 1.9 % of the two stages with the current
+// ones (allocate 4.5 %, update 1.0 %); the launch parameters are then 6 KB
+// and the host-batch staging two buffers of 64 frames.
+constexpr int kMaxBatch = 64;
 constexpr uint32_t kDenseListCapacity = 1u << 20;
 struct FrameBatch {
     int n;
