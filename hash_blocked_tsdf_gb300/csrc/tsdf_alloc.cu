@@ -60,7 +60,7 @@ struct InsertResult {
 // are merged, one leader per key probes, and the warp's winners take pool
 // indices together and publish them before the step returns.  Every offering
 // lane gets its key's outcome and slot.  Must be called by all 32 lanes.
-template <bool kInstrument>
+template <bool kInstrument, bool kResult = true>
 __device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, bool fresh,
                                                          unsigned long long key, ProbeStats* st)
 {
@@ -82,8 +82,10 @@ __device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, 
         if (kInstrument) record_probe(st, steps);
         if (res == kProbeOverflow) atomicAdd(&vol.counters->probe_overflow, 1ull);
     }
-    out.res = __shfl_sync(0xFFFFFFFFu, res, leader_lane);
-    out.slot = __shfl_sync(0xFFFFFFFFu, slot, leader_lane);
+    if (kResult) {                          // (the allocate kernel does not need it)
+        out.res = __shfl_sync(0xFFFFFFFFu, res, leader_lane);
+        out.slot = __shfl_sync(0xFFFFFFFFu, slot, leader_lane);
+    }
     const bool won = leader && res == kProbeWon;
     const unsigned won_mask = __ballot_sync(0xFFFFFFFFu, won);
     if (won_mask == 0) return out;
@@ -167,6 +169,9 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
         SurePass sure = {-INFINITY, false};
         if (!kReproject && valid) sure = sure_pass(cam, vol.div, p, half);
         const float fhalf = (float)half;
+        // when every lane's whole band lies in the key range (always, in
+        // practice) the per-sample range check is left out
+        const bool all_in = __all_sync(0xFFFFFFFFu, !valid || ray_in_range(p, fhalf));
 #pragma unroll
         for (int j = 0; j < kShortBand; ++j) {
             if (valid && j < steps) {
@@ -174,7 +179,10 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                 // the step j - half as a float: exact, with no integer
                 // conversion per step
                 const float fi = __fsub_rn((float)j, fhalf);
-                if (!band_voxel_f<kFast>(p, fi, s)) {
+                bool in_range = true;
+                if (all_in) band_voxel_unchecked(p, fi, s);
+                else in_range = band_voxel_f<kFast>(p, fi, s);
+                if (!in_range) {
                     ++out_of_range;
                 } else {
                     const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
@@ -203,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                 band_voxel<kFast>(cam, vol.div, p, j - half, s);
                 key = block_key(s.ix, s.iy, s.iz);
             }
-            warp_insert_step<kInstrument>(vol, offer, key, &st);
+            warp_insert_step<kInstrument, false>(vol, offer, key, &st);
         }
     } else {
         unsigned long long last = kEmptyKey;

@@ -147,6 +147,26 @@ __device__ __forceinline__ bool band_voxel_f(const RayPoint& p, float fi, VoxelS
            ((unsigned)s.iz + kVoxelIndexBias < kVoxelIndexSpan);
 }
 
+// The voxel of band step fi without the range check, for rays whose whole
+// band ray_in_range has proven to lie in the packable range.
+__device__ __forceinline__ void band_voxel_unchecked(const RayPoint& p, float fi, VoxelSample& s)
+{
+    s.ix = __float2int_rd(__fadd_rn(p.vx, __fmul_rn(fi, p.ex)));
+    s.iy = __float2int_rd(__fadd_rn(p.vy, __fmul_rn(fi, p.ey)));
+    s.iz = __float2int_rd(__fadd_rn(p.vz, __fmul_rn(fi, p.ez)));
+}
+
+// Whether every band step -half .. half of the ray lies in the packable
+// voxel range: per axis |p'| + half |e| stays 4 below 2^23 - 1, which covers
+// the floor and the rounding of p' + i e (at most one unit at these
+// magnitudes).  Non-finite rays fail it.
+__device__ __forceinline__ bool ray_in_range(const RayPoint& p, float fhalf)
+{
+    const float lim = 8388603.0f;
+    return fabsf(p.vx) + fhalf * fabsf(p.ex) <= lim && fabsf(p.vy) + fhalf * fabsf(p.ey) <= lim &&
+           fabsf(p.vz) + fhalf * fabsf(p.ez) <= lim;
+}
+
 // The same with the step as an int (i converts exactly: |i| <= 127).
 template <bool kFast>
 __device__ __forceinline__ bool band_voxel(const Camera& c, const DivisorPair& dv,
@@ -206,11 +226,13 @@ __device__ __forceinline__ bool ray_visible(const Camera& c, const DivisorPair& 
 // allocate kernel, which only needs the voxel and the test, calls
 // band_voxel and ray_visible itself.  Written without early exits: every
 // quantity is computed and the status is selected at the end.
-template <bool kFast>
+template <bool kFast, bool kCheckRange = true>
 __device__ __forceinline__ int band_sample(const Camera& c, const DivisorPair& dv,
                                            const RayPoint& p, float fi, VoxelSample& s)
 {
-    const bool in_range = band_voxel_f<kFast>(p, fi, s);
+    bool in_range = true;
+    if (kCheckRange) in_range = band_voxel_f<kFast>(p, fi, s);
+    else band_voxel_unchecked(p, fi, s);
     float zc;
     const bool visible = ray_visible(c, dv, p, s, zc);
     s.tsdf = truncated_sdf<kFast>(dv, p.d, zc);

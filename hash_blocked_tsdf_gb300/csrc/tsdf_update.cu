@@ -113,7 +113,11 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     bool looked_up = false;
     uint32_t idx = kIndexFailed;
     // every lane runs every band step (the warp merges each step's samples);
-    // the step also counts as a float, exactly, to spare a conversion per step
+    // the step also counts as a float, exactly, to spare a conversion per step;
+    // when every lane's whole band lies in the key range (always, in
+    // practice) the per-sample range check is left out
+    const bool all_in =
+        __all_sync(0xFFFFFFFFu, !valid || ray_in_range(p, (float)vol.band_half));
     float fi = -(float)vol.band_half;
     for (int i = -vol.band_half; i <= vol.band_half; ++i, fi = __fadd_rn(fi, 1.0f)) {
         VoxelSample s;
@@ -133,7 +137,8 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                     cb = __ldg(rgb + 3 * q + 2);
                 }
             } else {
-                status = band_sample<kFast>(cam, vol.div, p, fi, s);
+                status = all_in ? band_sample<kFast, false>(cam, vol.div, p, fi, s)
+                                : band_sample<kFast, true>(cam, vol.div, p, fi, s);
             }
             if (status == kSamplePass) {
                 const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
