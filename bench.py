@@ -67,6 +67,10 @@ def parse_args():
                     help="also write the nvidia-smi clock samples of the timed region here")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--gate", choices=["full", "sample"], default="full",
+                    help="what the parity gate compares with the oracle: the whole trajectory "
+                         "(default; the oracle in parallel on the host cores) or its first "
+                         "frames only (quick runs, profiling)")
     ap.add_argument("--sweep", action="store_true",
                     help="run the measurement matrix (one JSON line per cell) instead of the "
                          "headline workload")
@@ -253,13 +257,14 @@ def sum_over_ranks(x: float, world: int) -> float:
 # CPU oracle arm
 # ----------------------------------------------------------------------------
 
-def oracle_sample(frames, seconds_target: float, min_frames: int = 1):
+def oracle_sample(frames, seconds_target: float, min_frames: int = 1, occlusion: str = "ray"):
     """Time the oracle on the first frames of the workload until about
     `seconds_target` seconds of CPU work (at least `min_frames` frames);
     returns (points/s, voxel-updates/s, description, the oracle volume,
     frames integrated)."""
     import oracle
     o = oracle.OracleVolume(frames.voxel_size, frames.trunc)
+    o.set_occlusion(occlusion)
     t0 = time.perf_counter()
     n = 0
     while n < frames.n_frames:
@@ -274,22 +279,38 @@ def oracle_sample(frames, seconds_target: float, min_frames: int = 1):
             o, n)
 
 
-def parity_gate(torch, vol, frames, d_dev, c_dev, n, ovol) -> dict:
-    """The same first `n` frames the oracle integrated for the CPU baseline,
-    integrated again on the GPU (fresh volume, the bench's own batching), and
-    compared: exact block set, weights and counters; sums within the stated
-    bound max(1e-5 |x|, 1e-6), widened by the float32 summation bound
-    gamma(w - 1) sum |t| where a voxel's terms cancel.  Reports, per sum, how
-    many voxels needed the widening and the worst error against each bound.
-    The headline is withheld when this check fails."""
-    vol.reset()
-    vol.integrate_batch(d_dev[:n], c_dev[:n], frames.K, frames.poses[:n])
-    torch.cuda.synchronize()
-    st = vol.stats()
-    g = vol.export_blocks()
-    o = ovol.export()
-    oc = ovol.counters()
-    out = {"frames": n, "blocks": int(len(o["coords"])), "voxels": int(len(o["coords"])) * 512}
+def gate_reference(frames, scope: str, occlusion: str, sampled=None):
+    """The oracle's volume the gate compares with: the whole trajectory the
+    steps integrate (scope "full": the oracle run in parallel on the host
+    cores, frames cut into chunks and blocks into partitions), or the first
+    frames only (scope "sample": the CPU-baseline sample's volume when there
+    is one, else two frames).  Returns (frames covered, export, counters,
+    description)."""
+    t0 = time.perf_counter()
+    if scope == "full":
+        from oracle.parallel import full_volume_oracle, worker_count
+        o, oc = full_volume_oracle(frames, occlusion=occlusion)
+        n = frames.n_frames
+        how = (f"whole trajectory: all {n} frames, oracle in {worker_count()} processes "
+               f"({time.perf_counter() - t0:.0f} s)")
+        return n, o, oc, how
+    if sampled is None:
+        _, _, _, ovol, n = oracle_sample(frames, 0.0, min_frames=min(2, frames.n_frames),
+                                         occlusion=occlusion)
+    else:
+        ovol, n = sampled
+    how = f"first {n} of {frames.n_frames} frames (oracle sample)"
+    return n, ovol.export(), ovol.counters(), how
+
+
+def compare_volumes(g: dict, st: dict, o: dict, oc: dict) -> dict:
+    """The GPU export `g` and statistics `st` against the oracle's export `o`
+    (coords sorted) and counters `oc`: exact block set, weights and counters;
+    sums within the stated bound max(1e-5 |x|, 1e-6), widened by the float32
+    summation bound gamma(w - 1) sum |t| where a voxel's terms cancel.
+    Reports, per sum, how many voxels needed the widening and the worst error
+    against each bound."""
+    out = {"blocks": int(len(o["coords"])), "voxels": int(len(o["coords"])) * 512}
     order = np.lexsort((g["coords"][:, 2], g["coords"][:, 1], g["coords"][:, 0]))
     out["block_set_equal"] = bool(g["coords"].shape == o["coords"].shape and
                                   np.array_equal(g["coords"][order], o["coords"]))
@@ -320,6 +341,23 @@ def parity_gate(torch, vol, frames, d_dev, c_dev, n, ovol) -> dict:
     out["sums"] = sums
     out["sums_worst_error_over_bound"] = worst
     out["pass"] = bool(out["weights_equal"] and out["counters_equal"] and worst <= 1.0)
+    return out
+
+
+def parity_gate(torch, vol, frames, d_dev, c_dev, scope: str, occlusion: str,
+                sampled=None) -> dict:
+    """The frames the oracle integrated (by default the whole trajectory one
+    timed step integrates), integrated again on the GPU into a fresh volume
+    with the bench's settings, and compared with the oracle's volume.  The
+    headline is withheld when this check fails."""
+    n, o, oc, how = gate_reference(frames, scope, occlusion, sampled)
+    vol.reset()
+    vol.integrate_batch(d_dev[:n], c_dev[:n], frames.K, frames.poses[:n])
+    torch.cuda.synchronize()
+    st = vol.stats()
+    g = vol.export_blocks()
+    out = {"scope": scope, "frames": n, "oracle": how}
+    out.update(compare_volumes(g, st, o, oc))
     return out
 
 
@@ -952,17 +990,21 @@ def run_ours(args):
             torch, vol, frames, d_dev, c_dev, groups, one_step, stream, args, world,
             hbm_peak, red_peak)
     if rank == 0:
-        # the timing counts only if the GPU's volume matches the oracle's on
-        # the frames the oracle integrated (the CPU-baseline sample, or two
-        # frames when that leg is off); otherwise the headline is withheld
-        seconds = 0.0 if args.no_cpu_baseline else args.cpu_baseline_seconds
-        v, u, sample, ovol, n_sample = oracle_sample(frames, seconds,
-                                                     min_frames=min(2, frames.n_frames))
-        gate = parity_gate(torch, vol, frames, d_dev, c_dev, n_sample, ovol)
+        # the single-thread CPU baseline: the oracle as it stands on a
+        # bounded sample of the workload
+        sampled = None
         if world == 1 and not args.no_cpu_baseline:
+            v, u, sample, ovol, n_sample = oracle_sample(frames, args.cpu_baseline_seconds,
+                                                         occlusion=args.occlusion)
             result["cpu_baseline"] = {"value": v, "unit": "points/s", "cores": 1,
                                       "kind": "oracle", "sample": sample,
                                       "voxel_updates_per_s": u, "cpu": platform.machine()}
+            sampled = (ovol, n_sample)
+        # the timing counts only if the GPU's volume matches the oracle's
+        # (over the whole trajectory by default); otherwise the headline is
+        # withheld
+        gate = parity_gate(torch, vol, frames, d_dev, c_dev, args.gate, args.occlusion,
+                           sampled)
         apply_gate(result, gate)
     vol.close()
     if rank == 0:

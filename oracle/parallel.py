@@ -30,6 +30,12 @@ def _cpu_count() -> int:
         return os.cpu_count() or 1
 
 
+def worker_count() -> int:
+    """Worker processes full_volume_oracle starts by default: the host's
+    cores, at least 2 and at most 16."""
+    return max(2, min(16, _cpu_count()))
+
+
 def _oracle_piece(args):
     """One worker: frames [start, stop) of the memory-mapped trajectory,
     sums kept for block partition `part` of `parts`.  Returns the block set
@@ -73,7 +79,7 @@ def full_volume_oracle(frames, occlusion: str = "ray", workers: int = 0, parts: 
     import shutil
     import tempfile
 
-    workers = workers or max(2, min(16, _cpu_count()))
+    workers = workers or worker_count()
     parts = max(1, min(parts, workers))
     chunks = max(1, min(frames.n_frames, workers // parts))
     folder = tempfile.mkdtemp(prefix="tsdf_oracle_frames_")

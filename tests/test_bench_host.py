@@ -52,7 +52,7 @@ class _FakeVolume:
         return {k: v.copy() for k, v in self._export.items()}
 
 
-def _gate(oracle_mod, mutate=None):
+def _gate(oracle_mod, mutate=None, scope="sample"):
     frames = scenes.tiny_sphere_plane()
     o = oracle_mod.OracleVolume(frames.voxel_size, frames.trunc)
     o.integrate_frames(frames)
@@ -70,13 +70,24 @@ def _gate(oracle_mod, mutate=None):
              "probe_overflow": 0}
     fake_torch = types.SimpleNamespace(cuda=types.SimpleNamespace(synchronize=lambda: None))
     return bench.parity_gate(fake_torch, _FakeVolume(g, stats), frames, frames.depth,
-                             frames.rgb, frames.n_frames, o)
+                             frames.rgb, scope, "ray", sampled=(o, frames.n_frames))
 
 
 def test_parity_gate_passes_on_the_oracle_itself(oracle_mod):
     out = _gate(oracle_mod)
     assert out["pass"] and out["block_set_equal"] and out["weights_equal"]
     assert out["sums_worst_error_over_bound"] <= 1.0
+
+
+def test_parity_gate_over_the_whole_trajectory_uses_the_parallel_oracle(oracle_mod):
+    # scope "full" recomputes the oracle's volume in worker processes (frame
+    # chunks x block partitions) instead of taking the sample's volume
+    out = _gate(oracle_mod, scope="full")
+    assert out["scope"] == "full" and "processes" in out["oracle"]
+    assert out["pass"] and out["block_set_equal"] and out["weights_equal"]
+    assert out["sums_worst_error_over_bound"] <= 1.0
+    out = _gate(oracle_mod, lambda g: g["weight"].__setitem__((0, 0), 7.0), scope="full")
+    assert not out["pass"]
 
 
 def test_parity_gate_rejects_a_wrong_weight(oracle_mod):
