@@ -38,7 +38,8 @@ class tsdf_info(ctypes.Structure):
                 ("voxel_size", ctypes.c_float), ("trunc", ctypes.c_float),
                 ("band_samples", ctypes.c_int32), ("device", ctypes.c_int32),
                 ("fixed_divisor_fast_path", ctypes.c_int32),
-                ("max_frames_per_launch", ctypes.c_int32), ("pool_layout", ctypes.c_int32)]
+                ("max_frames_per_launch", ctypes.c_int32), ("pool_layout", ctypes.c_int32),
+                ("voxel_division_fast_path", ctypes.c_int32)]
 
 
 class tsdf_pool_view(ctypes.Structure):

@@ -155,8 +155,7 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
     bool valid = false;
     if (pix < n_pix) {
         const int v = pix / fb.width;
-        const int u = pix - v * fb.width;
-        valid = back_project(cam, vol.div, u, v, __ldg(depth + pix), p);
+        valid = back_project_pixel(vol, fb, cam, v, (size_t)pix, __ldg(depth + pix), p);
     }
     const int half = vol.band_half;
     const int steps = 2 * half + 1;
@@ -321,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
-        valid = back_project(cam, vol.div, u, v, depth, p);
+        valid = back_project_pixel(vol, fb, cam, v, pix, depth, p);
         if (valid) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);

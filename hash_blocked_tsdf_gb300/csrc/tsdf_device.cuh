@@ -34,27 +34,88 @@ struct VoxelSample {
     float tsdf;         // min(1, sdf / trunc)
 };
 
-__device__ __forceinline__ bool back_project(const Camera& c, const DivisorPair& dv, int u, int v,
+// Division by a divisor y that is fixed for the whole volume (the
+// truncation distance or the voxel edge), given r = RN(1 / y): Markstein's
+// reciprocal-and-correction scheme (P. Markstein, "Computation of elementary
+// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
+// 1990): q0 = RN(x r) is within an ulp of x / y, the residual x - q0 y is
+// exact in one fused multiply-add, and one more fused multiply-add rounds
+// q0 + r (x - q0 y) to the correctly rounded quotient.  At volume creation the
+// host has the GPU check, for every one of the 2^32 float32 bit patterns x,
+// that min(1, x / trunc) comes out the same as with IEEE division for every
+// x >= -trunc (the only dividends the walk divides by trunc), and that
+// x / voxel comes out bit for bit the same for every x (div_voxel).  Only
+// where its check passed is the scheme used.
+__device__ __forceinline__ float div_fixed(float x, float y, float r)
+{
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, y, x);
+    return __fmaf_rn(e, r, q0);
+}
+
+// x / trunc as the walk uses it (checked exhaustively for x >= -trunc).  The
+// residual of the correction step is only exact while it stays a normal
+// number, i.e. for |x| well above the subnormal range; smaller dividends
+// (which real depths never produce) take the IEEE division.
+template <bool kFast>
+__device__ __forceinline__ float div_trunc(float x, float y, float r)
+{
+    if (kFast && fabsf(x) >= 0x1p-96f) return div_fixed(x, y, r);
+    return __fdiv_rn(x, y);
+}
+
+// Division of a world coordinate by the voxel edge in the back-projection:
+// the reciprocal-and-correction quotient where `fast` (the volume checked
+// it, at create, against IEEE division for every float32 dividend) and
+// the magnitude lies in [2^-96, 2^100), where the residual stays a normal
+// number and x r cannot overflow; IEEE division otherwise.
+__device__ __forceinline__ float div_voxel(const DivisorPair& dv, bool fast, float x)
+{
+    const float a = fabsf(x);
+    if (fast && a >= 0x1p-96f && a < 0x1p100f) return div_fixed(x, dv.voxel, dv.inv_voxel);
+    return __fdiv_rn(x, dv.voxel);
+}
+
+// The viewing ray of pixel (u, v): xn = (u - cx) / fx, yn = (v - cy) / fy,
+// and the unit direction (xn, yn, 1) / sqrt(xn^2 + yn^2 + 1), returned as
+// (dx, dy, dz, xn).  It depends only on the pixel and the intrinsics, so a
+// batch computes it once per pixel into a table (build_rays) that every
+// frame's back-projection reads: the two divisions of the normalised
+// coordinates, the square root and the three divisions of the direction are
+// the expensive part of back-projecting a pixel, and the table holds their
+// IEEE results unchanged.
+__device__ __forceinline__ float4 pixel_ray(float fx, float fy, float cx, float cy, int u, int v,
+                                            float& yn)
+{
+    const float xn = __fdiv_rn(__fsub_rn((float)u, cx), fx);
+    yn = __fdiv_rn(__fsub_rn((float)v, cy), fy);
+    const float len = __fsqrt_rn(__fadd_rn(__fadd_rn(__fmul_rn(xn, xn), __fmul_rn(yn, yn)), 1.0f));
+    return make_float4(__fdiv_rn(xn, len), __fdiv_rn(yn, len), __fdiv_rn(1.0f, len), xn);
+}
+
+// Back-project a pixel of depth d whose ray (pixel_ray) is `ray`, with yn
+// its row's normalised coordinate: p = d (xn, yn, 1) moved to the world and
+// divided by the voxel edge, and the world direction of the ray.
+__device__ __forceinline__ bool back_project(const Camera& c, const DivisorPair& dv,
+                                             bool fast_voxel, const float4& ray, float yn,
                                              float d, RayPoint& p)
 {
     if (!(isfinite(d) && d > 0.0f)) return false;
-    const float xn = __fdiv_rn(__fsub_rn((float)u, c.cx), c.fx);
-    const float yn = __fdiv_rn(__fsub_rn((float)v, c.cy), c.fy);
-    const float px = __fmul_rn(xn, d);
+    const float px = __fmul_rn(ray.w, d);
     const float py = __fmul_rn(yn, d);
     const float pz = d;
-    const float len = __fsqrt_rn(__fadd_rn(__fadd_rn(__fmul_rn(xn, xn), __fmul_rn(yn, yn)), 1.0f));
-    const float dx = __fdiv_rn(xn, len);
-    const float dy = __fdiv_rn(yn, len);
-    const float dz = __fdiv_rn(1.0f, len);
-    // rows of R summed left to right, then t; one IEEE division per axis
+    const float dx = ray.x, dy = ray.y, dz = ray.z;
+    // rows of R summed left to right, then t; one division per axis
     p.d = d;
-    p.vx = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r00, px), __fmul_rn(c.r01, py)),
-                                         __fmul_rn(c.r02, pz)), c.tx), dv.voxel);
-    p.vy = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r10, px), __fmul_rn(c.r11, py)),
-                                         __fmul_rn(c.r12, pz)), c.ty), dv.voxel);
-    p.vz = __fdiv_rn(__fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, px), __fmul_rn(c.r21, py)),
-                                         __fmul_rn(c.r22, pz)), c.tz), dv.voxel);
+    p.vx = div_voxel(dv, fast_voxel,
+                     __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r00, px), __fmul_rn(c.r01, py)),
+                                         __fmul_rn(c.r02, pz)), c.tx));
+    p.vy = div_voxel(dv, fast_voxel,
+                     __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r10, px), __fmul_rn(c.r11, py)),
+                                         __fmul_rn(c.r12, pz)), c.ty));
+    p.vz = div_voxel(dv, fast_voxel,
+                     __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(c.r20, px), __fmul_rn(c.r21, py)),
+                                         __fmul_rn(c.r22, pz)), c.tz));
     p.ex = __fadd_rn(__fadd_rn(__fmul_rn(c.r00, dx), __fmul_rn(c.r01, dy)), __fmul_rn(c.r02, dz));
     p.ey = __fadd_rn(__fadd_rn(__fmul_rn(c.r10, dx), __fmul_rn(c.r11, dy)), __fmul_rn(c.r12, dz));
     p.ez = __fadd_rn(__fadd_rn(__fmul_rn(c.r20, dx), __fmul_rn(c.r21, dy)), __fmul_rn(c.r22, dz));
@@ -73,38 +134,19 @@ __device__ __forceinline__ bool back_project(const Camera& c, const DivisorPair&
     return true;
 }
 
+// Back-project pixel index pix = v * width + u of a batch's frame, its depth
+// d, reading the pixel's ray from the batch's table.
+__device__ __forceinline__ bool back_project_pixel(const VolumeView& vol, const FrameBatch& fb,
+                                                   const Camera& cam, int v, size_t pix, float d,
+                                                   RayPoint& p)
+{
+    const float4 ray = __ldg(fb.rays + pix);
+    const float yn = __ldg(fb.ray_yn + v);
+    return back_project(cam, vol.div, vol.fast_voxel, ray, yn, d, p);
+}
+
 // A pixel holds an observation when its depth is finite and positive.
 __device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
-
-// Division by a divisor y that is fixed for the whole volume (the
-// truncation distance), given r = RN(1 / y): Markstein's
-// reciprocal-and-correction scheme (P. Markstein, "Computation of elementary
-// functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1),
-// 1990): q0 = RN(x r) is within an ulp of x / y, the residual x - q0 y is
-// exact in one fused multiply-add, and one more fused multiply-add rounds
-// q0 + r (x - q0 y) to the correctly rounded quotient.  At volume creation the
-// host has the GPU check, for every one of the 2^32 float32 bit patterns x,
-// that min(1, x / trunc) comes out the same as with IEEE division for every
-// x >= -trunc (the only dividends the walk divides).  Only then is the
-// scheme used.  (The walk divides by the voxel edge once per pixel, with
-// IEEE division.)
-__device__ __forceinline__ float div_fixed(float x, float y, float r)
-{
-    const float q0 = __fmul_rn(x, r);
-    const float e = __fmaf_rn(-q0, y, x);
-    return __fmaf_rn(e, r, q0);
-}
-
-// x / trunc as the walk uses it (checked exhaustively for x >= -trunc).  The
-// residual of the correction step is only exact while it stays a normal
-// number, i.e. for |x| well above the subnormal range; smaller dividends
-// (which real depths never produce) take the IEEE division.
-template <bool kFast>
-__device__ __forceinline__ float div_trunc(float x, float y, float r)
-{
-    if (kFast && fabsf(x) >= 0x1p-96f) return div_fixed(x, y, r);
-    return __fdiv_rn(x, y);
-}
 
 // Voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1].
 constexpr unsigned kVoxelIndexBias = 1u << 23;

@@ -80,6 +80,7 @@ struct VolumeView {
     DeviceCounters* counters;
     DivisorPair div;            // voxel size and truncation, with reciprocals
     bool fast_div;              // the fixed-divisor division was verified exact
+    bool fast_voxel;            // ... and the one by the voxel edge (back-projection)
     int band_half;              // samples at offsets -band_half .. band_half voxels
     int occlusion;              // TSDF_OCCLUSION_RAY or TSDF_OCCLUSION_REPROJECT
     // Adaptive update: the dense 16 x 16 pixel tiles of the current update
@@ -113,6 +114,12 @@ struct FrameBatch {
     int n;
     int width;
     int height;
+    // The pixels' rays for the batch's intrinsics (build_rays): for pixel
+    // (u, v), rays[v * width + u] = (dx, dy, dz, xn), the unit viewing ray
+    // (xn, yn, 1) / |(xn, yn, 1)| and xn = (u - cx) / fx; ray_yn[v] =
+    // (v - cy) / fy.
+    const float4* rays;
+    const float* ray_yn;
     FrameView frame[kMaxBatch];
 };
 
@@ -128,11 +135,17 @@ cudaError_t launch_allocate_blocks(const VolumeView& vol, const int32_t* coords,
 // With the reprojection occlusion test every kind runs the per-sample kernel.
 cudaError_t launch_update(const VolumeView& vol, const FrameBatch& fb, int kind,
                           cudaStream_t stream);
-// Count the float32 x >= -y (all 2^32 bit patterns tried) for which
-// min(1, x / y) with the fixed-divisor quotient differs from the IEEE one;
-// result added to *mismatches.
-cudaError_t launch_verify_fixed_divisor(float y, float inv_y, unsigned long long* mismatches,
-                                        cudaStream_t stream);
+// All 2^32 float32 bit patterns x tried against IEEE division by y, the
+// count of mismatches added to *mismatches.  kDivideTrunc: x >= -y, compared
+// as min(1, x / y) (the truncated distance); kDivideVoxel: every x, compared
+// bit for bit (the back-projection's division by the voxel edge).
+enum DivisorCheck { kDivideTrunc = 0, kDivideVoxel = 1 };
+cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int check,
+                                        unsigned long long* mismatches, cudaStream_t stream);
+// The rays of every pixel of a width x height image for intrinsics
+// (fx, fy, cx, cy), written to rays and ray_yn as FrameBatch describes.
+cudaError_t launch_build_rays(float fx, float fy, float cx, float cy, int width, int height,
+                              float4* rays, float* ray_yn, cudaStream_t stream);
 cudaError_t launch_zero_used_blocks(const VolumeView& vol, cudaStream_t stream);
 // Marching tetrahedra over blocks [0, n_blocks) (coords[idx] = coordinate of
 // pool index idx); triangles past `capacity` are counted, not written.

@@ -1,5 +1,7 @@
-// Volume maintenance kernels: clearing the used prefix of the pool, and
-// recovering each pool block's coordinate from the table for read-out.
+// Volume maintenance kernels: clearing the used prefix of the pool,
+// recovering each pool block's coordinate from the table for read-out, the
+// per-batch table of pixel rays, and the check of the fixed-divisor
+// divisions.
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -62,36 +64,77 @@ __global__ void __launch_bounds__(kThreads) export_coords_kernel(VolumeView vol,
     unpack_block(e.key, coords + 3 * (size_t)e.idx);
 }
 
-// Every float32 bit pattern x >= -y: does min(1, x / y) come out the same
-// with div_fixed as with IEEE division (y the truncation distance)?
+// Every float32 bit pattern x: does the fixed-divisor quotient come out as
+// IEEE division gives it?  kDivideTrunc: for x >= -y, compared as
+// min(1, x / y) (y the truncation distance); kDivideVoxel: for every
+// non-NaN x, bit for bit (y the voxel edge, div_voxel's ranges).
+template <int kCheck>
 __global__ void __launch_bounds__(kThreads) verify_fixed_divisor_kernel(
     float y, float r, unsigned long long* mismatches)
 {
     const uint64_t stride = (uint64_t)gridDim.x * kThreads;
     uint32_t bad = 0;
+    DivisorPair dv = {y, r, y, r};
     for (uint64_t b = (uint64_t)blockIdx.x * kThreads + threadIdx.x; b < (1ull << 32);
          b += stride) {
         const float x = __uint_as_float((uint32_t)b);
-        const float fast = div_trunc<true>(x, y, r);
         const float ieee = __fdiv_rn(x, y);
-        const bool same = !(x >= -y) || fminf(1.0f, fast) == fminf(1.0f, ieee);
+        bool same;
+        if (kCheck == kDivideTrunc) {
+            const float fast = div_trunc<true>(x, y, r);
+            same = !(x >= -y) || fminf(1.0f, fast) == fminf(1.0f, ieee);
+        } else {
+            same = isnan(x) || __float_as_uint(div_voxel(dv, true, x)) == __float_as_uint(ieee);
+        }
         bad += same ? 0u : 1u;
     }
     bad = __reduce_add_sync(0xFFFFFFFFu, bad);
     if (lane_id() == 0 && bad) atomicAdd(mismatches, (unsigned long long)bad);
 }
 
+// The ray table of a width x height image (FrameBatch::rays, ray_yn).
+__global__ void __launch_bounds__(kThreads) build_rays_kernel(float fx, float fy, float cx,
+                                                              float cy, int width, int height,
+                                                              float4* rays, float* ray_yn)
+{
+    const size_t n = (size_t)width * (size_t)height;
+    const size_t stride = (size_t)gridDim.x * kThreads;
+    for (size_t i = (size_t)blockIdx.x * kThreads + threadIdx.x; i < n; i += stride) {
+        const int u = (int)(i % (size_t)width);
+        const int v = (int)(i / (size_t)width);
+        float yn;
+        rays[i] = pixel_ray(fx, fy, cx, cy, u, v, yn);
+        if (u == 0) ray_yn[v] = yn;
+    }
+}
+
 }  // namespace
 
-cudaError_t launch_verify_fixed_divisor(float y, float inv_y, unsigned long long* mismatches,
-                                        cudaStream_t stream)
+cudaError_t launch_verify_fixed_divisor(float y, float inv_y, int check,
+                                        unsigned long long* mismatches, cudaStream_t stream)
 {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (sms <= 0) sms = 1;
-    verify_fixed_divisor_kernel<<<(unsigned)(sms * 16), kThreads, 0, stream>>>(y, inv_y,
-                                                                              mismatches);
+    const unsigned grid = (unsigned)(sms * 16);
+    if (check == kDivideVoxel)
+        verify_fixed_divisor_kernel<kDivideVoxel><<<grid, kThreads, 0, stream>>>(y, inv_y,
+                                                                                 mismatches);
+    else
+        verify_fixed_divisor_kernel<kDivideTrunc><<<grid, kThreads, 0, stream>>>(y, inv_y,
+                                                                                 mismatches);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_build_rays(float fx, float fy, float cx, float cy, int width, int height,
+                              float4* rays, float* ray_yn, cudaStream_t stream)
+{
+    const size_t n = (size_t)width * (size_t)height;
+    const size_t want = (n + kThreads - 1) / kThreads;
+    const unsigned grid = (unsigned)(want < 8192 ? want : 8192);
+    build_rays_kernel<<<grid, kThreads, 0, stream>>>(fx, fy, cx, cy, width, height, rays,
+                                                     ray_yn);
     return cudaGetLastError();
 }
 

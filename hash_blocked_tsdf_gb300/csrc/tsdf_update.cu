@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
     float cr = 0.0f, cg = 0.0f, cb = 0.0f;
     if (inside) {
         const size_t pix = (size_t)v * fb.width + u;
-        valid = back_project(cam, vol.div, u, v, depth, p);
+        valid = back_project_pixel(vol, fb, cam, v, pix, depth, p);
         if (valid && !kReproject) {
             const float* rgb = fb.frame[f].rgb;
             cr = __ldg(rgb + 3 * pix);
@@ -262,7 +262,7 @@ __device__ __forceinline__ void rows_tile(const VolumeView& vol, const FrameBatc
         float c[3] = {0.0f, 0.0f, 0.0f};
         if (u < fb.width && v < fb.height) {
             const size_t pix = (size_t)v * fb.width + u;
-            valid = back_project(cam, vol.div, u, v, __ldg(fb.frame[f].depth + pix), p);
+            valid = back_project_pixel(vol, fb, cam, v, pix, __ldg(fb.frame[f].depth + pix), p);
             if (valid) {
                 const float* rgb = fb.frame[f].rgb;
                 c[0] = __ldg(rgb + 3 * pix);

@@ -54,6 +54,7 @@ struct tsdf_volume {
     int layout = TSDF_LAYOUT_INTERLEAVED;
     DivisorPair div = {};
     bool fast_div = false;          // the fixed-divisor division by trunc was verified
+    bool fast_voxel = false;        // ... and the one by the voxel edge
 
     Entry* table = nullptr;
     uint32_t* dense_list = nullptr;  // [kDenseListCapacity] adaptive update's dense tiles
@@ -65,6 +66,16 @@ struct tsdf_volume {
     int32_t* noalloc_scratch = nullptr;  // device address of the no-allocation export's
                                          // scratch array, looked up at create
     float* export_scratch = nullptr;  // [5][kExportChunkBlocks][512], allocated on first export
+
+    // the pixels' rays for the last batch's intrinsics and frame size
+    // (FrameBatch::rays), allocated on first use and grown for larger frames
+    float4* rays = nullptr;
+    float* ray_yn = nullptr;
+    size_t ray_pixels = 0;          // capacity of rays, in pixels
+    int ray_rows = 0;               // capacity of ray_yn
+    bool rays_built = false;        // rays hold ray_size / ray_k
+    int ray_size[2] = {0, 0};
+    float ray_k[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 
     // host-batch staging: two buffers of (depth, rgb) frames
     float* stage[2] = {nullptr, nullptr};
@@ -115,6 +126,7 @@ VolumeView view_of(const tsdf_volume* v)
     w.counters = &v->state->counters;
     w.div = v->div;
     w.fast_div = v->fast_div;
+    w.fast_voxel = v->fast_voxel;
     w.occlusion = v->occlusion;
     w.band_half = v->band_half;
     w.dense_list = v->dense_list;
@@ -239,6 +251,8 @@ void release(tsdf_volume* v)
     if (v->state) cudaFree(v->state);
     if (v->coords) cudaFree(v->coords);
     if (v->neighbours) cudaFree(v->neighbours);
+    if (v->rays) cudaFree(v->rays);
+    if (v->ray_yn) cudaFree(v->ray_yn);
     for (int b = 0; b < 2; ++b) {
         if (v->stage[b]) cudaFree(v->stage[b]);
         if (v->copied[b]) cudaEventDestroy(v->copied[b]);
@@ -246,6 +260,50 @@ void release(tsdf_volume* v)
     }
     if (v->copy_stream) cudaStreamDestroy(v->copy_stream);
     delete v;
+}
+
+// Make the volume's ray table hold the rays of a width x height image for
+// the intrinsics of camera c, building it on `stream` unless it already
+// does.  Under stream capture the build is always recorded (a replay must
+// not depend on the table's state outside the graph), and the table must
+// already be large enough: allocating synchronises the device.
+int ensure_rays(tsdf_volume* v, int width, int height, const Camera& c, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    TSDF_CUDA(cudaStreamIsCapturing(stream, &cap), "cudaStreamIsCapturing");
+    const bool capturing = cap != cudaStreamCaptureStatusNone;
+    const size_t px = (size_t)width * (size_t)height;
+    if (v->ray_pixels < px || v->ray_rows < height) {
+        if (capturing)
+            return fail(TSDF_ERR_ARG, "the first integrate call for a frame size allocates the "
+                                      "ray table and must not be made during stream capture");
+        if (v->rays) cudaFree(v->rays);
+        if (v->ray_yn) cudaFree(v->ray_yn);
+        v->rays = nullptr;
+        v->ray_yn = nullptr;
+        v->ray_pixels = 0;
+        v->ray_rows = 0;
+        v->rays_built = false;
+        TSDF_CUDA(cudaMalloc(&v->rays, px * sizeof(float4)), "cudaMalloc(rays)");
+        TSDF_CUDA(cudaMalloc(&v->ray_yn, (size_t)height * sizeof(float)), "cudaMalloc(rays)");
+        v->ray_pixels = px;
+        v->ray_rows = height;
+    }
+    const bool same = v->rays_built && v->ray_size[0] == width && v->ray_size[1] == height &&
+                      v->ray_k[0] == c.fx && v->ray_k[1] == c.fy && v->ray_k[2] == c.cx &&
+                      v->ray_k[3] == c.cy;
+    if (same && !capturing) return TSDF_OK;
+    v->rays_built = false;
+    TSDF_CUDA(launch_build_rays(c.fx, c.fy, c.cx, c.cy, width, height, v->rays, v->ray_yn,
+                                stream), "build_rays kernel");
+    v->rays_built = true;
+    v->ray_size[0] = width;
+    v->ray_size[1] = height;
+    v->ray_k[0] = c.fx;
+    v->ray_k[1] = c.fy;
+    v->ray_k[2] = c.cx;
+    v->ray_k[3] = c.cy;
+    return TSDF_OK;
 }
 
 // Launch the allocate and/or update kernels over n_frames frames laid out
@@ -258,11 +316,18 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
 {
     const VolumeView vol = view_of(v);
     const size_t px = (size_t)width * (size_t)height;
+    if (n_frames > 0) {
+        // one intrinsics matrix per call: every frame's camera has the same
+        const int rc = ensure_rays(v, width, height, cams[0], stream);
+        if (rc) return rc;
+    }
     for (int first = 0; first < n_frames; first += kMaxBatch) {
         FrameBatch fb;
         fb.n = n_frames - first < kMaxBatch ? n_frames - first : kMaxBatch;
         fb.width = width;
         fb.height = height;
+        fb.rays = v->rays;
+        fb.ray_yn = v->ray_yn;
         for (int f = 0; f < fb.n; ++f) {
             fb.frame[f].depth = depth + (first + f) * px;
             fb.frame[f].rgb = rgb ? rgb + 3 * (first + f) * px : nullptr;
@@ -319,19 +384,28 @@ int one_frame(tsdf_volume* v, const float* depth, const float* rgb, int width, i
                          as_stream(stream));
 }
 
-// Check, for every float32 dividend, that the walk's truncated distances come
-// out the same with the fixed-divisor division as with IEEE division.
+// Check, for every float32 dividend, that the walk's truncated distances
+// and the back-projection's divisions by the voxel edge come out the same
+// with the fixed-divisor division as with IEEE division; each is used only
+// where its check passed.
 int verify_divisors(tsdf_volume* v)
 {
     unsigned long long* bad = &v->state->counters.reserved[0];
-    TSDF_CUDA(cudaMemsetAsync(bad, 0, sizeof(unsigned long long), 0), "cudaMemsetAsync");
-    TSDF_CUDA(launch_verify_fixed_divisor(v->div.trunc, v->div.inv_trunc, bad, 0),
-              "verify kernel");
-    unsigned long long h = 1;
-    TSDF_CUDA(cudaMemcpyAsync(&h, bad, sizeof(h), cudaMemcpyDeviceToHost, 0), "cudaMemcpyAsync");
+    unsigned long long h[2] = {1, 1};
+    const float y[2] = {v->div.trunc, v->div.voxel};
+    const float r[2] = {v->div.inv_trunc, v->div.inv_voxel};
+    const int check[2] = {kDivideTrunc, kDivideVoxel};
+    for (int k = 0; k < 2; ++k) {
+        TSDF_CUDA(cudaMemsetAsync(bad, 0, sizeof(unsigned long long), 0), "cudaMemsetAsync");
+        TSDF_CUDA(launch_verify_fixed_divisor(y[k], r[k], check[k], bad, 0), "verify kernel");
+        TSDF_CUDA(cudaMemcpyAsync(&h[k], bad, sizeof(h[k]), cudaMemcpyDeviceToHost, 0),
+                  "cudaMemcpyAsync");
+        TSDF_CUDA(cudaStreamSynchronize(0), "cudaStreamSynchronize");
+    }
     TSDF_CUDA(cudaMemsetAsync(bad, 0, sizeof(unsigned long long), 0), "cudaMemsetAsync");
     TSDF_CUDA(cudaStreamSynchronize(0), "cudaStreamSynchronize");
-    v->fast_div = h == 0;
+    v->fast_div = h[0] == 0;
+    v->fast_voxel = h[1] == 0;
     return TSDF_OK;
 }
 
@@ -439,6 +513,7 @@ int tsdf_get_info(const tsdf_volume* vol, tsdf_info* out)
     out->band_samples = 2 * vol->band_half + 1;
     out->device = vol->device;
     out->fixed_divisor_fast_path = vol->fast_div ? 1 : 0;
+    out->voxel_division_fast_path = vol->fast_voxel ? 1 : 0;
     out->max_frames_per_launch = kMaxBatch;
     out->pool_layout = vol->layout;
     return TSDF_OK;

@@ -113,6 +113,10 @@ typedef struct tsdf_info {
                                           dividend; 0: IEEE division */
     int32_t max_frames_per_launch;    /* frames a batch call packs into one launch */
     int32_t pool_layout;              /* TSDF_LAYOUT_INTERLEAVED or TSDF_LAYOUT_PLANAR */
+    int32_t voxel_division_fast_path; /* 1: the back-projection's division by the voxel
+                                          edge uses the same sequence, checked at create
+                                          to equal IEEE division bit for bit for every
+                                          float32 dividend; 0: IEEE division */
 } tsdf_info;
 
 /* Device pointers to the pool's five sums.  Record v = b * 512 + s (block b,

@@ -631,4 +631,39 @@ def test_fixed_divisor_fast_path_verified(torch_cuda, voxel, trunc):
     from hash_blocked_tsdf_gb300 import TsdfVolume
     vol = TsdfVolume(64, voxel, trunc)
     assert vol.info["fixed_divisor_fast_path"] == 1
+    # the back-projection's division by the voxel edge, checked bit for bit
+    assert vol.info["voxel_division_fast_path"] == 1
+    vol.close()
+
+
+def test_ray_table_follows_frame_size_and_intrinsics(torch_cuda, oracle_mod):
+    """The back-projection reads each pixel's ray from a table the volume
+    builds for the call's frame size and intrinsics.  One volume takes frames
+    of two sizes and three intrinsics, back and forth (the table is rebuilt,
+    grown, and reused); the result must be the oracle's for the same
+    sequence."""
+    torch = torch_cuda
+    from hash_blocked_tsdf_gb300 import TsdfVolume
+    voxel, trunc = 0.01, 0.04
+    seq = []
+    for n, (W, H, scale) in enumerate([(161, 121, 0.8), (161, 121, 0.9), (320, 240, 0.8),
+                                       (161, 121, 0.8), (320, 240, 0.7)]):
+        depth, rgb, pose, K = scenes.sphere_plane(W, H, fx=scale * max(W, H),
+                                                  fy=scale * max(W, H) * 1.01,
+                                                  noise_sigma=0.002, invalid_frac=0.05, seed=n)
+        seq.append((depth, rgb, pose, np.asarray(K, np.float32)))
+    vol = TsdfVolume(8192, voxel, trunc)
+    o = oracle_mod.OracleVolume(voxel, trunc)
+    for n, (depth, rgb, pose, K) in enumerate(seq):
+        d = torch.from_numpy(depth).cuda()
+        c = torch.from_numpy(rgb).cuda()
+        if n % 2:
+            vol.integrate(d, c, K, pose)
+        else:
+            vol.integrate_batch(d[None], c[None], K, pose[None])
+        o.integrate(depth, rgb, K, pose)
+    torch.cuda.synchronize()
+    rep = parity.compare_volume(vol.export_blocks(), o.export(), strict=False)
+    parity.check_counters(vol.stats(), o.counters())
+    assert rep["blocks"] > 0
     vol.close()
