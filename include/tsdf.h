@@ -237,7 +237,14 @@ int tsdf_update(tsdf_volume* vol, const float* depth, const float* rgb, int widt
  * neighbouring frames meet in L2.  The result equals integrating the frames
  * one by one (same blocks, same weights; sums up to float summation order),
  * except under pool exhaustion, where which blocks are refused depends on the
- * order in which inserts win pool indices, which is unspecified. */
+ * order in which inserts win pool indices, which is unspecified.
+ *
+ * Every batch and single-frame call back-projects through a per-pixel ray
+ * table the volume keeps for the last frame size and K (16 bytes per pixel
+ * plus 4 per row), rebuilt on `stream` when either changes.  The first call
+ * with a larger frame than any before allocates it (cudaMalloc, which
+ * synchronises the device), so that call must not be made during stream
+ * capture (TSDF_ERR_ARG); under capture the rebuild is always recorded. */
 int tsdf_integrate_batch(tsdf_volume* vol, int n_frames, const float* depth, const float* rgb,
                          int width, int height, const float K[4], const float* poses,
                          void* stream);
