@@ -60,12 +60,28 @@ struct InsertResult {
 // are merged, one leader per key probes, and the warp's winners take pool
 // indices together and publish them before the step returns.  Every offering
 // lane gets its key's outcome and slot.  Must be called by all 32 lanes.
+// Most keys a frame offers are already in the table, and almost all of those
+// sit in their home slot: each offering lane first reads its key's home
+// slot, and only the lanes that do not find their key there go on to the
+// warp's de-duplication and the probe (keys are never removed, so a key seen
+// there is in the table).  With kInstrument every offered key is probed, so
+// that the probe statistics count every key.
 template <bool kInstrument, bool kResult = true>
 __device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, bool fresh,
                                                          unsigned long long key, ProbeStats* st)
 {
     const unsigned lane = lane_id();
     InsertResult out = {kProbeOverflow, 0u};
+    bool at_home = false;
+    if (!kInstrument && fresh) {
+        const uint32_t home = home_slot(key, vol.table_mask);
+        at_home = vol.table[home].key == key;
+        if (at_home) {
+            out.res = kProbeFound;
+            out.slot = home;
+            fresh = false;
+        }
+    }
     const unsigned fresh_mask = __ballot_sync(0xFFFFFFFFu, fresh);
     if (fresh_mask == 0) return out;
     bool leader = false;
@@ -83,8 +99,12 @@ __device__ __forceinline__ InsertResult warp_insert_step(const VolumeView& vol, 
         if (res == kProbeOverflow) atomicAdd(&vol.counters->probe_overflow, 1ull);
     }
     if (kResult) {                          // (the allocate kernel does not need it)
-        out.res = __shfl_sync(0xFFFFFFFFu, res, leader_lane);
-        out.slot = __shfl_sync(0xFFFFFFFFu, slot, leader_lane);
+        const int r = __shfl_sync(0xFFFFFFFFu, res, leader_lane);
+        const uint32_t sl = __shfl_sync(0xFFFFFFFFu, slot, leader_lane);
+        if (!at_home) {
+            out.res = r;
+            out.slot = sl;
+        }
     }
     const bool won = leader && res == kProbeWon;
     const unsigned won_mask = __ballot_sync(0xFFFFFFFFu, won);
