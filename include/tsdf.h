@@ -265,7 +265,9 @@ int tsdf_update_batch(tsdf_volume* vol, int n_frames, const float* depth, const 
  * call overlaps them with the kernels instead).  Each group of
  * frames is copied into a double-buffered device staging area owned by the
  * volume on a separate copy stream, overlapping the copy of group g + 1 with
- * the kernels of group g.  For the copies to be asynchronous the host arrays must be
+ * the kernels of group g.  The first group has 16 frames and each next one
+ * about a third more, up to max_frames_per_launch, so that the kernels start
+ * after a short copy instead of a full group's.  For the copies to be asynchronous the host arrays must be
  * page-locked (cudaHostAlloc / cudaHostRegister); pageable memory works but
  * serialises.  The host arrays must stay valid and unchanged until the work on
  * `stream` has finished.  The staging area is allocated on first use (and
