@@ -23,10 +23,12 @@
 // block's seven upper neighbours (+x, +y, +z and their combinations) in the
 // table, all in parallel; the block's 512 means and the 217 lattice points its cells take from those
 // neighbours go to shared memory (9 x 9 x 9, NaN where unobserved); each
-// thread classifies two cells by the sign mask of their corners; the
-// tetrahedra the surface crosses become one task list for the block (scans
-// of the task and triangle counts; one atomic takes the block's range of the
-// output), and all 256 threads emit the list's triangles.
+// thread classifies two cells by the sign mask of their corners (one lookup
+// in a table built at compile time gives the crossed tetrahedra); the
+// tetrahedra the surface crosses become one task list for the block, those
+// with two triangles first (scans of both counts; one atomic takes the
+// block's range of the output), and all 256 threads emit the list's
+// triangles.
 #include "tsdf_device.cuh"
 
 namespace tsdf {
@@ -145,13 +147,50 @@ constexpr int kLat = 9;
 constexpr int kLatPoints = kLat * kLat * kLat;          // 729
 constexpr int kHaloPoints = kLatPoints - kBlockVoxels;  // 217
 
-// Bit mask (bit k = corner k, k = 0..7) of the cube corners of tetrahedron
-// `tet` (tet_corner's sets).
-__device__ __forceinline__ uint32_t tet_corner_mask(int tet)
+// For every inside mask m of a cell's eight corners (bit k = corner k), the
+// cell's crossed tetrahedra: bits 0-5 mark the tetrahedra that have both
+// inside and outside corners, bits 8-13 those among them with two corners
+// inside (two triangles; one or three inside give one).  Built at compile
+// time from tet_corner's sets, so a cell is classified with one lookup.
+struct CellTable {
+    uint32_t v[256];
+};
+
+constexpr uint32_t tet_mask_c(int tet)
 {
-    return (1u << tet_corner(tet, 0)) | (1u << tet_corner(tet, 1)) | (1u << tet_corner(tet, 2)) |
-           (1u << tet_corner(tet, 3));
+    const int p = tet >> 1;
+    const int lo = p == 0 ? 1 : 0, hi = p == 2 ? 1 : 2;
+    const int q = (tet & 1) ? hi : lo;
+    return 1u | (1u << (1 << p)) | (1u << ((1 << p) | (1 << q))) | (1u << 7);
 }
+// the sets {0,1,3,7} {0,1,5,7} {0,2,3,7} {0,2,6,7} {0,4,5,7} {0,4,6,7}
+static_assert(tet_mask_c(0) == 0x8Bu && tet_mask_c(1) == 0xA3u && tet_mask_c(2) == 0x8Du &&
+                  tet_mask_c(3) == 0xC5u && tet_mask_c(4) == 0xB1u && tet_mask_c(5) == 0xD1u,
+              "tetrahedron corner sets");
+
+constexpr int popcount_c(uint32_t x)
+{
+    int n = 0;
+    for (; x; x &= x - 1) ++n;
+    return n;
+}
+
+constexpr CellTable make_cell_table()
+{
+    CellTable t{};
+    for (int m = 0; m < 256; ++m) {
+        uint32_t e = 0;
+        for (int tet = 0; tet < 6; ++tet) {
+            const int k = popcount_c((uint32_t)m & tet_mask_c(tet));
+            if (k != 0 && k != 4) e |= 1u << tet;
+            if (k == 2) e |= 1u << (8 + tet);
+        }
+        t.v[m] = e;
+    }
+    return t;
+}
+
+__device__ const CellTable kCellTable = make_cell_table();
 
 // Lattice index of corner k of the cell at (lx, ly, lz).
 __device__ __forceinline__ int corner_point(int base, int k)
@@ -195,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
     // first triangle within the block << 12
     __shared__ uint32_t s_task[6 * kBlockVoxels];
     __shared__ uint32_t s_warp_tasks[kThreads / 32], s_warp_tris[kThreads / 32];
-    __shared__ uint32_t s_total_tasks;
+    __shared__ uint32_t s_total_tasks, s_total_twos;
     __shared__ unsigned long long s_first;
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
@@ -237,11 +276,10 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
     __syncthreads();
 
     // the two cells of this thread: the sign mask of their corners (a cell
-    // counts when all 8 corners are observed and the surface crosses it), and
-    // the tetrahedra of each that the surface crosses
-    uint32_t tets = 0;                  // bits 0-5: cell 0's tetrahedra, 8-13: cell 1's
-    uint32_t masks = 0;                 // bits 0-7: cell 0's inside corners, 8-15: cell 1's
-    int n_tris = 0;
+    // counts when all 8 corners are observed), and from it the tetrahedra
+    // the surface crosses (bits 0-5 for cell 0, 8-13 for cell 1) and those
+    // of them holding two triangles
+    uint32_t tets = 0, twos = 0;
 #pragma unroll
     for (int c = 0; c < 2; ++c) {
         const int j = t + c * kThreads;
@@ -254,64 +292,63 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
             seen = seen && !isnan(v);
             m |= (v < 0.0f ? 1u : 0u) << k;
         }
-        if (seen && m != 0u && m != 0xFFu) {
-            masks |= m << (8 * c);
-#pragma unroll
-            for (int tet = 0; tet < 6; ++tet) {
-                const int k = __popc(m & tet_corner_mask(tet));
-                if (k != 0 && k != 4) {
-                    tets |= 1u << (8 * c + tet);
-                    n_tris += k == 2 ? 2 : 1;
-                }
-            }
+        if (seen) {
+            const uint32_t e = __ldg(&kCellTable.v[m]);
+            tets |= (e & 0x3Fu) << (8 * c);
+            twos |= ((e >> 8) & 0x3Fu) << (8 * c);
         }
     }
 
-    // the block's crossed tetrahedra become one task list (block-wide scans of
-    // the task and triangle counts), so every thread emits triangles, not
-    // only the few that hold surface cells
+    // the block's crossed tetrahedra become one task list: those with two
+    // triangles first, then those with one, so that the warps emitting
+    // them take the same path (block-wide scans of both counts)
     const unsigned lane = lane_id();
     const int warp = t >> 5;
-    uint32_t n_tasks = (uint32_t)__popc(tets);
-    uint32_t task_incl = n_tasks, tri_incl = (uint32_t)n_tris;
+    const uint32_t n2 = (uint32_t)__popc(twos), n1 = (uint32_t)__popc(tets) - n2;
+    uint32_t incl2 = n2, incl1 = n1;
 #pragma unroll
     for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t a = __shfl_up_sync(0xFFFFFFFFu, task_incl, d);
-        const uint32_t b2 = __shfl_up_sync(0xFFFFFFFFu, tri_incl, d);
+        const uint32_t a2 = __shfl_up_sync(0xFFFFFFFFu, incl2, d);
+        const uint32_t a1 = __shfl_up_sync(0xFFFFFFFFu, incl1, d);
         if ((int)lane >= d) {
-            task_incl += a;
-            tri_incl += b2;
+            incl2 += a2;
+            incl1 += a1;
         }
     }
     if (lane == 31) {
-        s_warp_tasks[warp] = task_incl;
-        s_warp_tris[warp] = tri_incl;
+        s_warp_tasks[warp] = incl2;
+        s_warp_tris[warp] = incl1;
     }
     __syncthreads();
     if (t == 0) {
-        uint32_t tasks = 0, tris = 0;
+        uint32_t c2 = 0, c1 = 0;
         for (int w = 0; w < kThreads / 32; ++w) {
-            const uint32_t a = s_warp_tasks[w], b2 = s_warp_tris[w];
-            s_warp_tasks[w] = tasks;
-            s_warp_tris[w] = tris;
-            tasks += a;
-            tris += b2;
+            const uint32_t a2 = s_warp_tasks[w], a1 = s_warp_tris[w];
+            s_warp_tasks[w] = c2;
+            s_warp_tris[w] = c1;
+            c2 += a2;
+            c1 += a1;
         }
-        s_total_tasks = tasks;
+        s_total_twos = c2;
+        s_total_tasks = c2 + c1;
+        const uint32_t tris = 2 * c2 + c1;
         s_first = tris ? atomicAdd(count, (unsigned long long)tris) : 0ull;
     }
     __syncthreads();
-    uint32_t task = s_warp_tasks[warp] + task_incl - n_tasks;
-    uint32_t tri = s_warp_tris[warp] + tri_incl - (uint32_t)n_tris;
+    const uint32_t total_twos = s_total_twos;
+    uint32_t r2 = s_warp_tasks[warp] + incl2 - n2;          // this thread's first ranks
+    uint32_t r1 = s_warp_tris[warp] + incl1 - n1;
     while (tets) {
         const int bit = __ffs(tets) - 1;
         tets &= tets - 1u;
-        const int c = bit >> 3, tet = bit & 7;
-        s_task[task] = (uint32_t)(t + c * kThreads) | ((uint32_t)tet << 9) | (tri << 12);
-        ++task;
-        // (a crossed tetrahedron holds 1 or 2 triangles)
-        const uint32_t m = (masks >> (8 * c)) & 0xFFu;
-        tri += __popc(m & tet_corner_mask(tet)) == 2 ? 2u : 1u;
+        const uint32_t cell_tet = (uint32_t)(t + (bit >> 3) * kThreads) | ((uint32_t)(bit & 7) << 9);
+        if ((twos >> bit) & 1u) {
+            s_task[r2] = cell_tet | ((2 * r2) << 12);
+            ++r2;
+        } else {
+            s_task[total_twos + r1] = cell_tet | ((2 * total_twos + r1) << 12);
+            ++r1;
+        }
     }
     __syncthreads();
 
