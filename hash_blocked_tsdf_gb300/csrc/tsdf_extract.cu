@@ -105,39 +105,48 @@ __device__ __forceinline__ int inside_mask(const Tet& T)
            (T.v[3] < 0.0f ? 8 : 0);
 }
 
-// Writes the tetrahedron's triangles from index `next` on (those at or past
-// `capacity` are dropped); returns the index after them.
-__device__ __forceinline__ uint64_t emit_tet(const Tet& T, const int cell[3], float voxel,
-                                             float* out, uint64_t capacity, uint64_t next)
+// Triangle `which` of the tetrahedron (which = 1 only when two of its
+// corners are inside and it holds two): its three edges are chosen by case,
+// then one write_triangle computes them, so that lanes in different cases
+// share the vertex arithmetic.
+__device__ __forceinline__ void tet_triangle(const Tet& T, const int cell[3], float voxel,
+                                             int which, float* tri)
 {
     const int in = inside_mask(T);
     const int ot = ~in & 0xF;
     const int n_in = __popc(in);
-    if (n_in == 1 || n_in == 3) {
-        // the odd corner, then the other three in tetrahedron order
-        const int odd_set = n_in == 1 ? in : ot;
-        int rest = n_in == 1 ? ot : in;
-        const int o = __ffs(odd_set) - 1;
-        const int r0 = __ffs(rest) - 1;
-        rest &= rest - 1;
-        const int r1 = __ffs(rest) - 1;
-        rest &= rest - 1;
-        const int r2 = __ffs(rest) - 1;
-        if (next < capacity) write_triangle(T, cell, o, r0, o, r1, o, r2, voxel, out + 9 * next);
-        return next + 1;
-    }
+    int p0, q0, p1, q1, p2, q2;
     if (n_in == 2) {
         const int i0 = __ffs(in) - 1;
         const int i1 = __ffs(in & (in - 1)) - 1;
         const int o0 = __ffs(ot) - 1;
         const int o1 = __ffs(ot & (ot - 1)) - 1;
-        if (next < capacity)
-            write_triangle(T, cell, i0, o0, i0, o1, i1, o1, voxel, out + 9 * next);
-        if (next + 1 < capacity)
-            write_triangle(T, cell, i0, o0, i1, o1, i1, o0, voxel, out + 9 * (next + 1));
-        return next + 2;
+        p0 = i0; q0 = o0;
+        p1 = which ? i1 : i0; q1 = o1;
+        p2 = i1; q2 = which ? o0 : o1;
+    } else {
+        // the odd corner, then the other three in tetrahedron order
+        const int odd_set = n_in == 1 ? in : ot;
+        int rest = n_in == 1 ? ot : in;
+        const int o = __ffs(odd_set) - 1;
+        p0 = p1 = p2 = o;
+        q0 = __ffs(rest) - 1;
+        rest &= rest - 1;
+        q1 = __ffs(rest) - 1;
+        rest &= rest - 1;
+        q2 = __ffs(rest) - 1;
     }
-    return next;
+    write_triangle(T, cell, p0, q0, p1, q1, p2, q2, voxel, tri);
+}
+
+// A warp's staged triangles (n of them, 9 floats each) to output triangles
+// [at, at + n), in contiguous stores; those at or past `capacity` are
+// dropped.
+__device__ __forceinline__ void flush_triangles(const float* stage, float* out, uint64_t at,
+                                                uint32_t n, uint64_t capacity, unsigned lane)
+{
+    const uint32_t kept = at >= capacity ? 0u : (uint32_t)min((uint64_t)n, capacity - at);
+    for (uint32_t i = lane; i < 9u * kept; i += 32u) out[9 * at + i] = stage[i];
 }
 
 // The block's lattice with its upper neighbours' first layer: 9 x 9 x 9
@@ -230,11 +239,11 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
                                                           unsigned long long* count)
 {
     __shared__ float s_lat[kLatPoints];
-    // crossed tetrahedra of the block: cell (9 bits) | tetrahedron (3) << 9 |
-    // first triangle within the block << 12
+    // crossed tetrahedra of the block: cell (9 bits) | tetrahedron (3) << 9
     __shared__ uint32_t s_task[6 * kBlockVoxels];
     __shared__ uint32_t s_warp_tasks[kThreads / 32], s_warp_tris[kThreads / 32];
     __shared__ uint32_t s_total_tasks, s_total_twos;
+    __shared__ float s_stage[kThreads / 32 * 32 * 9];    // each warp's 32 staged triangles
     __shared__ unsigned long long s_first;
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
@@ -342,34 +351,55 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
         const int bit = __ffs(tets) - 1;
         tets &= tets - 1u;
         const uint32_t cell_tet = (uint32_t)(t + (bit >> 3) * kThreads) | ((uint32_t)(bit & 7) << 9);
-        if ((twos >> bit) & 1u) {
-            s_task[r2] = cell_tet | ((2 * r2) << 12);
-            ++r2;
-        } else {
-            s_task[total_twos + r1] = cell_tet | ((2 * total_twos + r1) << 12);
-            ++r1;
-        }
+        if ((twos >> bit) & 1u)
+            s_task[r2++] = cell_tet;
+        else
+            s_task[total_twos + r1++] = cell_tet;
     }
     __syncthreads();
 
+    // Emission, 32 tasks per warp round (task k0 + lane).  A round's
+    // triangles fill one contiguous range of the block's output: the first
+    // triangles of its two-triangle tasks, then their second triangles and
+    // the one-triangle tasks' triangles.  Each half is staged in the warp's
+    // shared slots and leaves in contiguous stores.
     const float voxel = vol.div.voxel;
     const unsigned long long first = s_first;
     const uint32_t total = s_total_tasks;
-    for (uint32_t k = (uint32_t)t; k < total; k += kThreads) {
-        const uint32_t code = s_task[k];
-        const int j = (int)(code & 511u);
-        const int tet = (int)((code >> 9) & 7u);
-        const uint32_t at = code >> 12;
-        const int base = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
-        const int cell[3] = {bc[0] * kBlockEdge + (j & 7), bc[1] * kBlockEdge + ((j >> 3) & 7),
-                             bc[2] * kBlockEdge + (j >> 6)};
+    float* stage = s_stage + warp * 32 * 9;
+    for (uint32_t k0 = (uint32_t)warp * 32u; k0 < total; k0 += kThreads) {
+        const uint32_t k = k0 + lane;
+        const bool active = k < total;
+        const uint32_t n_a = total_twos > k0 ? min(total_twos - k0, 32u) : 0u;
+        const uint32_t n_act = min(total - k0, 32u);
+        const uint64_t at = first + 2ull * min(k0, total_twos) + (k0 > total_twos ? k0 - total_twos : 0u);
         Tet T;
+        int cell[3] = {0, 0, 0};
+        if (active) {
+            const uint32_t code = s_task[k];
+            const int j = (int)(code & 511u);
+            const int tet = (int)((code >> 9) & 7u);
+            const int base = (j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat;
+            cell[0] = bc[0] * kBlockEdge + (j & 7);
+            cell[1] = bc[1] * kBlockEdge + ((j >> 3) & 7);
+            cell[2] = bc[2] * kBlockEdge + (j >> 6);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            T.id[q] = tet_corner(tet, q);
-            T.v[q] = s_lat[corner_point(base, T.id[q])];
+            for (int q = 0; q < 4; ++q) {
+                T.id[q] = tet_corner(tet, q);
+                T.v[q] = s_lat[corner_point(base, T.id[q])];
+            }
         }
-        emit_tet(T, cell, voxel, out, capacity, first + at);
+        if (n_a) {
+            if (lane < n_a && at + lane < capacity) tet_triangle(T, cell, voxel, 0, stage + 9 * lane);
+            __syncwarp();
+            flush_triangles(stage, out, at, n_a, capacity, lane);
+            __syncwarp();
+        }
+        if (active && at + n_a + lane < capacity)
+            tet_triangle(T, cell, voxel, lane < n_a ? 1 : 0, stage + 9 * lane);
+        __syncwarp();
+        flush_triangles(stage, out, at + n_a, n_act, capacity, lane);
+        __syncwarp();
     }
 }
 

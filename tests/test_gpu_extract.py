@@ -98,6 +98,36 @@ def test_extract_equals_oracle_on_a_closed_sphere(torch_cuda, oracle_mod):
     vol.close()
 
 
+def test_extract_block_with_thousands_of_triangles(torch_cuda, oracle_mod):
+    # an alternating-sign field: every cell crossed, up to 12 triangles per
+    # cell, thousands per block (many emission rounds per warp, with both
+    # halves of a round full), in full and with an output capacity that cuts
+    # through a block's range
+    voxel = 0.01
+    o = oracle_mod.OracleVolume(voxel, 4 * voxel)
+    j = np.arange(512)
+    local = np.stack([j % 8, (j // 8) % 8, j // 64], axis=1)
+    rng = np.random.default_rng(5)
+    for bx in range(2):
+        for bz in range(2):
+            idx = local + 8 * np.array([bx, 0, bz])
+            sign = np.where(idx.sum(axis=1) % 2 == 0, 1.0, -1.0)
+            val = sign * (0.25 + rng.random(512))
+            w = rng.integers(1, 5, size=512).astype(np.float64)
+            o.set_block((bx, 0, bz), w * val, w, w * 0.1, w * 0.2, w * 0.3)
+    vol, _ = _import_oracle(torch_cuda, o, voxel, 4 * voxel)
+    ref = o.extract()
+    assert len(ref) > 4 * 2000
+    full = vol.extract_triangles()
+    _assert_same_triangles(full, ref)
+    for cap in (len(ref) // 2 + 7, 31, 33):
+        part = vol.extract_triangles(capacity=cap)
+        assert len(part) == cap
+        full_rows = {tuple(r) for r in _sorted_rows(full.cpu().numpy())}
+        assert all(tuple(r) in full_rows for r in _sorted_rows(part.cpu().numpy()))
+    vol.close()
+
+
 def test_extract_after_gpu_integration_against_the_oracle(torch_cuda, oracle_mod):
     from hash_blocked_tsdf_gb300 import TsdfVolume
     torch = torch_cuda
