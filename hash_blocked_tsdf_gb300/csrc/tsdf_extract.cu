@@ -248,40 +248,46 @@ __global__ void __launch_bounds__(kThreads, 8) extract_kernel(VolumeView vol, co
     const uint32_t b = blockIdx.x;
     const int t = threadIdx.x;
     const int bc[3] = {coords[3 * b], coords[3 * b + 1], coords[3 * b + 2]};
-    // the block's own 512 means
-    for (int j = t; j < kBlockVoxels; j += kThreads) {
-        const float2 tw = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + voxel_slot_of(vol, j));
-        s_lat[(j & 7) + ((j >> 3) & 7) * kLat + (j >> 6) * kLat * kLat] =
-            tw.y > 0.0f ? __fdiv_rn(tw.x, tw.y) : __int_as_float(0x7FFFFFFF);
+    // the block's own 512 means (two per thread) and the upper neighbours'
+    // first layers: +x face, +y face, +z face (64 points each), the three
+    // edges (8 each) and the corner.  The neighbour's index is loaded first,
+    // so that its dependent load overlaps the thread's own two.
+    static_assert(kBlockVoxels == 2 * kThreads, "two voxels per thread");
+    const bool halo = t < kHaloPoints;
+    int d = 0, lx = 0, ly = 0, lz = 0;      // neighbour, and the lattice point (0..8)
+    if (t < 64) {
+        d = 1; lx = 8; ly = t & 7; lz = t >> 3;
+    } else if (t < 128) {
+        d = 2; lx = (t - 64) & 7; ly = 8; lz = (t - 64) >> 3;
+    } else if (t < 192) {
+        d = 4; lx = (t - 128) & 7; ly = (t - 128) >> 3; lz = 8;
+    } else if (t < 200) {
+        d = 3; lx = 8; ly = 8; lz = t - 192;
+    } else if (t < 208) {
+        d = 5; lx = 8; ly = t - 200; lz = 8;
+    } else if (t < 216) {
+        d = 6; lx = t - 208; ly = 8; lz = 8;
+    } else {
+        d = 7; lx = 8; ly = 8; lz = 8;
     }
-    // the upper neighbours' first layers: +x face, +y face, +z face (64 points
-    // each), the three edges (8 each) and the corner
-    if (t < kHaloPoints) {
-        int d, lx, ly, lz;                  // neighbour, and the lattice point (0..8)
-        if (t < 64) {
-            d = 1; lx = 8; ly = t & 7; lz = t >> 3;
-        } else if (t < 128) {
-            d = 2; lx = (t - 64) & 7; ly = 8; lz = (t - 64) >> 3;
-        } else if (t < 192) {
-            d = 4; lx = (t - 128) & 7; ly = (t - 128) >> 3; lz = 8;
-        } else if (t < 200) {
-            d = 3; lx = 8; ly = 8; lz = t - 192;
-        } else if (t < 208) {
-            d = 5; lx = 8; ly = t - 200; lz = 8;
-        } else if (t < 216) {
-            d = 6; lx = t - 208; ly = 8; lz = 8;
-        } else {
-            d = 7; lx = 8; ly = 8; lz = 8;
-        }
-        float v = __int_as_float(0x7FFFFFFF);
-        const uint32_t n_idx = __ldg(nb + 8 * (size_t)b + d);
-        if (n_idx < vol.pool_capacity) {
-            const int jj = (lx & 7) | ((ly & 7) << 3) | ((lz & 7) << 6);
-            const float2 tw = tsdf_and_weight(vol, (size_t)n_idx * kBlockVoxels + voxel_slot_of(vol, jj));
-            if (tw.y > 0.0f) v = __fdiv_rn(tw.x, tw.y);
-        }
-        s_lat[lx + ly * kLat + lz * kLat * kLat] = v;
+    const uint32_t n_idx = halo ? __ldg(nb + 8 * (size_t)b + d) : kIndexFailed;
+    const float2 own0 = tsdf_and_weight(vol, (size_t)b * kBlockVoxels + voxel_slot_of(vol, t));
+    const float2 own1 =
+        tsdf_and_weight(vol, (size_t)b * kBlockVoxels + voxel_slot_of(vol, t + kThreads));
+    float2 tw_h = make_float2(0.0f, 0.0f);
+    if (n_idx < vol.pool_capacity) {
+        const int jj = (lx & 7) | ((ly & 7) << 3) | ((lz & 7) << 6);
+        tw_h = tsdf_and_weight(vol, (size_t)n_idx * kBlockVoxels + voxel_slot_of(vol, jj));
     }
+    const float nan = __int_as_float(0x7FFFFFFF);
+    {
+        const int j0 = t, j1 = t + kThreads;
+        s_lat[(j0 & 7) + ((j0 >> 3) & 7) * kLat + (j0 >> 6) * kLat * kLat] =
+            own0.y > 0.0f ? __fdiv_rn(own0.x, own0.y) : nan;
+        s_lat[(j1 & 7) + ((j1 >> 3) & 7) * kLat + (j1 >> 6) * kLat * kLat] =
+            own1.y > 0.0f ? __fdiv_rn(own1.x, own1.y) : nan;
+    }
+    if (halo) s_lat[lx + ly * kLat + lz * kLat * kLat] = tw_h.y > 0.0f ? __fdiv_rn(tw_h.x, tw_h.y) : nan;
     __syncthreads();
 
     // the two cells of this thread: the sign mask of their corners (a cell
