@@ -191,6 +191,12 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
         // when every lane's whole band lies in the key range (always, in
         // practice) the per-sample range check is left out
         const bool all_in = __all_sync(0xFFFFFFFFu, !valid || ray_in_range(p, fhalf));
+        // the proven steps as one bound on j: step j (at fi = j - half, an
+        // integer) is proven when max(fi, 0) <= i_max, i.e. when
+        // j <= half + floor(i_max) and i_max >= 0
+        int j_proven = -1;
+        if (!kReproject && sure.near && sure.i_max >= 0.0f)
+            j_proven = half + (int)floorf(fminf(sure.i_max, fhalf));
 #pragma unroll
         for (int j = 0; j < kShortBand; ++j) {
             if (valid && j < steps) {
@@ -205,8 +211,7 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                     ++out_of_range;
                 } else {
                     const int bx = s.ix >> 3, by = s.iy >> 3, bz = s.iz >> 3;
-                    const bool proven = !kReproject && sure.near &&
-                                        fmaxf(fi, 0.0f) <= sure.i_max;
+                    const bool proven = j <= j_proven;
                     if ((!any || bx != lbx || by != lby || bz != lbz) &&
                         (proven || allocate_visible<kFast, kReproject>(vol, cam, p, depth,
                                                                        fb.width, fb.height, s))) {
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
                 const int j = __ffs(starts) - 1;
                 starts &= starts - 1u;
                 VoxelSample s;
-                band_voxel<kFast>(cam, vol.div, p, j - half, s);
+                band_voxel_unchecked(p, __fsub_rn((float)j, fhalf), s);    // a passing step: in range
                 key = block_key(s.ix, s.iy, s.iz);
             }
             warp_insert_step<kInstrument, false>(vol, offer, key, &st);
