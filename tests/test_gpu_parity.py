@@ -295,6 +295,41 @@ def test_host_batch_matches_device_batch(torch_cuda, oracle_mod):
     b.close()
 
 
+def test_host_batch_over_many_groups_matches_device_batch(torch_cuda):
+    """A host batch long enough for several staging groups: the groups grow
+    from 16 frames (16, 21, 28, 15 for 80 frames), and the double-buffered
+    staging area is reused twice.  The result must be the device batch's:
+    the same blocks, weights and counters, sums equal up to the order of
+    the float additions."""
+    torch = torch_cuda
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 80))
+    a = _gpu_volume(torch, frames)
+    _integrate_gpu(torch, frames, a)
+    b = _gpu_volume(torch, frames)
+    d = torch.from_numpy(frames.depth).pin_memory()
+    c = torch.from_numpy(frames.rgb).pin_memory()
+    b.integrate_batch_host(d, c, frames.K, frames.poses)
+    torch.cuda.synchronize()
+    ga, gb = a.export_blocks(), b.export_blocks()
+    oa, ob = parity.sort_by_coords(ga["coords"]), parity.sort_by_coords(gb["coords"])
+    assert np.array_equal(ga["coords"][oa], gb["coords"][ob])
+    assert np.array_equal(ga["weight"][oa], gb["weight"][ob])
+    # two float32 summations of the same w terms, |tsdf term| <= 1 and colour
+    # terms >= 0: each within gamma(w) of the exact sum of |terms|
+    w = ga["weight"][oa].astype(np.float64)
+    u = 2.0 ** -24
+    for k in ("tsdf", "r", "g", "b"):
+        x, y = ga[k][oa].astype(np.float64), gb[k][ob].astype(np.float64)
+        mag = w if k == "tsdf" else np.abs(x)
+        bound = 2.0 * w * u * mag + 1e-5 * np.abs(x) + 1e-6
+        assert np.all(np.abs(x - y) <= bound), k
+    sa, sb = a.stats(), b.stats()
+    for k in ("valid_points", "voxel_updates", "missed_contributions", "out_of_range_samples"):
+        assert sa[k] == sb[k], k
+    a.close()
+    b.close()
+
+
 @pytest.mark.parametrize("layout", ["interleaved", "planar"])
 def test_pool_view_matches_export(torch_cuda, layout):
     """The zero-copy pool view: tsdf, weight, r and g interleaved per voxel
