@@ -330,6 +330,41 @@ def test_host_batch_over_many_groups_matches_device_batch(torch_cuda):
     b.close()
 
 
+def test_integrate_batch_replayed_from_a_cuda_graph(torch_cuda):
+    """A reset and a batch integration captured into a CUDA graph (after one
+    call with the same frame size has allocated the ray table) and replayed
+    twice give the volume a direct call gives: the same blocks and weights,
+    sums equal up to the order of the float additions."""
+    torch = torch_cuda
+    frames = scenes.orbit_trajectory(n_frames=100, frames=(0, 8))
+    d = torch.from_numpy(frames.depth).cuda()
+    c = torch.from_numpy(frames.rgb).cuda()
+    ref = _gpu_volume(torch, frames)
+    ref.integrate_batch(d, c, frames.K, frames.poses)
+    vol = _gpu_volume(torch, frames)
+    vol.integrate_batch(d[:1], c[:1], frames.K, frames.poses[:1])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        vol.reset()
+        vol.integrate_batch(d, c, frames.K, frames.poses)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    ga, gb = ref.export_blocks(), vol.export_blocks()
+    oa, ob = parity.sort_by_coords(ga["coords"]), parity.sort_by_coords(gb["coords"])
+    assert np.array_equal(ga["coords"][oa], gb["coords"][ob])
+    assert np.array_equal(ga["weight"][oa], gb["weight"][ob])
+    w = ga["weight"][oa].astype(np.float64)
+    u = 2.0 ** -24
+    for k in ("tsdf", "r", "g", "b"):
+        x, y = ga[k][oa].astype(np.float64), gb[k][ob].astype(np.float64)
+        mag = w if k == "tsdf" else np.abs(x)
+        assert np.all(np.abs(x - y) <= 2.0 * w * u * mag + 1e-5 * np.abs(x) + 1e-6), k
+    ref.close()
+    vol.close()
+
+
 @pytest.mark.parametrize("layout", ["interleaved", "planar"])
 def test_pool_view_matches_export(torch_cuda, layout):
     """The zero-copy pool view: tsdf, weight, r and g interleaved per voxel
