@@ -77,6 +77,9 @@ def parse_args():
     ap.add_argument("--probe-report", action="store_true",
                     help="print the probe-depth histogram at table occupancy 0.1 .. 0.5 "
                          "(untimed) instead of the headline workload")
+    ap.add_argument("--probe-atomics", action="store_true",
+                    help="print the shared-memory atomic and 32-byte record reduction rates "
+                         "(untimed by the driver) instead of the headline workload")
     ap.add_argument("--pool", type=int, default=0,
                     help="override the workload's pool capacity in blocks (small profiling runs)")
     ap.add_argument("--update-kernel",
@@ -1159,6 +1162,72 @@ def measure_red_peaks(torch) -> dict:
     return out, cas_out
 
 
+def measure_atomic_probes(torch) -> dict:
+    """What two alternative update designs would pay, measured: atomic adds
+    to shared memory at random addresses of a 64 KB array (float and 32-bit
+    integer; lane operations per second and per SM per clock at the sampled
+    clock), and random 32-byte records (all five sums of a voxel in one
+    sector) reduced as a 4-wide plus a scalar reduction or as one 32-byte
+    bulk reduction from shared memory, into an L2-resident 32 MB footprint
+    (records per second).  Best of 5 launches each, CUDA events."""
+    import ctypes
+    from hash_blocked_tsdf_gb300 import _build
+    lib = ctypes.CDLL(_build.peaks_library_path())
+    lib.peak_smem_atomic.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_void_p]
+    lib.peak_smem_atomic.restype = ctypes.c_int
+    lib.peak_record_red.argtypes = [ctypes.c_void_p, ctypes.c_uint32, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_void_p]
+    lib.peak_record_red.restype = ctypes.c_int
+    props = torch.cuda.get_device_properties(torch.cuda.current_device())
+    sms = props.multi_processor_count
+    stream = torch.cuda.current_stream()
+
+    def best_ms(launch):
+        best = None
+        for _ in range(6):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            rc = launch()
+            b.record(stream)
+            assert rc == 0, rc
+            torch.cuda.synchronize()
+            ms = a.elapsed_time(b)
+            best = ms if best is None else min(best, ms)
+        return best
+
+    clk = ClockSampler(torch.cuda.current_device())
+    clk.start()
+    out = {}
+    blocks, reps = sms * 2, 4096
+    col = torch.zeros(blocks * 256, dtype=torch.float32, device="cuda")
+    smem = {}
+    for mode, name in ((0, "f32_atomic_add"), (1, "u32_atomic_add")):
+        ms = best_ms(lambda: lib.peak_smem_atomic(col.data_ptr(), mode, reps, blocks,
+                                                  stream.cuda_stream))
+        smem[name] = {"lane_ops_per_s": blocks * 256 * reps / (ms / 1e3)}
+    rec = {}
+    buf = torch.zeros((32 << 20) // 4, dtype=torch.float32, device="cuda")
+    n_records = buf.numel() // 8
+    for mode, name in ((0, "v4_plus_scalar"), (1, "bulk_32B_from_shared")):
+        rb, rr = sms * 8, 256
+        ms = best_ms(lambda: lib.peak_record_red(buf.data_ptr(), n_records, mode, rr, rb,
+                                                 stream.cuda_stream))
+        rec[name] = {"records_per_s": rb * 256 * rr / (ms / 1e3)}
+    c = clk.stop() or {}
+    mhz = c.get("sm_mhz") or 2070.0
+    for v in smem.values():
+        v["per_sm_per_clock"] = v["lane_ops_per_s"] / sms / (mhz * 1e6)
+    out["shared_memory_64KB"] = smem
+    out["records_32B_l2_32MB"] = rec
+    out["sm_mhz"] = mhz
+    out["sms"] = sms
+    del buf, col
+    torch.cuda.empty_cache()
+    return out
+
+
 def _profile_record(name: str, sources) -> dict:
     """Figures recorded in a committed ncu summary under profiles/, used only
     while the kernel's source is unchanged since the capture (matching hash)."""
@@ -1275,6 +1344,12 @@ def main():
         __graft_entry__.build()
         for rec in probe_depth_report(torch):
             print(json.dumps({"probe_depth": rec}), flush=True)
+        return
+    if args.probe_atomics:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build()
+        print(json.dumps({"probe_atomics": measure_atomic_probes(torch)}), flush=True)
         return
     if args.impl == "reference":
         run_reference(args)
