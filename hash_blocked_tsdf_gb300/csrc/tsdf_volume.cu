@@ -103,6 +103,10 @@ int fail(int code, const std::string& msg)
 int cuda_fail(cudaError_t e, const char* what)
 {
     g_last_error = std::string(what) + ": " + cudaGetErrorString(e);
+    // take a non-sticky error (a failed allocation, a bad launch argument)
+    // off the runtime's last-error slot, so that the launch check of a later
+    // call does not report it again
+    cudaGetLastError();
     return e == cudaErrorMemoryAllocation ? TSDF_ERR_OOM : TSDF_ERR_CUDA;
 }
 
