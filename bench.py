@@ -865,7 +865,7 @@ def run_ours(args):
                        "(peak_l2_resident: best pattern, 32 MB footprint)",
         "probe": red_peaks,
     }
-    # the binding resource: L2 reduction requests.  Sectors the kernel sends
+    # the closest memory-side ceiling: L2 reduction sectors the kernel sends
     # (ncu, per launch, while the source matches the capture) per second of
     # the live launch time, against the measured rate of scattered 4-wide
     # reductions into L2-resident lines (one sector each)
