@@ -143,6 +143,84 @@ __device__ __forceinline__ bool allocate_visible(const VolumeView& vol, const Ca
     return ray_visible(cam, vol.div, p, s, zc);
 }
 
+// (float)j for 0 <= j < 2^23, exactly and without a conversion: the float
+// whose significand holds j above 2^23, less 2^23.
+__device__ __forceinline__ float small_int_to_float(int j)
+{
+    return __fsub_rn(__int_as_float(0x4B000000 + j), 8388608.0f);
+}
+
+// The block index along one axis (origin o and direction e in voxel units)
+// of band step j, evaluated as band_voxel_unchecked evaluates the step's
+// voxel.
+__device__ __forceinline__ int axis_block(float o, float e, int j, float fhalf)
+{
+    const float fi = __fsub_rn(small_int_to_float(j), fhalf);
+    return __float2int_rd(__fadd_rn(o, __fmul_rn(fi, e))) >> 3;
+}
+
+// The band step at which the block index along one axis moves from a0 (at
+// step 0) to a1 = a0 +- 1 (at step `last`).  Each rounding of o + fi e is
+// monotone in fi, so the index is monotone in the step and moves exactly
+// once.  The step is estimated from where the ray meets the block boundary
+// and confirmed by evaluating the two steps around it exactly; -1 where the
+// estimate misses (an axis the ray barely moves along).
+__device__ __forceinline__ int axis_crossing(float o, float e, int a0, int a1, int last,
+                                             float fhalf)
+{
+    const bool up = a1 > a0;
+    const float boundary = (float)(8 * (up ? a1 : a0));   // |8 a| <= 2^23: exact
+    const float q = __fadd_rn(__fdividef(__fsub_rn(boundary, o), e), fhalf);
+    int t = up ? __float2int_ru(q) : min(__float2int_rd(q), last) + 1;
+    t = min(max(t, 1), last);
+    return axis_block(o, e, t - 1, fhalf) == a0 && axis_block(o, e, t, fhalf) == a1 ? t : -1;
+}
+
+// The allocate kernel's start mask for a short band (see allocate_kernel)
+// from the steps at which the ray's block changes, without visiting every
+// step: for rays whose band steps are all proven to pass the occlusion test
+// except perhaps the last, and whose block moves by at most one along each
+// axis over the band.  Then every proven step passes, so the proven steps
+// that start a block are step 0 and the steps where the block changes, and
+// the last step, when unproven, starts one if it enters another block and
+// passes the test.  Returns false (mask untouched) where the conditions fail
+// or a crossing estimate misses; the caller then walks step by step.
+template <bool kFast>
+__device__ __forceinline__ bool starts_from_crossings(const VolumeView& vol, const Camera& cam,
+                                                      const RayPoint& p, int steps, int j_proven,
+                                                      float fhalf, uint32_t& starts)
+{
+    const int last = steps - 1;
+    VoxelSample a, b;
+    band_voxel_unchecked(p, __fsub_rn(0.0f, fhalf), a);
+    band_voxel_unchecked(p, __fsub_rn(small_int_to_float(last), fhalf), b);
+    const int ax = a.ix >> 3, ay = a.iy >> 3, az = a.iz >> 3;
+    const int bx = b.ix >> 3, by = b.iy >> 3, bz = b.iz >> 3;
+    if (abs(bx - ax) > 1 || abs(by - ay) > 1 || abs(bz - az) > 1) return false;
+    uint32_t changes = 1u;                  // step 0 and the steps entering another block
+    if (bx != ax) {
+        const int t = axis_crossing(p.vx, p.ex, ax, bx, last, fhalf);
+        if (t < 0) return false;
+        changes |= 1u << t;
+    }
+    if (by != ay) {
+        const int t = axis_crossing(p.vy, p.ey, ay, by, last, fhalf);
+        if (t < 0) return false;
+        changes |= 1u << t;
+    }
+    if (bz != az) {
+        const int t = axis_crossing(p.vz, p.ez, az, bz, last, fhalf);
+        if (t < 0) return false;
+        changes |= 1u << t;
+    }
+    const uint32_t proven = j_proven >= 0 ? (2u << j_proven) - 1u : 0u;
+    uint32_t m = changes & proven;
+    if ((changes & ~proven) != 0u && allocate_visible<kFast, false>(vol, cam, p, nullptr, 0, 0, b))
+        m |= 1u << last;
+    starts = m;
+    return true;
+}
+
 // Block b of the grid covers 256 consecutive pixels (chunk b / n) of frame
 // b % n: the batch's frames are interleaved chunk by chunk.
 //
@@ -197,9 +275,14 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
         int j_proven = -1;
         if (!kReproject && sure.near && sure.i_max >= 0.0f)
             j_proven = half + (int)floorf(fminf(sure.i_max, fhalf));
+        // most rays: the mask from the band's block crossings; the others
+        // walk the band step by step
+        bool walked = !valid;
+        if (!kReproject && valid && all_in && j_proven >= steps - 2)
+            walked = starts_from_crossings<kFast>(vol, cam, p, steps, j_proven, fhalf, starts);
 #pragma unroll
         for (int j = 0; j < kShortBand; ++j) {
-            if (valid && j < steps) {
+            if (!walked && j < steps) {
                 VoxelSample s;
                 // the step j - half as a float: exact, with no integer
                 // conversion per step
