@@ -166,6 +166,38 @@ def test_parity_pose_not_exactly_a_rotation(torch_cuda, oracle_mod, scale):
     _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="per_sample")
 
 
+# For most rays the allocate kernel finds the band steps that start a block
+# from where the band crosses block boundaries (an estimate per axis,
+# confirmed by evaluating the steps on both sides exactly) instead of
+# visiting every step.  These frames put rays along the world axes and
+# nearly so (a direction component of a few 1e-5 makes the estimate
+# unreliable; the kernel then walks step by step), band samples exactly on
+# voxel and block boundaries (a voxel edge of 1/16 m and depths that are
+# exact in binary), and every band length from 1 to 9 steps.
+_AXIS_POSES = {
+    "identity": (np.eye(3), (0.0, 0.0, 0.0)),
+    "z_to_x": (np.array([[0.0, 0.0, 1.0], [1.0, 0.0, 0.0], [0.0, 1.0, 0.0]]), (0.5, -0.5, 1.0)),
+    "z_to_minus_y": (np.array([[1.0, 0.0, 0.0], [0.0, 0.0, -1.0], [0.0, 1.0, 0.0]]),
+                     (-1.0, 0.25, 0.0)),
+    "nearly_identity": (scenes.axis_angle(np.array([1.0, 2.0, 3.0]) / np.sqrt(14.0), 3e-5),
+                        (0.5, 0.5, -0.5)),
+}
+
+
+@pytest.mark.parametrize("ratio", [0.4, 1.0, 2.0, 3.0, 4.0])
+@pytest.mark.parametrize("pose_name", sorted(_AXIS_POSES))
+@pytest.mark.parametrize("depth_m", [2.0, 2.03125])
+def test_parity_axis_rays_on_block_boundaries(torch_cuda, oracle_mod, ratio, pose_name, depth_m):
+    R, t = _AXIS_POSES[pose_name]
+    pose = np.eye(4)
+    pose[:3, :3] = R
+    pose[:3, 3] = t
+    voxel = 0.0625
+    frames = _flat_frame(f"axis_{pose_name}_{ratio}_{depth_m}", 33, 33, 16.0, depth_m, pose,
+                         voxel, ratio * voxel, 4096, seed=5)
+    _full_parity(torch_cuda, oracle_mod, frames, strict=True, kernel="per_sample")
+
+
 @pytest.mark.parametrize("depth_m", [0.03, 0.045, 0.0488, 0.05, 0.06])
 def test_parity_surface_at_the_near_limit(torch_cuda, oracle_mod, depth_m):
     # voxel 1 cm, truncation 4 cm: the proof needs depth / voxel above about
