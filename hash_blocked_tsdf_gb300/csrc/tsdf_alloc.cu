@@ -243,16 +243,16 @@ __global__ void __launch_bounds__(kThreads) allocate_kernel(VolumeView vol,
     __shared__ ProbeStats st;
     if (kInstrument) init_probe_stats(&st);
 
-    const int f = blockIdx.x % fb.n;
-    const int chunk = blockIdx.x / fb.n;
+    const uint32_t chunk = divide_index(fb.by_n, blockIdx.x);
+    const int f = (int)(blockIdx.x - chunk * (uint32_t)fb.n);
     const Camera cam = fb.frame[f].cam;
     const float* depth = fb.frame[f].depth;
     const int n_pix = fb.width * fb.height;
-    const int pix = chunk * kThreads + threadIdx.x;
+    const int pix = (int)chunk * kThreads + (int)threadIdx.x;
     RayPoint p;
     bool valid = false;
     if (pix < n_pix) {
-        const int v = pix / fb.width;
+        const int v = (int)divide_index(fb.by_width, (uint32_t)pix);
         valid = back_project_pixel(vol, fb, cam, v, (size_t)pix, __ldg(depth + pix), p);
     }
     const int half = vol.band_half;
@@ -414,13 +414,12 @@ __global__ void __launch_bounds__(kThreads) integrate_fused_kernel(
     __shared__ float4 s_stage[kThreads];    // each warp's merge slots
     if (kInstrument) init_probe_stats(&st);
 
-    const int f = blockIdx.x % fb.n;
-    const int tile = blockIdx.x / fb.n;
-    const int tiles_x = (fb.width + 15) / 16;
+    const TilePos tp = tile_of_block(fb, fb.by_tiles16_x, blockIdx.x);
+    const int f = tp.f;
     const Camera cam = fb.frame[f].cam;
     const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31u);
-    const int u = (tile % tiles_x) * 16 + (w & 1) * 8 + (l & 7);
-    const int v = (tile / tiles_x) * 16 + (w >> 1) * 4 + (l >> 3);
+    const int u = tp.tx * 16 + (w & 1) * 8 + (l & 7);
+    const int v = tp.ty * 16 + (w >> 1) * 4 + (l >> 3);
     const bool inside = u < fb.width && v < fb.height;
     const float depth = inside ? __ldg(fb.frame[f].depth + (size_t)v * fb.width + u) : 0.0f;
     RayPoint p;

@@ -148,6 +148,21 @@ __device__ __forceinline__ bool back_project_pixel(const VolumeView& vol, const 
 // A pixel holds an observation when its depth is finite and positive.
 __device__ __forceinline__ bool valid_depth(float d) { return isfinite(d) && d > 0.0f; }
 
+// Frame f and tile (tx, ty) of block b of a tiled grid ordered tile-major,
+// frame-minor (b = tile * n + f, tile = ty * tiles_x + tx), by_tiles_x the
+// frame's width in tiles.
+struct TilePos {
+    int f, tx, ty;
+};
+
+__device__ __forceinline__ TilePos tile_of_block(const FrameBatch& fb,
+                                                 const IndexDivisor& by_tiles_x, uint32_t b)
+{
+    const uint32_t tile = divide_index(fb.by_n, b);
+    const uint32_t ty = divide_index(by_tiles_x, tile);
+    return {(int)(b - tile * (uint32_t)fb.n), (int)(tile - ty * by_tiles_x.d), (int)ty};
+}
+
 // Voxel indices in [-2^23, 2^23 - 1] <=> block indices in [-2^20, 2^20 - 1].
 constexpr unsigned kVoxelIndexBias = 1u << 23;
 constexpr unsigned kVoxelIndexSpan = 1u << 24;

@@ -110,10 +110,43 @@ struct FrameView {
 // and the host-batch staging two buffers of 64 frames.
 constexpr int kMaxBatch = 64;
 constexpr uint32_t kDenseListCapacity = 1u << 20;
+
+// Division of an index x < 2^31 by a divisor 1 <= d < 2^31 that is fixed for
+// a launch, by one multiply-high and a shift (T. Granlund and P. Montgomery,
+// "Division by invariant integers using multiplication", PLDI 1994).  With
+// l = ceil(log2 d) and m = ceil(2^(31+l) / d) (below 2^32: d > 2^(l-1)),
+//     x / d = floor(x m / 2^(31+l)) = umulhi(2x, m) >> l,
+// since x m / 2^(31+l) - x / d = x (m d - 2^(31+l)) / (d 2^(31+l)) lies in
+// [0, 1/d) for x < 2^31, too little to reach the next integer.  The kernels'
+// indices (grid positions, pixel and tile indices) stay below 2^31: frames
+// hold at most 2^30 pixels.
+struct IndexDivisor {
+    uint32_t d;
+    uint32_t m;
+    uint32_t l;
+};
+
+inline IndexDivisor make_index_divisor(uint32_t d)
+{
+    uint32_t l = 0;
+    while (l < 31 && (1u << l) < d) ++l;
+    const uint64_t p = 1ull << (31 + l);
+    return {d, (uint32_t)((p + d - 1) / d), l};
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t divide_index(const IndexDivisor& q, uint32_t x)
+{
+    return __umulhi(x << 1, q.m) >> q.l;
+}
+#endif
+
 struct FrameBatch {
     int n;
     int width;
     int height;
+    // n, width and the frame's widths in 16- and 8-pixel tiles, as divisors
+    IndexDivisor by_n, by_width, by_tiles16_x, by_tiles8_x;
     // The pixels' rays for the batch's intrinsics (build_rays): for pixel
     // (u, v), rays[v * width + u] = (dx, dy, dz, xn), the unit viewing ray
     // (xn, yn, 1) / |(xn, yn, 1)| and xn = (u - cx) / fx; ray_yn[v] =

@@ -65,16 +65,15 @@ template <bool kFast, bool kSparseOnly, bool kReproject>
 __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
                                                          const __grid_constant__ FrameBatch fb)
 {
-    const int f = blockIdx.x % fb.n;
-    const int tile = blockIdx.x / fb.n;
-    const int tiles_x = (fb.width + kTileW - 1) / kTileW;
+    const TilePos tp = tile_of_block(fb, fb.by_tiles16_x, blockIdx.x);
+    const int f = tp.f;
     const Camera cam = fb.frame[f].cam;
     // each warp takes an 8 x 4 pixel patch of the tile (8 warps: 2 across,
     // 4 down): a squarer footprint puts more of a warp's samples in common
     // voxel rows than a 16 x 2 strip
     const int w = (int)(threadIdx.x >> 5), l = (int)(threadIdx.x & 31u);
-    const int u = (tile % tiles_x) * kTileW + (w & 1) * 8 + (l & 7);
-    const int v = (tile / tiles_x) * kTileH + (w >> 1) * 4 + (l >> 3);
+    const int u = tp.tx * kTileW + (w & 1) * 8 + (l & 7);
+    const int v = tp.ty * kTileH + (w >> 1) * 4 + (l >> 3);
 
     const bool inside = u < fb.width && v < fb.height;
     const float depth = inside ? __ldg(fb.frame[f].depth + (size_t)v * fb.width + u) : 0.0f;
@@ -89,7 +88,8 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
             if (threadIdx.x == 0) {
                 const uint32_t pos = atomicAdd(vol.dense_count, 1u);
                 s_listed = pos < vol.dense_capacity ? 1u : 0u;
-                if (s_listed) vol.dense_list[pos] = (uint32_t)f << 24 | (uint32_t)tile;
+                if (s_listed)
+                    vol.dense_list[pos] = (uint32_t)f << 24 | divide_index(fb.by_n, blockIdx.x);
             }
             __syncthreads();
             if (s_listed) return;
@@ -178,6 +178,8 @@ __global__ void __launch_bounds__(kThreads) update_kernel(VolumeView vol,
 // Pre-reduced update.
 // ---------------------------------------------------------------------------
 constexpr int kRowTile = 8;                           // 8 x 8 pixel tiles
+static_assert(kTileW == 16 && kTileH == 16 && kRowTile == 8,
+              "the batch's tile divisors (by_tiles16_x, by_tiles8_x) assume these tiles");
 constexpr int kRowPix = kRowTile * kRowTile;          // 64
 constexpr int kRowParts = 3;                          // threads per pixel
 constexpr int kRowThreads = kRowPix * kRowParts;      // 192
@@ -357,16 +359,13 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) update_rows_kern
     const int t = threadIdx.x;
     uint32_t n_valid = 0, updates = 0, missed = 0;
     if (kAlways) {
-        const int f = blockIdx.x % fb.n;
-        const int tile = blockIdx.x / fb.n;
-        const int tiles_x = (fb.width + kRowTile - 1) / kRowTile;
-        rows_tile<kFast>(vol, fb, f, (tile % tiles_x) * kRowTile, (tile / tiles_x) * kRowTile, sm,
-                         n_valid, updates, missed);
+        const TilePos tp = tile_of_block(fb, fb.by_tiles8_x, blockIdx.x);
+        rows_tile<kFast>(vol, fb, tp.f, tp.tx * kRowTile, tp.ty * kRowTile, sm, n_valid, updates,
+                         missed);
     } else {
         const uint32_t n_listed = *vol.dense_count;
         if (n_listed == 0) return;          // nothing listed: nothing taken, nothing to reset
         const uint32_t n_items = 4u * min(n_listed, vol.dense_capacity);
-        const int tiles16_x = (fb.width + 15) / 16;
         uint32_t* s_item = sm + kOffCount + 2;
         for (;;) {
             if (t == 0) *s_item = atomicAdd(vol.dense_next, 1u);
@@ -376,9 +375,10 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) update_rows_kern
             if (j >= n_items) break;        // uniform over the block
             const uint32_t entry = vol.dense_list[j >> 2];
             const int f = (int)(entry >> 24);
-            const int tile16 = (int)(entry & 0xFFFFFFu);
-            const int u0 = (tile16 % tiles16_x) * 16 + (int)(j & 1u) * kRowTile;
-            const int v0 = (tile16 / tiles16_x) * 16 + (int)((j >> 1) & 1u) * kRowTile;
+            const uint32_t tile16 = entry & 0xFFFFFFu;
+            const uint32_t ty = divide_index(fb.by_tiles16_x, tile16);
+            const int u0 = (int)(tile16 - ty * fb.by_tiles16_x.d) * 16 + (int)(j & 1u) * kRowTile;
+            const int v0 = (int)ty * 16 + (int)((j >> 1) & 1u) * kRowTile;
             if (u0 < fb.width && v0 < fb.height)
                 rows_tile<kFast>(vol, fb, f, u0, v0, sm, n_valid, updates, missed);
         }

@@ -335,6 +335,10 @@ int batch_kernels(tsdf_volume* v, int n_frames, const float* depth, const float*
         fb.n = n_frames - first < kMaxBatch ? n_frames - first : kMaxBatch;
         fb.width = width;
         fb.height = height;
+        fb.by_n = make_index_divisor((uint32_t)fb.n);
+        fb.by_width = make_index_divisor((uint32_t)width);
+        fb.by_tiles16_x = make_index_divisor((uint32_t)((width + 15) / 16));
+        fb.by_tiles8_x = make_index_divisor((uint32_t)((width + 7) / 8));
         fb.rays = v->rays;
         fb.ray_yn = v->ray_yn;
         for (int f = 0; f < fb.n; ++f) {
